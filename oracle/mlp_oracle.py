@@ -1,0 +1,226 @@
+"""Plain, slow fp64 CPU oracle of the fused transformer MLP block.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py`` (its ``cpu_baseline`` leg and its ``--impl reference`` arm) may
+import this module.  The library (``activated_mlp_gemms_gb300``) never does,
+and nothing here imports the library: the two share no code.
+
+What is computed, and where the pages define it
+-----------------------------------------------
+* flash-swiglu-mlp 0.4.2 README (PyPI METADATA), opening paragraph: the
+  computed object is ``down_proj(silu(gate_proj(x)) * up_proj(x))``, with
+  ``gate_proj``/``up_proj`` weights ``[intermediate, hidden]`` and
+  ``down_proj`` weight ``[hidden, intermediate]`` (section "Module usage",
+  nn.Linear layout, no bias).
+* Same README, section "Falcon H1 style models": the scaled form
+  ``down_multiplier * down_proj(gate_multiplier * silu(gate_proj(x)) *
+  up_proj(x))``; both multipliers default to 1.0.
+* quack ``mlp.py`` (Tri Dao), ``MLP.forward`` fallback branch: fc1, then the
+  activation, then fc2; ``MLPRecomputeFunc.backward``: ``dW2 = dout^T
+  postact``, ``dx = dpreact W1``, ``dW1 = dpreact^T x``, and
+  ``_compute_weight_grad``: with ``fuse_grad_accum`` the weight gradient is
+  added in place into the existing fp32 ``.grad``.
+* modded-nanogpt ``track_1_short/model/gpt.py``, the ``ReLUSqrdMLP``
+  comment: ``relu(x @ W1.T)^2 @ W2.T`` (the non-gated relu_sq MLP).
+* quack ``mlp.py``, the ``Activation`` literal: ``gelu_tanh_approx`` (the
+  default activation of ``MLP``).  Its formula is not on the pages; the
+  published tanh approximation of GELU (Hendrycks & Gimpel, 2016) is used:
+  ``0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))``.
+
+Readings where the pages are silent (each also listed in the design notes):
+* ``gate_multiplier`` multiplies ``act(g)`` outside the activation, exactly
+  as the Falcon-H1 formula is written.
+* For the non-gated activations the same two multipliers apply with the
+  ``* up_proj(x)`` factor dropped: ``h = gm * act(x W1^T)``.
+* Inputs are the exact bf16 values widened to fp64; the oracle rounds
+  nothing to bf16 on the way (the GPU path stores G, U and the postact in
+  bf16; that difference lies inside the parity tolerance).
+
+Every array is a numpy float64 array, row-major, with the shapes
+x ``[M,H]``, Wg/Wu ``[I,H]``, Wd ``[H,I]``, dout ``[M,H]``.
+For the non-gated activations ``Wu`` is ``None`` and ``Wg`` plays ``W1``.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+ACTIVATIONS = ("swiglu", "relu_sq", "gelu_tanh_approx")
+GATED = ("swiglu",)
+
+# Hendrycks & Gimpel (2016), tanh approximation of GELU.
+_GELU_C = np.sqrt(2.0 / np.pi)
+_GELU_A = 0.044715
+
+
+def is_gated(act: str) -> bool:
+    if act not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {act!r}")
+    return act in GATED
+
+
+def _sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def act_fn(act: str, z):
+    """The activation applied to the gate (gated) or to the preact (non-gated)."""
+    z = np.asarray(z, dtype=np.float64)
+    if act == "swiglu":  # silu(z) = z * sigmoid(z)
+        return z * _sigmoid(z)
+    if act == "relu_sq":  # relu(z)^2
+        r = np.maximum(z, 0.0)
+        return r * r
+    if act == "gelu_tanh_approx":
+        t = np.tanh(_GELU_C * (z + _GELU_A * z ** 3))
+        return 0.5 * z * (1.0 + t)
+    raise ValueError(f"unknown activation {act!r}")
+
+
+def act_grad(act: str, z):
+    """d act / dz, differentiated by hand from ``act_fn``."""
+    z = np.asarray(z, dtype=np.float64)
+    if act == "swiglu":
+        s = _sigmoid(z)
+        return s * (1.0 + z * (1.0 - s))
+    if act == "relu_sq":
+        return 2.0 * np.maximum(z, 0.0)
+    if act == "gelu_tanh_approx":
+        t = np.tanh(_GELU_C * (z + _GELU_A * z ** 3))
+        dinner = _GELU_C * (1.0 + 3.0 * _GELU_A * z * z)
+        return 0.5 * (1.0 + t) + 0.5 * z * (1.0 - t * t) * dinner
+    raise ValueError(f"unknown activation {act!r}")
+
+
+def _check(x, Wg, Wu, Wd, act):
+    gated = is_gated(act)
+    M, H = x.shape
+    I = Wg.shape[0]
+    assert Wg.shape == (I, H), Wg.shape
+    assert Wd.shape == (H, I), Wd.shape
+    if gated:
+        assert Wu is not None and Wu.shape == (I, H)
+    else:
+        assert Wu is None, "non-gated activations take a single fc1 weight"
+    return gated
+
+
+def mlp_forward(x, Wg, Wu, Wd, act="swiglu", gate_mult=1.0, down_mult=1.0):
+    """Forward pass.  Returns a dict with ``out [M,H]`` and the intermediates
+    ``g`` (= gate preact, or the non-gated preact), ``u`` (None if
+    non-gated) and ``h`` (the postact ``gm*act(g)*u``, before ``down_mult``).
+    """
+    gated = _check(x, Wg, Wu, Wd, act)
+    g = x @ Wg.T  # gate_proj(x)   [M,I]
+    u = x @ Wu.T if gated else None  # up_proj(x)     [M,I]
+    h = gate_mult * act_fn(act, g)
+    if gated:
+        h = h * u
+    out = down_mult * (h @ Wd.T)  # down_proj(h)   [M,H]
+    return {"out": out, "g": g, "u": u, "h": h}
+
+
+def mlp_backward(dout, x, Wg, Wu, Wd, act="swiglu", gate_mult=1.0,
+                 down_mult=1.0, dW_prev=None):
+    """Backward pass of ``mlp_forward`` for the upstream gradient ``dout``.
+
+    Returns ``dx``, ``dWg``, ``dWu`` (None if non-gated) and ``dWd``.
+    ``dW_prev``, when given, is a dict ``{"dWg":…, "dWu":…, "dWd":…}`` of
+    pre-existing gradients; each returned weight gradient is then
+    ``dW_prev + dW`` (the fused fp32 accumulation of quack's
+    ``_compute_weight_grad``).
+    """
+    gated = _check(x, Wg, Wu, Wd, act)
+    fw = mlp_forward(x, Wg, Wu, Wd, act, gate_mult, down_mult)
+    g, u, h = fw["g"], fw["u"], fw["h"]
+    # out = dm * h Wd^T  =>  dL/dh = dm * dout Wd ,  dL/dWd = dm * dout^T h
+    dh = down_mult * (dout @ Wd)
+    dWd = down_mult * (dout.T @ h)
+    if gated:
+        # h = gm * act(g) * u
+        dG = gate_mult * dh * u * act_grad(act, g)
+        dU = gate_mult * dh * act_fn(act, g)
+        dx = dG @ Wg + dU @ Wu
+        dWg = dG.T @ x
+        dWu = dU.T @ x
+    else:
+        # h = gm * act(g)
+        dG = gate_mult * dh * act_grad(act, g)
+        dx = dG @ Wg
+        dWg = dG.T @ x
+        dWu = None
+    res = {"dx": dx, "dWg": dWg, "dWu": dWu, "dWd": dWd}
+    if dW_prev is not None:
+        for k in ("dWg", "dWu", "dWd"):
+            if res[k] is not None:
+                res[k] = dW_prev[k] + res[k]
+    return res
+
+
+# ---------------------------------------------------------------------------
+# Sampled evaluation at full sizes.  Each function is the same definition as
+# above, restricted to a subset of output rows or columns; nothing is
+# blocked, fused or reordered beyond selecting the rows the subset needs.
+# ---------------------------------------------------------------------------
+
+def sampled_token_rows(rows, dout, x, Wg, Wu, Wd, act="swiglu", gate_mult=1.0,
+                       down_mult=1.0):
+    """``out[rows]`` and ``dx[rows]`` for a list of token indices ``rows``.
+
+    A token's output and input gradient depend only on that token's row of
+    ``x`` and ``dout`` (the MLP is applied per token)."""
+    rows = np.asarray(rows)
+    fw = mlp_forward(x[rows], Wg, Wu, Wd, act, gate_mult, down_mult)
+    bw = mlp_backward(dout[rows], x[rows], Wg, Wu, Wd, act, gate_mult, down_mult)
+    return {"out": fw["out"], "dx": bw["dx"]}
+
+
+def sampled_inter_units(cols, dout, x, Wg, Wu, Wd, act="swiglu", gate_mult=1.0,
+                        down_mult=1.0, dW_prev=None):
+    """For a list of intermediate units ``cols`` (indices into I):
+    ``dWg[cols]``, ``dWu[cols]`` (rows of the ``[I,H]`` gradients) and
+    ``dWd[:, cols]`` (columns of the ``[H,I]`` gradient), each summed over
+    all M tokens.  Unit ``i`` only involves row ``i`` of Wg/Wu and column
+    ``i`` of Wd, so this is ``mlp_backward`` on the sub-network of those
+    units, whose ``dWd`` columns equal the full network's because ``dWd =
+    dm * dout^T h`` is column-separable in ``h``.
+
+    ``dW_prev`` (optional) holds the FULL pre-existing gradients; the
+    matching slices are added."""
+    cols = np.asarray(cols)
+    gated = is_gated(act)
+    sub = mlp_backward(dout, x, Wg[cols], Wu[cols] if gated else None,
+                       Wd[:, cols], act, gate_mult, down_mult)
+    res = {"dWg": sub["dWg"], "dWu": sub["dWu"], "dWd": sub["dWd"]}
+    if dW_prev is not None:
+        res["dWg"] = dW_prev["dWg"][cols] + res["dWg"]
+        if gated:
+            res["dWu"] = dW_prev["dWu"][cols] + res["dWu"]
+        res["dWd"] = dW_prev["dWd"][:, cols] + res["dWd"]
+    return res
+
+
+def rel_err(got, ref):
+    """The parity metric: max|got - ref| / max|ref| (0 if both are zero)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    num = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    den = float(np.max(np.abs(ref))) if ref.size else 0.0
+    if den == 0.0:
+        return num
+    return num / den
+
+
+def flops(M, H, I, act, mode):
+    """Multiply-add count x2 of the GEMMs a mode executes.
+
+    mode: 'fwd' | 'infer' | 'bwd' | 'bwd_recompute'.  (gated: fwd 6MHI, bwd
+    12MHI, +4MHI to recompute; non-gated: fwd 4MHI, bwd 8MHI, +2MHI.)"""
+    mhi = float(M) * H * I
+    g = is_gated(act)
+    if mode in ("fwd", "infer"):
+        return (6 if g else 4) * mhi
+    if mode == "bwd":
+        return (12 if g else 8) * mhi
+    if mode == "bwd_recompute":
+        return (16 if g else 10) * mhi
+    raise ValueError(mode)
