@@ -1,0 +1,225 @@
+"""Fused transformer MLP block on one GB300 (sm_103a): Python binding of libmlp.so.
+
+Argument marshalling only: every step of the forward and backward passes
+runs in the library's CUDA kernels.  PyTorch supplies device memory and
+streams.  The functions carry the names of the C ABI (include/mlp.h):
+
+    mlp_workspace_size, mlp_fwd, mlp_fwd_infer, mlp_bwd, mlp_bwd_recompute,
+    mlp_status_string, mlp_device_status, mlp_version
+
+Tensors are CUDA, contiguous, bf16 (fp32 for accumulated weight gradients),
+with x [M,H], Wg/Wu [I,H], Wd [H,I].  A missing library raises at the first
+call: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "ACTS", "MlpError", "Problem", "lib", "mlp_workspace_size", "mlp_fwd", "mlp_fwd_infer",
+    "mlp_bwd", "mlp_bwd_recompute", "mlp_status_string", "mlp_device_status", "mlp_version",
+    "MODE_FWD", "MODE_INFER", "MODE_BWD", "MODE_BWD_RECOMPUTE", "mlp_trace_enable",
+    "mlp_trace_read", "mlp_kernel_name",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmlp.so")
+
+ACTS = {"swiglu": 0, "relu_sq": 1, "gelu_tanh_approx": 2}
+MODE_FWD, MODE_INFER, MODE_BWD, MODE_BWD_RECOMPUTE = 0, 1, 2, 3
+
+
+class MlpError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {mlp_status_string(code)} ({code})")
+
+
+class Problem(ctypes.Structure):
+    """mlp_problem_t"""
+    _fields_ = [("M", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
+                ("act", ctypes.c_int), ("gate_mult", ctypes.c_float),
+                ("down_mult", ctypes.c_float)]
+
+
+_LIB = None
+_VP = ctypes.c_void_p
+
+
+def lib():
+    """Load libmlp.so (built in-tree by __graft_entry__.build())."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libmlp.so is not built ({LIB_PATH} missing); run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER(Problem)
+    L.mlp_workspace_size.argtypes = [P, ctypes.c_int]
+    L.mlp_workspace_size.restype = ctypes.c_size_t
+    L.mlp_fwd.argtypes = [P] + [_VP] * 7 + [_VP, ctypes.c_size_t, _VP]
+    L.mlp_fwd.restype = ctypes.c_int
+    L.mlp_fwd_infer.argtypes = [P] + [_VP] * 5 + [_VP, ctypes.c_size_t, _VP]
+    L.mlp_fwd_infer.restype = ctypes.c_int
+    L.mlp_bwd.argtypes = [P] + [_VP] * 11 + [ctypes.c_int, _VP, ctypes.c_size_t, _VP]
+    L.mlp_bwd.restype = ctypes.c_int
+    L.mlp_bwd_recompute.argtypes = [P] + [_VP] * 9 + [ctypes.c_int, _VP, ctypes.c_size_t, _VP]
+    L.mlp_bwd_recompute.restype = ctypes.c_int
+    L.mlp_status_string.argtypes = [ctypes.c_int]
+    L.mlp_status_string.restype = ctypes.c_char_p
+    L.mlp_device_status.argtypes = [_VP, _VP]
+    L.mlp_device_status.restype = ctypes.c_int
+    L.mlp_version.argtypes = []
+    L.mlp_version.restype = ctypes.c_char_p
+    L.mlp_trace_enable.argtypes = [ctypes.c_int]
+    L.mlp_trace_enable.restype = ctypes.c_int
+    L.mlp_trace_read.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_float),
+                                 ctypes.c_int]
+    L.mlp_trace_read.restype = ctypes.c_int
+    L.mlp_kernel_name.argtypes = [ctypes.c_int]
+    L.mlp_kernel_name.restype = ctypes.c_char_p
+    _LIB = L
+    return L
+
+
+def problem(M, H, I, act="swiglu", gate_mult=1.0, down_mult=1.0) -> Problem:
+    if act not in ACTS:
+        raise ValueError(f"unknown activation {act!r}; one of {list(ACTS)}")
+    return Problem(int(M), int(H), int(I), ACTS[act], float(gate_mult), float(down_mult))
+
+
+def _ptr(t, dtype=torch.bfloat16, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(rc, where):
+    if rc != 0:
+        raise MlpError(rc, where)
+
+
+def mlp_status_string(code: int) -> str:
+    return lib().mlp_status_string(int(code)).decode()
+
+
+def mlp_version() -> str:
+    return lib().mlp_version().decode()
+
+
+def mlp_workspace_size(prob: Problem, mode: int) -> int:
+    return int(lib().mlp_workspace_size(ctypes.byref(prob), int(mode)))
+
+
+def alloc_workspace(prob: Problem, mode: int, device=None) -> torch.Tensor:
+    n = mlp_workspace_size(prob, mode)
+    if n == 0:
+        raise MlpError(-1, "mlp_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(ws, prob, mode, device):
+    if ws is None:
+        ws = alloc_workspace(prob, mode, device)
+    if not (ws.is_cuda and ws.dtype == torch.uint8 and ws.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
+    return ws
+
+
+def mlp_fwd(prob: Problem, x, Wg, Wu, Wd, out, G_save=None, U_save=None, ws=None, stream=None):
+    """Training forward: out = down_mult * Wd (gate_mult * act(x Wg^T) * (x Wu^T)); optionally
+    stores the preacts G = x Wg^T, U = x Wu^T (bf16 [M,I]).  Returns the workspace used."""
+    ws = _ws(ws, prob, MODE_FWD, x.device)
+    rc = lib().mlp_fwd(ctypes.byref(prob), _ptr(x, name="x"), _ptr(Wg, name="Wg"),
+                       _ptr(Wu, name="Wu"), _ptr(Wd, name="Wd"), _ptr(out, name="out"),
+                       _ptr(G_save, name="G_save"), _ptr(U_save, name="U_save"),
+                       ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(rc, "mlp_fwd")
+    return ws
+
+
+def mlp_fwd_infer(prob: Problem, x, Wg, Wu, Wd, out, ws=None, stream=None):
+    """No-grad forward; stores no intermediates outside the workspace."""
+    ws = _ws(ws, prob, MODE_INFER, x.device)
+    rc = lib().mlp_fwd_infer(ctypes.byref(prob), _ptr(x, name="x"), _ptr(Wg, name="Wg"),
+                             _ptr(Wu, name="Wu"), _ptr(Wd, name="Wd"), _ptr(out, name="out"),
+                             ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(rc, "mlp_fwd_infer")
+    return ws
+
+
+def _wdt(fuse):
+    return torch.float32 if fuse else torch.bfloat16
+
+
+def mlp_bwd(prob: Problem, dout, x, Wg, Wu, Wd, G, U, dx=None, dWg=None, dWu=None, dWd=None,
+            fuse_grad_accum=False, ws=None, stream=None):
+    """Backward from saved preacts G, U (overwritten with dG, dU).  Outputs that are None
+    are skipped; weight gradients are bf16 (overwritten) or fp32 (+= in place) when
+    fuse_grad_accum."""
+    ws = _ws(ws, prob, MODE_BWD, x.device)
+    wd = _wdt(fuse_grad_accum)
+    rc = lib().mlp_bwd(ctypes.byref(prob), _ptr(dout, name="dout"), _ptr(x, name="x"),
+                       _ptr(Wg, name="Wg"), _ptr(Wu, name="Wu"), _ptr(Wd, name="Wd"),
+                       _ptr(G, name="G"), _ptr(U, name="U"), _ptr(dx, name="dx"),
+                       _ptr(dWg, wd, "dWg"), _ptr(dWu, wd, "dWu"), _ptr(dWd, wd, "dWd"),
+                       int(bool(fuse_grad_accum)), ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(rc, "mlp_bwd")
+    return ws
+
+
+def mlp_bwd_recompute(prob: Problem, dout, x, Wg, Wu, Wd, dx=None, dWg=None, dWu=None, dWd=None,
+                      fuse_grad_accum=False, ws=None, stream=None):
+    """Backward that recomputes the preacts from x (save-only-x training)."""
+    ws = _ws(ws, prob, MODE_BWD_RECOMPUTE, x.device)
+    wd = _wdt(fuse_grad_accum)
+    rc = lib().mlp_bwd_recompute(ctypes.byref(prob), _ptr(dout, name="dout"), _ptr(x, name="x"),
+                                 _ptr(Wg, name="Wg"), _ptr(Wu, name="Wu"), _ptr(Wd, name="Wd"),
+                                 _ptr(dx, name="dx"), _ptr(dWg, wd, "dWg"), _ptr(dWu, wd, "dWu"),
+                                 _ptr(dWd, wd, "dWd"), int(bool(fuse_grad_accum)),
+                                 ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(rc, "mlp_bwd_recompute")
+    return ws
+
+
+def mlp_device_status(ws, stream=None) -> int:
+    """Synchronises the stream and returns the device status word (0 = OK)."""
+    return int(lib().mlp_device_status(ws.data_ptr(), _stream(stream)))
+
+
+def mlp_trace_enable(on: bool = True) -> None:
+    """Bracket every kernel launch of later calls with CUDA events (timing)."""
+    _check(lib().mlp_trace_enable(1 if on else 0), "mlp_trace_enable")
+
+
+def mlp_kernel_name(tag: int) -> str:
+    return lib().mlp_kernel_name(int(tag)).decode()
+
+
+def mlp_trace_read(capacity: int = 4096):
+    """Returns [(kernel name, ms), ...] for the launches recorded since the
+    last read, in launch order, and frees the records."""
+    tags = (ctypes.c_int * capacity)()
+    ms = (ctypes.c_float * capacity)()
+    n = lib().mlp_trace_read(tags, ms, capacity)
+    if n < 0:
+        raise MlpError(n, "mlp_trace_read")
+    return [(mlp_kernel_name(tags[i]), float(ms[i])) for i in range(n)]

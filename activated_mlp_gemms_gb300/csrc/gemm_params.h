@@ -1,0 +1,77 @@
+// gemm_params.h -- launch parameters shared by the host code and the
+// persistent tcgen05 GEMM kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mlpk {
+
+// CTA tile: BM x (MMA N = 256) x BK, bf16 operands, fp32 accumulators.
+constexpr int BM = 128;
+constexpr int MMA_N = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;      // 16 KB
+constexpr int B_STAGE_BYTES = MMA_N * BK * 2;   // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int SCHED_SLOTS = 8;
+constexpr int NUM_THREADS = 192;                // producer, MMA, 4 epilogue warps
+constexpr int TMEM_COLS = 512;                  // two 256-column accumulators
+constexpr int MAX_PROBS = 3;
+constexpr int MAX_MAPS = 12;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 1024 /*barriers*/;
+
+// What the epilogue does with the accumulator tile.
+enum Epi : int {
+  EPI_GATED_FWD = 0,   // acc = [g | u] (128 + 128 cols): a = s*act(g)*u; optional G, U stores
+  EPI_ACT_FWD = 1,     // acc = p (256 cols): a = s*act(p); optional P store
+  EPI_DGATED = 2,      // acc = dout*Wd: dG = s*acc*u*act'(g), dU = s*acc*act(g), a = s*act(g)*u
+  EPI_DACT = 3,        // acc = dout*Wd: dP = s*acc*act'(p), a = s*act(p)
+  EPI_STORE_BF16 = 4,  // D = bf16(acc)
+  EPI_ACCUM_F32 = 5    // D += acc (fp32, atomic add; split-K safe)
+};
+
+enum Act : int { ACT_SILU = 0, ACT_RELU_SQ = 1, ACT_GELU_TANH = 2 };
+
+// One GEMM D[M,N] = sum_k A[m,k] B[n,k] of a (possibly grouped) launch.
+struct Prob {
+  int M, N;               // output rows / columns
+  int kb0, kb1;           // k-blocks of K-segment 0 and 1 (kb1 = 0: one segment)
+  int tiles_m, tiles_n;   // output tiles (tile N = 128 for EPI_GATED_FWD, else 256)
+  int ksplit, kper;       // split-K factor, k-blocks per split
+  int unit_begin, units;  // this problem's slice of the global work-unit range
+  int mapA0, mapB0;       // tensor maps of segment 0
+  int mapA1, mapB1;       // segment 1 (EPI_GATED_FWD: mapB1 = the up weight)
+  int ld;                 // row pitch (elements) of the epilogue's outputs and inputs
+  int pad_;
+  void* out0;
+  void* out1;
+  void* out2;
+  const void* in0;
+  const void* in1;
+};
+
+struct Params {  // 64-byte aligned through CUtensorMap
+  CUtensorMap maps[MAX_MAPS];
+  Prob prob[MAX_PROBS];
+  int nprob;
+  int total_units;
+  int act;
+  int group_m;            // L2 raster: tiles are visited in groups of group_m tile rows
+  float scale;            // gate_mult * down_mult (activation epilogues)
+  int pad_;
+  int* counter;           // dynamic tile scheduler counter, zero at launch
+  int* status;            // device status word (MLP_ERR_TIMEOUT on a bounded-wait expiry)
+  unsigned long long timeout_ns;
+};
+
+// Host-side launcher, explicitly instantiated in the kernel translation units.
+template <int EPI, bool A_MN, bool B_MN>
+cudaError_t launch_gemm(const Params& p, int grid, cudaStream_t stream, bool pdl);
+
+// Elementwise postact a = s*act(G)*U (U == nullptr: non-gated), n elements.
+cudaError_t launch_postact(const void* G, const void* U, void* a, long long n, int act,
+                           float scale, cudaStream_t stream, bool pdl);
+
+}  // namespace mlpk

@@ -1,0 +1,584 @@
+// mlp_api.cu -- the C ABI of libmlp.so (declared in include/mlp.h):
+// argument validation, workspace layout, TMA descriptor construction (with
+// a cache keyed by pointer/shape/box), and the launch sequences of the
+// forward, inference and backward passes.
+//
+// Launch sequences (every GEMM is the persistent tcgen05 kernel of gemm.cuh):
+//   mlp_fwd / mlp_fwd_infer
+//     1. gate/up GEMM, epilogue a = s*act(g)*u (+ G, U stores in training)
+//     2. down GEMM  out = a Wd^T            (s = gate_mult*down_mult is folded into a)
+//   mlp_bwd (the four stages of the flash-swiglu-mlp README, "Design notes")
+//     1. dgated GEMM  dout Wd  (K = H), epilogue dG, dU over G, U and the postact a
+//     2. dx GEMM      [dG|dU] [Wg;Wu]  (K = 2I, one accumulator)
+//     3. one grouped launch of the weight gradients dWg = dG^T x, dWu = dU^T x,
+//        dWd = dout^T a  (K = M), bf16 store or fp32 in-place accumulation
+//   mlp_bwd_recompute
+//     0. gate/up GEMM storing only G, U into the workspace, then as mlp_bwd.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "gemm_params.h"
+#include "mlp.h"
+
+using namespace mlpk;
+
+namespace {
+
+constexpr size_t CTRL_BYTES = 1024;  // status word + tile-scheduler counters
+constexpr int COUNTER_BASE = 16;     // counters start at int index 16 (byte 64)
+constexpr int MAX_COUNTERS = (CTRL_BYTES / 4) - COUNTER_BASE;
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encode_fn_ok() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+struct MapKey {
+  const void* ptr;
+  uint64_t inner, outer, stride;
+  uint32_t box0, box1;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && inner == o.inner && outer == o.outer && stride == o.stride &&
+           box0 == o.box0 && box1 == o.box1;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    size_t h = reinterpret_cast<size_t>(k.ptr);
+    h = h * 1000003u ^ k.inner;
+    h = h * 1000003u ^ k.outer;
+    h = h * 1000003u ^ k.stride;
+    h = h * 1000003u ^ (static_cast<size_t>(k.box0) << 16 | k.box1);
+    return h;
+  }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
+
+// 2-D bf16 tensor map over a row-major [outer, inner] array with row pitch
+// `pitch` elements, box {box0 (inner), box1 (outer)}, 128-byte swizzle,
+// out-of-bounds elements read as zero.
+bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch,
+              uint32_t box0, uint32_t box1) {
+  MapKey key{ptr, inner, outer, pitch, box0, box1};
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    auto it = g_map_cache.find(key);
+    if (it != g_map_cache.end()) {
+      *out = it->second;
+      return true;
+    }
+  }
+  if (!encode_fn_ok()) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch * 2};
+  cuuint32_t box[2] = {box0, box1};
+  cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  if (g_map_cache.size() > 4096) g_map_cache.clear();
+  g_map_cache.emplace(key, m);
+  *out = m;
+  return true;
+}
+
+// ------------------------------------------------------------ device info
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+unsigned long long wait_limit_ns() {
+  static unsigned long long v = [] {
+    const char* e = std::getenv("MLP_WAIT_TIMEOUT_MS");
+    unsigned long long ms = e ? std::strtoull(e, nullptr, 10) : 0ull;
+    if (ms == 0) ms = 2000;  // 2 s: far above any legitimate wait (tiles take microseconds)
+    return ms * 1000000ull;
+  }();
+  return v;
+}
+
+// ------------------------------------------------------------ launch builder
+// Operand roles: a K-major operand [rows, K] is loaded with boxes
+// {64, rows-per-box}; an MN-major operand [K, MN] with boxes {64, 64}.
+struct Gemm {
+  Params p;
+  int nmaps = 0;
+  bool ok = true;
+  Gemm(const mlp_problem_t& pr, int* counter, int* status) {
+    std::memset(&p, 0, sizeof(p));
+    p.act = pr.act;
+    p.scale = pr.gate_mult * pr.down_mult;
+    p.group_m = 16;
+    p.counter = counter;
+    p.status = status;
+    p.timeout_ns = wait_limit_ns();
+  }
+  // K-major operand: array [rows, K] (row pitch K), box {64, box_rows}
+  int kmajor(const void* ptr, int rows, int K, int box_rows) {
+    if (nmaps >= MAX_MAPS) { ok = false; return 0; }
+    if (!make_map(&p.maps[nmaps], ptr, K, rows, K, BK, box_rows)) ok = false;
+    return nmaps++;
+  }
+  // MN-major operand: array [K, MN] (row pitch MN), box {64, 64}
+  int mnmajor(const void* ptr, int K, int MN) {
+    if (nmaps >= MAX_MAPS) { ok = false; return 0; }
+    if (!make_map(&p.maps[nmaps], ptr, MN, K, MN, 64, BK)) ok = false;
+    return nmaps++;
+  }
+  Prob& add(int M, int N, int K0, int K1, int tile_n, int ksplit = 1) {
+    Prob& P = p.prob[p.nprob++];
+    P.M = M;
+    P.N = N;
+    P.kb0 = (K0 + BK - 1) / BK;
+    P.kb1 = (K1 + BK - 1) / BK;
+    P.tiles_m = (M + BM - 1) / BM;
+    P.tiles_n = (N + tile_n - 1) / tile_n;
+    const int kbt = P.kb0 + P.kb1;
+    if (ksplit < 1) ksplit = 1;
+    if (ksplit > kbt) ksplit = kbt;
+    P.kper = (kbt + ksplit - 1) / ksplit;
+    P.ksplit = (kbt + P.kper - 1) / P.kper;  // no empty splits
+    P.unit_begin = p.total_units;
+    P.units = P.tiles_m * P.tiles_n * P.ksplit;
+    p.total_units += P.units;
+    P.ld = N;
+    return P;
+  }
+  int grid() const {
+    int sms = num_sms();
+    int g = p.total_units < sms ? p.total_units : sms;
+    return g < 1 ? 1 : g;
+  }
+};
+
+struct Call {
+  cudaStream_t stream;
+  int* status;
+  int* counters;
+  int next_counter = 0;
+  int launches = 0;
+  int* counter() { return counters + (next_counter++ % MAX_COUNTERS); }
+  bool pdl() { return launches++ > 0; }  // the first kernel follows the control-block memset
+};
+
+int cuda_err(cudaError_t e) { return e == cudaSuccess ? MLP_OK : MLP_ERR_CUDA; }
+
+// ------------------------------------------------------------ tracing
+// When enabled, every kernel launch is bracketed by a pair of CUDA events on
+// its stream; mlp_trace_read returns (kernel tag, milliseconds) per launch.
+struct TraceRec {
+  int tag;
+  cudaEvent_t a, b;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t trace_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+template <class F>
+int traced(int tag, cudaStream_t s, F&& launch) {
+  std::unique_lock<std::mutex> lk(g_trace_mu);
+  if (!g_trace_on) {
+    lk.unlock();
+    return cuda_err(launch());
+  }
+  TraceRec r{tag, trace_event(), trace_event()};
+  if (!r.a || !r.b) return MLP_ERR_CUDA;
+  if (cudaEventRecord(r.a, s) != cudaSuccess) return MLP_ERR_CUDA;
+  cudaError_t e = launch();
+  if (cudaEventRecord(r.b, s) != cudaSuccess) return MLP_ERR_CUDA;
+  g_trace.push_back(r);
+  return cuda_err(e);
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+int run(Gemm& g, Call& c, int tag) {
+  if (!g.ok) return MLP_ERR_CUDA;
+  if (g.p.total_units == 0) return MLP_OK;
+  const bool pdl = c.pdl();
+  return traced(tag, c.stream, [&] { return launch_gemm<EPI, A_MN, B_MN>(g.p, g.grid(), c.stream, pdl); });
+}
+
+// ------------------------------------------------------------ validation
+int check_problem(const mlp_problem_t* p) {
+  if (!p) return MLP_ERR_INVALID_ARG;
+  if (p->M <= 0 || p->H <= 0 || p->I <= 0) return MLP_ERR_INVALID_ARG;
+  if (p->act < MLP_ACT_SWIGLU || p->act > MLP_ACT_GELU_TANH) return MLP_ERR_INVALID_ARG;
+  if (!std::isfinite(p->gate_mult) || !std::isfinite(p->down_mult)) return MLP_ERR_INVALID_ARG;
+  if (p->H % 8 || p->I % 8) return MLP_ERR_ALIGNMENT;
+  // TMA coordinates and tile counts are 32-bit
+  if ((long long)p->M * p->I >= (1LL << 40) || (long long)p->M * p->H >= (1LL << 40))
+    return MLP_ERR_UNSUPPORTED;
+  return MLP_OK;
+}
+
+bool gated(const mlp_problem_t* p) { return p->act == MLP_ACT_SWIGLU; }
+
+size_t inter_bytes(const mlp_problem_t* p) { return round256((size_t)p->M * p->I * 2); }
+
+size_t ws_size(const mlp_problem_t* p, int mode) {
+  size_t n = CTRL_BYTES + inter_bytes(p);  // control block + postact a
+  if (mode == MLP_MODE_BWD_RECOMPUTE) n += inter_bytes(p) * (gated(p) ? 2 : 1);
+  return n;
+}
+
+// Required pointer present and 16-byte aligned; optional pointer aligned if present.
+int need(const void* ptr) {
+  if (!ptr) return MLP_ERR_INVALID_ARG;
+  return aligned16(ptr) ? MLP_OK : MLP_ERR_ALIGNMENT;
+}
+int opt(const void* ptr) { return (!ptr || aligned16(ptr)) ? MLP_OK : MLP_ERR_ALIGNMENT; }
+
+#define MLP_TRY(...)                 \
+  do {                               \
+    int _rc = (__VA_ARGS__);         \
+    if (_rc != MLP_OK) return _rc;   \
+  } while (0)
+
+int check_weights(const mlp_problem_t* p, const void* Wg, const void* Wu, const void* Wd) {
+  MLP_TRY(need(Wg));
+  MLP_TRY(need(Wd));
+  if (gated(p)) {
+    MLP_TRY(need(Wu));
+  } else if (Wu) {
+    return MLP_ERR_INVALID_ARG;  // non-gated activations take one fc1 weight
+  }
+  return MLP_OK;
+}
+
+int check_ws(const mlp_problem_t* p, int mode, const void* ws, size_t ws_bytes) {
+  if (!ws) return MLP_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MLP_ERR_ALIGNMENT;
+  if (ws_bytes < ws_size(p, mode)) return MLP_ERR_WORKSPACE_TOO_SMALL;
+  return MLP_OK;
+}
+
+int begin_call(Call& c, void* ws, void* stream) {
+  c.stream = static_cast<cudaStream_t>(stream);
+  c.status = static_cast<int*>(ws);
+  c.counters = static_cast<int*>(ws) + COUNTER_BASE;
+  return cuda_err(cudaMemsetAsync(ws, 0, CTRL_BYTES, c.stream));
+}
+
+// gate/up (or fc1) GEMM with the activation epilogue.
+//   a_out: postact (may be null), G_out/U_out: preact stores (may be null)
+int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* Wg, const void* Wu,
+                   void* a_out, void* G_out, void* U_out) {
+  Gemm g(*p, c.counter(), c.status);
+  const int mA = g.kmajor(x, p->M, p->H, BM);
+  if (gated(p)) {
+    const int mG = g.kmajor(Wg, p->I, p->H, 128);
+    const int mU = g.kmajor(Wu, p->I, p->H, 128);
+    Prob& P = g.add(p->M, p->I, p->H, 0, 128);
+    P.mapA0 = mA;
+    P.mapB0 = mG;
+    P.mapB1 = mU;
+    P.out0 = a_out;
+    P.out1 = G_out;
+    P.out2 = U_out;
+    return run<EPI_GATED_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
+  }
+  const int mW = g.kmajor(Wg, p->I, p->H, MMA_N);
+  Prob& P = g.add(p->M, p->I, p->H, 0, MMA_N);
+  P.mapA0 = mA;
+  P.mapB0 = mW;
+  P.out0 = a_out;
+  P.out1 = G_out;
+  return run<EPI_ACT_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
+}
+
+// out = a Wd^T
+int launch_down(const mlp_problem_t* p, Call& c, const void* a, const void* Wd, void* out) {
+  Gemm g(*p, c.counter(), c.status);
+  const int mA = g.kmajor(a, p->M, p->I, BM);
+  const int mB = g.kmajor(Wd, p->H, p->I, MMA_N);
+  Prob& P = g.add(p->M, p->H, p->I, 0, MMA_N);
+  P.mapA0 = mA;
+  P.mapB0 = mB;
+  P.out0 = out;
+  return run<EPI_STORE_BF16, false, false>(g, c, MLP_KERNEL_DOWN);
+}
+
+int forward(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu, const void* Wd,
+            void* out, void* G_save, void* U_save, void* ws, size_t ws_bytes, void* stream,
+            int mode) {
+  MLP_TRY(check_problem(p));
+  MLP_TRY(need(x));
+  MLP_TRY(check_weights(p, Wg, Wu, Wd));
+  MLP_TRY(need(out));
+  MLP_TRY(opt(G_save));
+  MLP_TRY(opt(U_save));
+  if (!gated(p) && U_save) return MLP_ERR_INVALID_ARG;
+  MLP_TRY(check_ws(p, mode, ws, ws_bytes));
+  Call c;
+  MLP_TRY(begin_call(c, ws, stream));
+  void* a = static_cast<char*>(ws) + CTRL_BYTES;
+  MLP_TRY(launch_fwd_act(p, c, x, Wg, Wu, a, G_save, U_save));
+  return launch_down(p, c, a, Wd, out);
+}
+
+int backward(const mlp_problem_t* p, const void* dout, const void* x, const void* Wg,
+             const void* Wu, const void* Wd, void* G, void* U, void* dx, void* dWg, void* dWu,
+             void* dWd, int fuse, void* ws, size_t ws_bytes, void* stream, bool recompute) {
+  MLP_TRY(check_problem(p));
+  if (fuse != 0 && fuse != 1) return MLP_ERR_INVALID_ARG;
+  MLP_TRY(need(dout));
+  MLP_TRY(need(x));
+  MLP_TRY(check_weights(p, Wg, Wu, Wd));
+  if (!recompute) {
+    MLP_TRY(need(G));
+    if (gated(p)) {
+      MLP_TRY(need(U));
+    } else if (U) {
+      return MLP_ERR_INVALID_ARG;
+    }
+  }
+  MLP_TRY(opt(dx));
+  MLP_TRY(opt(dWg));
+  MLP_TRY(opt(dWu));
+  MLP_TRY(opt(dWd));
+  if (!gated(p) && dWu) return MLP_ERR_INVALID_ARG;
+  const int mode = recompute ? MLP_MODE_BWD_RECOMPUTE : MLP_MODE_BWD;
+  MLP_TRY(check_ws(p, mode, ws, ws_bytes));
+
+  const bool need_dact = dx || dWg || dWu;
+  if (!need_dact && !dWd) return MLP_OK;  // nothing requested
+
+  Call c;
+  MLP_TRY(begin_call(c, ws, stream));
+  char* base = static_cast<char*>(ws) + CTRL_BYTES;
+  void* a = base;  // postact (input of dWd)
+  if (recompute) {
+    G = base + inter_bytes(p);
+    U = gated(p) ? base + 2 * inter_bytes(p) : nullptr;
+    // stage 0: recompute the preacts (quack MLPRecomputeFunc: preact = x W1^T)
+    MLP_TRY(launch_fwd_act(p, c, x, Wg, Wu, nullptr, G, U));
+  }
+  const int M = p->M, H = p->H, I = p->I;
+
+  if (need_dact) {
+    // stage 1: dh = dout Wd (K = H); epilogue writes dG, dU over G, U and the postact a
+    Gemm g(*p, c.counter(), c.status);
+    const int mA = g.kmajor(dout, M, H, BM);
+    const int mB = g.mnmajor(Wd, H, I);  // Wd [H,I]: B(n=i, k=h) is N-contiguous
+    Prob& P = g.add(M, I, H, 0, MMA_N);
+    P.mapA0 = mA;
+    P.mapB0 = mB;
+    P.in0 = G;
+    P.in1 = U;
+    P.out0 = G;
+    P.out1 = U;
+    P.out2 = dWd ? a : nullptr;
+    MLP_TRY(gated(p) ? run<EPI_DGATED, false, true>(g, c, MLP_KERNEL_DGATED)
+                     : run<EPI_DACT, false, true>(g, c, MLP_KERNEL_DGATED));
+  } else {
+    // only dWd requested: rebuild the postact without the derivative
+    const bool pdl = c.pdl();
+    MLP_TRY(traced(MLP_KERNEL_POSTACT, c.stream, [&] {
+      return launch_postact(G, U, a, (long long)M * I, p->act, p->gate_mult * p->down_mult,
+                            c.stream, pdl);
+    }));
+  }
+  void* dG = G;
+  void* dU = U;
+
+  if (dx) {
+    // stage 2: dx = [dG|dU] [Wg;Wu], one accumulator over K = 2I (non-gated: K = I)
+    Gemm g(*p, c.counter(), c.status);
+    const int mA0 = g.kmajor(dG, M, I, BM);
+    const int mB0 = g.mnmajor(Wg, I, H);  // Wg [I,H]: B(n=h, k=i) is N-contiguous
+    int mA1 = 0, mB1 = 0;
+    if (gated(p)) {
+      mA1 = g.kmajor(dU, M, I, BM);
+      mB1 = g.mnmajor(Wu, I, H);
+    }
+    Prob& P = g.add(M, H, I, gated(p) ? I : 0, MMA_N);
+    P.mapA0 = mA0;
+    P.mapB0 = mB0;
+    P.mapA1 = mA1;
+    P.mapB1 = mB1;
+    P.out0 = dx;
+    MLP_TRY((run<EPI_STORE_BF16, false, true>(g, c, MLP_KERNEL_DX)));
+  }
+
+  if (dWg || dWu || dWd) {
+    // stage 3: weight gradients in one grouped launch, reduced over the M tokens:
+    //   dWg = dG^T x, dWu = dU^T x  ([I,H])   dWd = dout^T a  ([H,I])
+    Gemm g(*p, c.counter(), c.status);
+    struct W { const void* A; int rows; const void* B; int cols; void* out; };
+    W list[3];
+    int n = 0;
+    if (dWg) list[n++] = {dG, I, x, H, dWg};
+    if (dWu) list[n++] = {dU, I, x, H, dWu};
+    if (dWd) list[n++] = {dout, H, a, I, dWd};
+    long long tiles = 0;
+    for (int i = 0; i < n; ++i)
+      tiles += (long long)((list[i].rows + BM - 1) / BM) * ((list[i].cols + MMA_N - 1) / MMA_N);
+    // split the token reduction when the output tiles cannot fill the GPU
+    // (fp32 accumulation only: partial sums meet through atomic adds)
+    int ksplit = 1;
+    const int sms = num_sms();
+    const int kb = (M + BK - 1) / BK;
+    if (fuse && tiles < sms) {
+      ksplit = (int)(sms / tiles);
+      while (ksplit > 1 && kb / ksplit < 8) --ksplit;
+    }
+    for (int i = 0; i < n; ++i) {
+      const int mA = g.mnmajor(list[i].A, M, list[i].rows);
+      const int mB = g.mnmajor(list[i].B, M, list[i].cols);
+      Prob& P = g.add(list[i].rows, list[i].cols, M, 0, MMA_N, ksplit);
+      P.mapA0 = mA;
+      P.mapB0 = mB;
+      P.out0 = list[i].out;
+    }
+    if (fuse) {
+      MLP_TRY((run<EPI_ACCUM_F32, true, true>(g, c, MLP_KERNEL_WGRAD)));
+    } else {
+      MLP_TRY((run<EPI_STORE_BF16, true, true>(g, c, MLP_KERNEL_WGRAD)));
+    }
+  }
+  return MLP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mlp_workspace_size(const mlp_problem_t* p, int mode) {
+  if (check_problem(p) != MLP_OK) return 0;
+  if (mode < MLP_MODE_FWD || mode > MLP_MODE_BWD_RECOMPUTE) return 0;
+  return ws_size(p, mode);
+}
+
+int mlp_fwd(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu, const void* Wd,
+            void* out, void* G_save, void* U_save, void* ws, size_t ws_bytes, void* stream) {
+  return forward(p, x, Wg, Wu, Wd, out, G_save, U_save, ws, ws_bytes, stream, MLP_MODE_FWD);
+}
+
+int mlp_fwd_infer(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu,
+                  const void* Wd, void* out, void* ws, size_t ws_bytes, void* stream) {
+  return forward(p, x, Wg, Wu, Wd, out, nullptr, nullptr, ws, ws_bytes, stream, MLP_MODE_INFER);
+}
+
+int mlp_bwd(const mlp_problem_t* p, const void* dout, const void* x, const void* Wg,
+            const void* Wu, const void* Wd, void* G, void* U, void* dx, void* dWg, void* dWu,
+            void* dWd, int fuse_grad_accum, void* ws, size_t ws_bytes, void* stream) {
+  return backward(p, dout, x, Wg, Wu, Wd, G, U, dx, dWg, dWu, dWd, fuse_grad_accum, ws, ws_bytes,
+                  stream, false);
+}
+
+int mlp_bwd_recompute(const mlp_problem_t* p, const void* dout, const void* x, const void* Wg,
+                      const void* Wu, const void* Wd, void* dx, void* dWg, void* dWu, void* dWd,
+                      int fuse_grad_accum, void* ws, size_t ws_bytes, void* stream) {
+  return backward(p, dout, x, Wg, Wu, Wd, nullptr, nullptr, dx, dWg, dWu, dWd, fuse_grad_accum,
+                  ws, ws_bytes, stream, true);
+}
+
+const char* mlp_status_string(int s) {
+  switch (s) {
+    case MLP_OK: return "MLP_OK";
+    case MLP_ERR_INVALID_ARG: return "MLP_ERR_INVALID_ARG";
+    case MLP_ERR_ALIGNMENT: return "MLP_ERR_ALIGNMENT";
+    case MLP_ERR_UNSUPPORTED: return "MLP_ERR_UNSUPPORTED";
+    case MLP_ERR_WORKSPACE_TOO_SMALL: return "MLP_ERR_WORKSPACE_TOO_SMALL";
+    case MLP_ERR_CUDA: return "MLP_ERR_CUDA";
+    case MLP_ERR_TIMEOUT: return "MLP_ERR_TIMEOUT";
+    default: return "MLP_ERR_UNKNOWN";
+  }
+}
+
+int mlp_device_status(const void* ws, void* stream) {
+  if (!ws) return MLP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MLP_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLP_ERR_CUDA;
+  return v;
+}
+
+const char* mlp_version(void) { return "0.1.0"; }
+
+int mlp_trace_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = on != 0;
+  return MLP_OK;
+}
+
+int mlp_trace_read(int* tags, float* ms, int capacity) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  int n = 0;
+  int rc = MLP_OK;
+  for (auto& r : g_trace) {
+    float t = -1.0f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      rc = MLP_ERR_CUDA;
+    if (n < capacity && tags && ms) {
+      tags[n] = r.tag;
+      ms[n] = t;
+    }
+    ++n;
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_trace.clear();
+  if (rc != MLP_OK) return rc;
+  return n < capacity ? n : capacity;
+}
+
+const char* mlp_kernel_name(int tag) {
+  switch (tag) {
+    case MLP_KERNEL_GATE_UP: return "gate_up_act";
+    case MLP_KERNEL_DOWN: return "down_proj";
+    case MLP_KERNEL_DGATED: return "dgated";
+    case MLP_KERNEL_DX: return "dx";
+    case MLP_KERNEL_WGRAD: return "wgrad";
+    case MLP_KERNEL_POSTACT: return "postact";
+    default: return "unknown";
+  }
+}
+
+}  // extern "C"

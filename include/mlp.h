@@ -1,0 +1,200 @@
+/*
+ * mlp.h -- C ABI of libmlp.so, the fused transformer MLP block on one GB300
+ * (sm_103a) GPU, forward and backward.
+ *
+ * The operation (bf16 storage, fp32 accumulation, row-major everywhere):
+ *
+ *   g   = x Wg^T                    [M,I]   gate_proj(x)
+ *   u   = x Wu^T                    [M,I]   up_proj(x)        (gated only)
+ *   h   = gate_mult * act(g) * u    [M,I]   (non-gated: gate_mult * act(g))
+ *   out = down_mult * h Wd^T        [M,H]   down_proj(h)
+ *
+ * with x [M,H], Wg/Wu [I,H] and Wd [H,I] in nn.Linear layout, no bias.
+ * Sources:
+ *   - flash-swiglu-mlp 0.4.2 README (PyPI METADATA), opening paragraph: the
+ *     computed object down_proj(silu(gate_proj(x)) * up_proj(x)); section
+ *     "Falcon H1 style models": the scaled form down_multiplier *
+ *     down_proj(gate_multiplier * silu(gate_proj(x)) * up_proj(x)), both
+ *     multipliers defaulting to 1.0; section "Supported configurations":
+ *     no bias, contiguous [B,S,dim] input, rows 16-byte aligned (dim and
+ *     hidden_dim multiples of 8 in bf16); section "Design notes": the
+ *     backward in four stages with dG/dU written over G/U, the merged
+ *     dW_g/dW_u GEMM and the single-accumulator dI; separate train and
+ *     inference paths, the latter storing no G/U.
+ *   - quack mlp.py (Tri Dao): MLP(activation=...) with the Activation
+ *     literal (gelu_tanh_approx, relu_sq, swiglu, ...); mlp_func(x, weight1,
+ *     weight2, activation, fuse_grad_accum, tuned, recompute);
+ *     MLPRecomputeFunc (saves only x, recomputes preact = x W1^T in
+ *     backward); _compute_weight_grad (fuse_grad_accum: W.grad += dout^T x
+ *     in place, else a fresh gradient in the weight dtype); the
+ *     needs_input_grad logic that skips unrequested gradients.
+ *   - modded-nanogpt track_1_short/model/gpt.py, ReLUSqrdMLP:
+ *     relu(x W1^T)^2 W2^T.
+ *
+ * Conventions shared by every entry point
+ *   - Ownership: the caller allocates and owns every buffer (device memory);
+ *     the library never allocates or frees device memory.  The only state it
+ *     keeps is per-device properties and a cache of TMA descriptors keyed by
+ *     (pointer, shape, box).
+ *   - Streams: all work is enqueued on `stream` (a cudaStream_t, or NULL for
+ *     the legacy default stream); nothing synchronises, except
+ *     mlp_device_status.
+ *   - Pointers marked bf16 hold __nv_bfloat16 values; every device pointer
+ *     must be 16-byte aligned.  M, H, I > 0; H and I multiples of 8.
+ *   - Return value: MLP_OK (0) or a negative mlp_status_t.  Arguments are
+ *     validated before anything is enqueued; on a validation error nothing
+ *     is enqueued and outputs are untouched.
+ *   - Workspace: `ws` is caller-owned device scratch of at least
+ *     mlp_workspace_size(p, mode) bytes, 256-byte aligned.  Its first bytes
+ *     hold the device status word and the tile-scheduler counters; every
+ *     call clears them on the stream before its kernels run.  Calls that
+ *     share one workspace must be ordered (same stream, or synchronised).
+ *   - Device-side errors (a bounded wait that expired) are recorded in the
+ *     workspace status word; read it with mlp_device_status.
+ */
+#ifndef MLP_GB300_H
+#define MLP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLP_OK = 0,
+  MLP_ERR_INVALID_ARG = -1,        /* null required pointer, M/H/I <= 0, bad enum, NULL problem */
+  MLP_ERR_ALIGNMENT = -2,          /* H or I not a multiple of 8, or a pointer not 16-byte aligned */
+  MLP_ERR_UNSUPPORTED = -3,        /* a combination the library does not implement */
+  MLP_ERR_WORKSPACE_TOO_SMALL = -4,/* ws_bytes < mlp_workspace_size(p, mode) */
+  MLP_ERR_CUDA = -5,               /* a CUDA runtime/driver call or a launch failed */
+  MLP_ERR_TIMEOUT = -6             /* device side: a bounded wait expired (see mlp_device_status) */
+} mlp_status_t;
+
+/* Activation (quack mlp.py, the Activation literal).  SWIGLU is the gated
+ * case (act = silu on the gate, times the up projection); RELU_SQ
+ * (relu(z)^2) and GELU_TANH (the tanh approximation of GELU,
+ * 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))) are non-gated: there is
+ * one fc1 weight, passed as Wg, and Wu must be NULL. */
+typedef enum {
+  MLP_ACT_SWIGLU = 0,
+  MLP_ACT_RELU_SQ = 1,
+  MLP_ACT_GELU_TANH = 2
+} mlp_act_t;
+
+/* Problem description.  M = tokens (batch * sequence), H = hidden (model
+ * dim), I = intermediate.  gate_mult and down_mult are the Falcon-H1
+ * multipliers (1.0 for Llama-style MLPs). */
+typedef struct {
+  int M, H, I;
+  int act;          /* mlp_act_t */
+  float gate_mult;
+  float down_mult;
+} mlp_problem_t;
+
+/* Workspace modes for mlp_workspace_size. */
+typedef enum {
+  MLP_MODE_FWD = 0,
+  MLP_MODE_INFER = 1,
+  MLP_MODE_BWD = 2,
+  MLP_MODE_BWD_RECOMPUTE = 3
+} mlp_mode_t;
+
+/* Bytes of workspace a call in `mode` needs for problem `p` (0 on invalid
+ * arguments).  FWD/INFER/BWD: the control block plus one bf16 [M,I] buffer
+ * (the postact); BWD_RECOMPUTE: plus the recomputed preacts, two bf16
+ * [M,I] buffers when gated, one when not. */
+size_t mlp_workspace_size(const mlp_problem_t* p, int mode);
+
+/* Training forward (flash-swiglu-mlp README "Design notes", forward fusion;
+ * quack mlp.py mlp_func with store_preact).
+ *   x      bf16 [M,H]  in
+ *   Wg     bf16 [I,H]  in   (non-gated: W1)
+ *   Wu     bf16 [I,H]  in   (NULL when non-gated)
+ *   Wd     bf16 [H,I]  in
+ *   out    bf16 [M,H]  out
+ *   G_save bf16 [M,I]  out, optional: the gate preact x Wg^T (non-gated: x W1^T)
+ *   U_save bf16 [M,I]  out, optional: the up preact x Wu^T (NULL when non-gated)
+ * Pass G_save/U_save as NULL for the recompute mode (save only x).  The
+ * bf16 values written to `out` are bitwise identical to mlp_fwd_infer's. */
+int mlp_fwd(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu,
+            const void* Wd, void* out, void* G_save, void* U_save,
+            void* ws, size_t ws_bytes, void* stream);
+
+/* No-grad inference forward (flash-swiglu-mlp README, "inference path":
+ * stores no G/U, only the transient postact in the workspace).
+ * Arguments as in mlp_fwd. */
+int mlp_fwd_infer(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu,
+                  const void* Wd, void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward from saved preacts (flash-swiglu-mlp README "Design notes",
+ * the four backward stages; quack mlp.py backward of linear_gated_func /
+ * gated_linear_func).
+ *   dout  bf16 [M,H]  in   upstream gradient of out
+ *   x, Wg, Wu, Wd     in   as in mlp_fwd
+ *   G, U  bf16 [M,I]  in/out: in = the saved preacts from mlp_fwd; out =
+ *                     overwritten with dG, dU (the gradients w.r.t. the
+ *                     preacts), as flash-swiglu does to lower peak memory.
+ *                     They are left untouched when dx, dWg and dWu are all
+ *                     NULL.  U is NULL when non-gated.
+ *   dx    bf16 [M,H]  out, or NULL to skip
+ *   dWg, dWu [I,H], dWd [H,I]: each NULL to skip.  fuse_grad_accum = 0:
+ *                     bf16, overwritten with the gradient.  fuse_grad_accum
+ *                     = 1: fp32, dW += gradient in place (quack
+ *                     _compute_weight_grad with fuse_grad_accum).
+ * When only dWd is requested, the postact is rebuilt from G/U without the
+ * activation derivative (quack MLPRecomputeFunc.backward, "only dW2 needed"). */
+int mlp_bwd(const mlp_problem_t* p, const void* dout, const void* x, const void* Wg,
+            const void* Wu, const void* Wd, void* G, void* U, void* dx,
+            void* dWg, void* dWu, void* dWd, int fuse_grad_accum,
+            void* ws, size_t ws_bytes, void* stream);
+
+/* Backward that saved only x (quack mlp.py MLPRecomputeFunc): recomputes
+ * the preacts x Wg^T, x Wu^T into the workspace, then runs mlp_bwd's
+ * stages.  Arguments as in mlp_bwd without G and U. */
+int mlp_bwd_recompute(const mlp_problem_t* p, const void* dout, const void* x,
+                      const void* Wg, const void* Wu, const void* Wd, void* dx,
+                      void* dWg, void* dWu, void* dWd, int fuse_grad_accum,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mlp_status_string(int status);
+
+/* Synchronises `stream`, then returns the device status word of the last
+ * call that used workspace `ws` (MLP_OK or MLP_ERR_TIMEOUT), or
+ * MLP_ERR_CUDA if the synchronisation or the copy failed. */
+int mlp_device_status(const void* ws, void* stream);
+
+/* Library version, e.g. "0.1.0". */
+const char* mlp_version(void);
+
+/* ---- Tracing (timing support; no counterpart on the pages) ----
+ * With tracing on, every kernel launch of the calls above is bracketed by
+ * a pair of CUDA events recorded on the call's stream (this may keep
+ * consecutive kernels from overlapping through programmatic dependent
+ * launch).  Kernel tags: */
+typedef enum {
+  MLP_KERNEL_GATE_UP = 0,  /* gate/up (or fc1) GEMM with the activation epilogue */
+  MLP_KERNEL_DOWN = 1,     /* down projection GEMM */
+  MLP_KERNEL_DGATED = 2,   /* dout Wd GEMM with the dgated / dact epilogue */
+  MLP_KERNEL_DX = 3,       /* dx GEMM */
+  MLP_KERNEL_WGRAD = 4,    /* grouped weight-gradient GEMMs */
+  MLP_KERNEL_POSTACT = 5   /* elementwise postact rebuild (dWd-only backward) */
+} mlp_kernel_t;
+
+/* on != 0 starts recording, 0 stops (records already taken are kept). */
+int mlp_trace_enable(int on);
+
+/* Waits for the recorded events, writes up to `capacity` (tag, ms) pairs
+ * in launch order into host arrays `tags` and `ms`, frees all records, and
+ * returns the number written (or MLP_ERR_CUDA). */
+int mlp_trace_read(int* tags, float* ms, int capacity);
+
+/* Static name of a kernel tag ("dgated", ...). */
+const char* mlp_kernel_name(int tag);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLP_GB300_H */

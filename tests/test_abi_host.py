@@ -1,0 +1,113 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every symbol include/mlp.h declares, and rejects bad arguments before
+enqueueing anything (fake, never-dereferenced pointers are used)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import activated_mlp_gemms_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mlp.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(m.LIB_PATH):
+        from activated_mlp_gemms_gb300 import _build
+        _build.build()
+    return m.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_]+\s*\*?\s*(mlp_[a-z_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert names == sorted(["mlp_workspace_size", "mlp_fwd", "mlp_fwd_infer", "mlp_bwd",
+                            "mlp_bwd_recompute", "mlp_status_string", "mlp_device_status",
+                            "mlp_version", "mlp_trace_enable", "mlp_trace_read",
+                            "mlp_kernel_name"])
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    assert m.mlp_version() == "0.1.0"
+
+
+def test_status_strings(L):
+    assert m.mlp_status_string(0) == "MLP_OK"
+    assert m.mlp_status_string(-4) == "MLP_ERR_WORKSPACE_TOO_SMALL"
+    assert m.mlp_status_string(-6) == "MLP_ERR_TIMEOUT"
+    assert m.mlp_status_string(12345) == "MLP_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(L):
+    p = m.problem(2048, 4096, 11008)
+    inter = 2048 * 11008 * 2
+    assert m.mlp_workspace_size(p, m.MODE_FWD) == 1024 + inter
+    assert m.mlp_workspace_size(p, m.MODE_INFER) == 1024 + inter
+    assert m.mlp_workspace_size(p, m.MODE_BWD) == 1024 + inter
+    assert m.mlp_workspace_size(p, m.MODE_BWD_RECOMPUTE) == 1024 + 3 * inter
+    q = m.problem(49152, 768, 3072, "relu_sq")
+    assert m.mlp_workspace_size(q, m.MODE_BWD_RECOMPUTE) == 1024 + 2 * 49152 * 3072 * 2
+    assert m.mlp_workspace_size(m.problem(0, 8, 8), 0) == 0
+    assert m.mlp_workspace_size(m.problem(8, 12, 8), 0) == 0  # H % 8 != 0
+    assert m.mlp_workspace_size(p, 7) == 0
+
+
+FAKE = 0x10000  # aligned, never dereferenced: validation fails before any launch
+
+
+def _fwd(L, prob, x=FAKE, Wg=FAKE, Wu=FAKE, Wd=FAKE, out=FAKE, ws=FAKE, ws_bytes=1 << 40):
+    return L.mlp_fwd_infer(ctypes.byref(prob), x, Wg, Wu, Wd, out, ws, ws_bytes, None)
+
+
+def test_validation_errors(L):
+    assert _fwd(L, m.problem(0, 128, 352)) == -1            # M <= 0
+    assert _fwd(L, m.problem(64, 130, 352)) == -2           # H % 8
+    assert _fwd(L, m.problem(64, 128, 350)) == -2           # I % 8
+    assert _fwd(L, m.problem(64, 128, 352), x=None) == -1   # null input
+    assert _fwd(L, m.problem(64, 128, 352), Wg=FAKE + 2) == -2  # misaligned
+    assert _fwd(L, m.problem(64, 128, 352), Wu=None) == -1  # gated needs Wu
+    assert _fwd(L, m.problem(64, 128, 352, "relu_sq")) == -1  # non-gated takes no Wu
+    assert _fwd(L, m.problem(64, 128, 352), ws_bytes=100) == -4
+    assert _fwd(L, m.problem(64, 128, 352), ws=FAKE + 16) == -2  # workspace 256-aligned
+    bad = m.problem(64, 128, 352)
+    bad.act = 9
+    assert _fwd(L, bad) == -1
+    nanp = m.problem(64, 128, 352, gate_mult=float("nan"))
+    assert _fwd(L, nanp) == -1
+    assert L.mlp_fwd_infer(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == -1
+
+
+def test_backward_validation(L):
+    p = m.problem(64, 128, 352)
+    args = [FAKE] * 5  # dout, x, Wg, Wu, Wd
+    # saved mode needs G and U
+    assert L.mlp_bwd(ctypes.byref(p), *args, None, FAKE, FAKE, None, None, None, 0, FAKE,
+                     1 << 40, None) == -1
+    # fuse flag must be 0/1
+    assert L.mlp_bwd(ctypes.byref(p), *args, FAKE, FAKE, FAKE, None, None, None, 3, FAKE,
+                     1 << 40, None) == -1
+    # recompute-mode workspace is larger
+    need = m.mlp_workspace_size(p, m.MODE_BWD_RECOMPUTE)
+    assert L.mlp_bwd_recompute(ctypes.byref(p), *args, FAKE, None, None, None, 0, FAKE,
+                               need - 1, None) == -4
+    # non-gated: dWu must be NULL
+    q = m.problem(64, 128, 352, "relu_sq")
+    assert L.mlp_bwd_recompute(ctypes.byref(q), FAKE, FAKE, FAKE, None, FAKE, None, None, FAKE,
+                               None, 0, FAKE, 1 << 40, None) == -1
+
+
+def test_kernel_names_and_empty_trace(L):
+    assert m.mlp_kernel_name(2) == "dgated"
+    assert m.mlp_kernel_name(99) == "unknown"
+    assert m.mlp_trace_read() == []  # nothing recorded: no CUDA call is made

@@ -1,0 +1,197 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances: max|err|/max|ref| <= 2e-2 for bf16 outputs and <= 5e-3 for
+fp32-accumulated weight gradients, per tensor.  Every output buffer carries
+a NaN-filled guard band (checked after each call) and starts NaN-filled, so
+an untouched tile or an out-of-range store fails the test.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import activated_mlp_gemms_gb300 as m
+from activated_mlp_gemms_gb300.workloads import (WORKLOADS, closed_form_inputs, make_inputs,
+                                                 to_f64, workload_inputs)
+from mlp_gpu_helpers import (TOL_BF16, TOL_F32, compare_full, dev_tensors, oracle_full,
+                             oracle_sampled, run_gpu)
+from oracle import rel_err
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_form_small.json")
+
+
+def _golden_cases():
+    with open(GOLDEN) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("mode", ["saved", "recompute"])
+def test_golden_closed_form(mode):
+    for c in _golden_cases():
+        M, H, I, act = c["M"], c["H"], c["I"], c["act"]
+        t = dev_tensors(closed_form_inputs(M, H, I, act))
+        got, bad, _ = run_gpu(t, M, H, I, act, c["gate_mult"], c["down_mult"], mode=mode)
+        assert not bad, f"guard band overwritten: {bad}"
+        ref = {k: (np.array(c[k]) if c[k] is not None else None)
+               for k in ("out", "dx", "dWg", "dWu", "dWd")}
+        compare_full(got, ref, fuse=False)
+
+
+SMALL = [  # (M, H, I): one tile; several tiles with ragged tails in every dimension
+    (64, 128, 352),
+    (300, 200, 392),
+    (257, 264, 520),
+    (1, 8, 8),
+]
+
+
+@pytest.mark.parametrize("act,gm,dm", [("swiglu", 1.0, 1.0), ("swiglu", 1.125, 2.0),
+                                       ("relu_sq", 1.0, 1.0), ("gelu_tanh_approx", 0.75, 1.5)])
+@pytest.mark.parametrize("shape", SMALL)
+@pytest.mark.parametrize("mode,fuse", [("saved", False), ("recompute", False), ("saved", True),
+                                       ("recompute", True)])
+def test_small_parity(act, gm, dm, shape, mode, fuse):
+    M, H, I = shape
+    t = make_inputs(M, H, I, act, seed=1, dW_prev=fuse)
+    tc = {k: v for k, v in t.items() if not k.endswith("_prev")}
+    prev = {k: v for k, v in t.items() if k.endswith("_prev")} if fuse else None
+    got, bad, _ = run_gpu(dev_tensors(tc), M, H, I, act, gm, dm, mode=mode, fuse=fuse, dW_prev=prev)
+    assert not bad, f"guard band overwritten: {bad}"
+    ref = oracle_full(tc, act, gm, dm, dW_prev=prev)
+    compare_full(got, ref, fuse)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "relu_sq", "gelu_tanh_approx"])
+def test_infer_equals_train_forward_bitwise(act):
+    M, H, I = 300, 264, 392
+    t = dev_tensors(make_inputs(M, H, I, act, seed=2))
+    prob = m.problem(M, H, I, act, 1.125, 2.0)
+    o1 = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    o2 = torch.empty_like(o1)
+    G = torch.empty(M, I, dtype=torch.bfloat16, device="cuda")
+    U = torch.empty_like(G) if act == "swiglu" else None
+    m.mlp_fwd(prob, t["x"], t["Wg"], t["Wu"], t["Wd"], o1, G, U)
+    m.mlp_fwd_infer(prob, t["x"], t["Wg"], t["Wu"], t["Wd"], o2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "relu_sq"])
+def test_saved_equals_recompute_bitwise(act):
+    # Both paths read bf16 preacts produced by the same GEMM tiles, so the
+    # bf16 outputs agree exactly.
+    M, H, I = 300, 264, 392
+    tc = dev_tensors(make_inputs(M, H, I, act, seed=3))
+    a, _, _ = run_gpu(tc, M, H, I, act, 1.0, 1.0, mode="saved")
+    b, _, _ = run_gpu(tc, M, H, I, act, 1.0, 1.0, mode="recompute")
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("mode", ["saved", "recompute"])
+@pytest.mark.parametrize("want", [("dWd",), ("dx",), ("dWg",), ("dx", "dWd")])
+def test_partial_gradients(mode, want):
+    # Unrequested gradients are skipped (NULL outputs); requested ones match.
+    M, H, I, act = 200, 136, 264, "swiglu"
+    t = make_inputs(M, H, I, act, seed=4)
+    got, bad, _ = run_gpu(dev_tensors(t), M, H, I, act, 1.125, 2.0, mode=mode, want=want)
+    assert not bad
+    ref = oracle_full(t, act, 1.125, 2.0)
+    errs = compare_full(got, ref, fuse=False)
+    assert set(errs) == {"out", *want}
+
+
+def test_split_m_accumulation_matches_one_call():
+    # The data-parallel invariant: two half-M backward calls accumulating into
+    # the same fp32 gradients equal one full-M call.
+    M, H, I, act = 512, 256, 384, "swiglu"
+    t = dev_tensors(make_inputs(M, H, I, act, seed=5))
+    prob_full = m.problem(M, H, I, act)
+    z = lambda *s: torch.zeros(*s, dtype=torch.float32, device="cuda")  # noqa: E731
+    full = {"dWg": z(I, H), "dWu": z(I, H), "dWd": z(H, I)}
+    m.mlp_bwd_recompute(prob_full, t["dout"], t["x"], t["Wg"], t["Wu"], t["Wd"], None,
+                        full["dWg"], full["dWu"], full["dWd"], fuse_grad_accum=True)
+    half = {"dWg": z(I, H), "dWu": z(I, H), "dWd": z(H, I)}
+    for sl in (slice(0, 200), slice(200, M)):
+        n = sl.stop - sl.start
+        prob = m.problem(n, H, I, act)
+        m.mlp_bwd_recompute(prob, t["dout"][sl].contiguous(), t["x"][sl].contiguous(), t["Wg"],
+                            t["Wu"], t["Wd"], None, half["dWg"], half["dWu"], half["dWd"],
+                            fuse_grad_accum=True)
+    torch.cuda.synchronize()
+    for k in full:
+        assert rel_err(to_f64(half[k]), to_f64(full[k])) < 1e-5, k
+
+
+def test_device_status_ok_and_errors():
+    M, H, I = 64, 128, 352
+    t = dev_tensors(make_inputs(M, H, I, "swiglu"))
+    prob = m.problem(M, H, I)
+    out = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    ws = m.alloc_workspace(prob, m.MODE_INFER)
+    m.mlp_fwd_infer(prob, t["x"], t["Wg"], t["Wu"], t["Wd"], out, ws=ws)
+    assert m.mlp_device_status(ws) == 0
+    # workspace too small
+    with pytest.raises(m.MlpError) as e:
+        m.mlp_fwd_infer(prob, t["x"], t["Wg"], t["Wu"], t["Wd"], out, ws=ws[:1024])
+    assert e.value.code == -4
+    # misaligned input pointer (offset by one element = 2 bytes)
+    xb = torch.empty(M * H + 8, dtype=torch.bfloat16, device="cuda")
+    xmis = xb[1:1 + M * H].view(M, H)
+    with pytest.raises(m.MlpError) as e:
+        m.mlp_fwd_infer(prob, xmis, t["Wg"], t["Wu"], t["Wd"], out, ws=ws)
+    assert e.value.code == -2
+    # non-gated activation with an up weight
+    with pytest.raises(m.MlpError) as e:
+        m.mlp_fwd_infer(m.problem(M, H, I, "relu_sq"), t["x"], t["Wg"], t["Wu"], t["Wd"], out)
+    assert e.value.code == -1
+
+
+# ------------------------------------------------------------- full sizes (sampled)
+
+@pytest.mark.parametrize("name", ["llama7b_swiglu", "falcon_h1_swiglu", "nanogpt_relu_sq",
+                                  "llama3_8b_swiglu"])
+def test_full_size_sampled(name):
+    """The pages' shapes at full size, in the launch configuration the
+    benchmark times; parity on sampled token rows (out, dx) and sampled
+    intermediate units (rows of dWg/dWu, columns of dWd, each reduced over
+    all M tokens), computed exactly by the oracle."""
+    w = WORKLOADS[name]
+    t = workload_inputs(w)
+    tc = {k: v for k, v in t.items() if not k.endswith("_prev")}
+    prev = {k: v for k, v in t.items() if k.endswith("_prev")} if w.fuse_grad_accum else None
+    mode = "recompute" if w.recompute else "saved"
+    got, bad, _ = run_gpu(dev_tensors(tc), w.M, w.H, w.I, w.act, w.gate_mult, w.down_mult,
+                          mode=mode, fuse=w.fuse_grad_accum, dW_prev=prev)
+    assert not bad
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(w.M, size=48, replace=False))
+    rows[0], rows[-1] = 0, w.M - 1
+    cols = np.sort(rng.choice(w.I, size=24, replace=False))
+    cols[0], cols[-1] = 0, w.I - 1
+    r, c = oracle_sampled(tc, w.act, w.gate_mult, w.down_mult, rows, cols, dW_prev=prev)
+    tol_w = TOL_F32 if w.fuse_grad_accum else TOL_BF16
+    errs = {
+        "out": rel_err(to_f64(got["out"][torch.as_tensor(rows)]), r["out"]),
+        "dx": rel_err(to_f64(got["dx"][torch.as_tensor(rows)]), r["dx"]),
+        "dWg": rel_err(to_f64(got["dWg"][torch.as_tensor(cols)]), c["dWg"]),
+        "dWd": rel_err(to_f64(got["dWd"][:, torch.as_tensor(cols)]), c["dWd"]),
+    }
+    if w.gated:
+        errs["dWu"] = rel_err(to_f64(got["dWu"][torch.as_tensor(cols)]), c["dWu"])
+    for k, e in errs.items():
+        tol = tol_w if k.startswith("dW") else TOL_BF16
+        assert e <= tol, (name, k, errs)
+    for k in ("out", "dx", "dWg", "dWd"):
+        assert torch.isfinite(got[k].float()).all(), k
+    if w.infer:
+        out2 = torch.empty_like(got["out"])
+        dt = dev_tensors(tc)
+        m.mlp_fwd_infer(m.problem(w.M, w.H, w.I, w.act, w.gate_mult, w.down_mult),
+                        dt["x"], dt["Wg"], dt["Wu"], dt["Wd"], out2)
+        torch.cuda.synchronize()
+        assert torch.equal(out2, got["out"])
