@@ -22,7 +22,7 @@ __all__ = [
     "ACTS", "MlpError", "Problem", "lib", "mlp_workspace_size", "mlp_fwd", "mlp_fwd_infer",
     "mlp_bwd", "mlp_bwd_recompute", "mlp_status_string", "mlp_device_status", "mlp_version",
     "MODE_FWD", "MODE_INFER", "MODE_BWD", "MODE_BWD_RECOMPUTE", "mlp_trace_enable",
-    "mlp_trace_read", "mlp_kernel_name",
+    "mlp_trace_read", "mlp_kernel_name", "mlp_set_tile_policy",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -75,6 +75,8 @@ def lib():
     L.mlp_device_status.restype = ctypes.c_int
     L.mlp_version.argtypes = []
     L.mlp_version.restype = ctypes.c_char_p
+    L.mlp_set_tile_policy.argtypes = [ctypes.c_int]
+    L.mlp_set_tile_policy.restype = ctypes.c_int
     L.mlp_trace_enable.argtypes = [ctypes.c_int]
     L.mlp_trace_enable.restype = ctypes.c_int
     L.mlp_trace_read.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_float),
@@ -223,3 +225,8 @@ def mlp_trace_read(capacity: int = 4096):
     if n < 0:
         raise MlpError(n, "mlp_trace_read")
     return [(mlp_kernel_name(tags[i]), float(ms[i])) for i in range(n)]
+
+
+def mlp_set_tile_policy(policy: int) -> None:
+    """0 = automatic, 1 = single-CTA 128x256 tiles, 2 = CTA-pair 256x256 tiles."""
+    _check(lib().mlp_set_tile_policy(int(policy)), "mlp_set_tile_policy")

@@ -1,7 +1,7 @@
 // gemm.cuh -- the persistent, warp-specialised tcgen05 GEMM with the MLP's
 // fused epilogues.
 //
-// One CTA per SM (192 threads, ~195 KB shared memory, all 512 TMEM columns):
+// One CTA per SM (320 threads, ~195 KB shared memory, all 512 TMEM columns):
 //   warp 0     TMA producer and tile scheduler: fetches work units from a
 //              global atomic counter (first unit = blockIdx.x), publishes
 //              them through a shared-memory ring, and streams the A/B
@@ -9,8 +9,9 @@
 //   warp 1     allocates TMEM; one lane issues tcgen05.mma (M=128, N=256,
 //              K=16) into one of two 256-column fp32 accumulators and
 //              commits stage releases / accumulator-full signals.
-//   warps 2-5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
-//              32*(w%4)..+31, i.e. one output row per thread), apply the
+//   warps 2-9  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
+//              32*(w%4)..+31, i.e. one output row per thread; warps w and
+//              w+4 take the two column halves of those rows), apply the
 //              fused activation / derivative / scaling, store to global.
 // The double-buffered accumulator lets the epilogue of tile t overlap the
 // MMAs of tile t+1.  Every wait is bounded (globaltimer); on expiry the
@@ -79,14 +80,14 @@ __device__ __forceinline__ void record_timeout(const Params& p, volatile int* ab
 
 template <int ACT>
 __device__ __forceinline__ void epi_gated_fwd(const Params& p, const Prob& P, uint32_t tb, int row,
-                                              int col0) {
+                                              int col0, int cb, int ce) {
   const bool row_ok = row < P.M;
   const float s = p.scale;
   __nv_bfloat16* a_out = static_cast<__nv_bfloat16*>(P.out0);
   __nv_bfloat16* g_out = static_cast<__nv_bfloat16*>(P.out1);
   __nv_bfloat16* u_out = static_cast<__nv_bfloat16*>(P.out2);
 #pragma unroll 1
-  for (int c = 0; c < 128; c += 32) {
+  for (int c = cb; c < ce; c += 32) {
     uint32_t g[32], u[32];
     __syncwarp();
     tmem_ld32(tb + c, g);
@@ -118,13 +119,13 @@ __device__ __forceinline__ void epi_gated_fwd(const Params& p, const Prob& P, ui
 
 template <int ACT>
 __device__ __forceinline__ void epi_act_fwd(const Params& p, const Prob& P, uint32_t tb, int row,
-                                            int col0) {
+                                            int col0, int cb, int ce) {
   const bool row_ok = row < P.M;
   const float s = p.scale;
   __nv_bfloat16* a_out = static_cast<__nv_bfloat16*>(P.out0);
   __nv_bfloat16* p_out = static_cast<__nv_bfloat16*>(P.out1);
 #pragma unroll 1
-  for (int c = 0; c < 256; c += 32) {
+  for (int c = cb; c < ce; c += 32) {
     uint32_t z[32];
     __syncwarp();
     tmem_ld32(tb + c, z);
@@ -150,20 +151,41 @@ __device__ __forceinline__ void epi_act_fwd(const Params& p, const Prob& P, uint
   }
 }
 
-// GATED = true: in0 = G, in1 = U -> out0 = dG, out1 = dU, out2 = a (optional)
-// GATED = false: in0 = P -> out0 = dP, out2 = a (optional)
-template <int ACT, bool GATED>
-__device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, uint32_t tb, int row,
-                                         int col0) {
-  const bool row_ok = row < P.M;
-  const float s = p.scale;
+// Loads this thread's 32 saved preacts (G and, if gated, U) of chunk `col`.
+template <bool GATED>
+__device__ __forceinline__ void dact_load(const Prob& P, int row, int col, uint4 (&g)[4],
+                                          uint4 (&u)[4]) {
   const __nv_bfloat16* g_in = static_cast<const __nv_bfloat16*>(P.in0);
   const __nv_bfloat16* u_in = static_cast<const __nv_bfloat16*>(P.in1);
+  const bool row_ok = row < P.M;
+  const size_t off = static_cast<size_t>(row) * P.ld + col;
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const bool ok = row_ok && (col + 8 * v < P.N);
+    g[v] = ok ? ld_global_v4(g_in + off + 8 * v) : make_uint4(0, 0, 0, 0);
+    u[v] = (GATED && ok) ? ld_global_v4(u_in + off + 8 * v) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// GATED = true: in0 = G, in1 = U -> out0 = dG, out1 = dU, out2 = a (optional)
+// GATED = false: in0 = P -> out0 = dP, out2 = a (optional)
+// The saved preacts of chunk c+1 are loaded while chunk c is computed; the
+// caller has already loaded chunk `cb` into (pg, pu) before waiting for the
+// accumulator.  In-place outputs are safe: each thread reads an element
+// before it writes it, and no other thread touches it.
+template <int ACT, bool GATED>
+__device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, uint32_t tb, int row,
+                                         int col0, int cb, int ce, uint4 (&pg)[4],
+                                         uint4 (&pu)[4]) {
+  const bool row_ok = row < P.M;
+  const float s = p.scale;
   __nv_bfloat16* dg_out = static_cast<__nv_bfloat16*>(P.out0);
   __nv_bfloat16* du_out = static_cast<__nv_bfloat16*>(P.out1);
   __nv_bfloat16* a_out = static_cast<__nv_bfloat16*>(P.out2);
 #pragma unroll 1
-  for (int c = 0; c < 256; c += 32) {
+  for (int c = cb; c < ce; c += 32) {
+    uint4 ng[4], nu[4];
+    if (c + 32 < ce) dact_load<GATED>(P, row, col0 + c + 32, ng, nu);
     uint32_t d[32];
     __syncwarp();
     tmem_ld32(tb + c, d);
@@ -174,10 +196,8 @@ __device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, uint32_
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         if (col + 8 * v < P.N) {
-          uint4 gv = ld_global_v4(g_in + off + 8 * v);
-          uint4 uv = GATED ? ld_global_v4(u_in + off + 8 * v) : make_uint4(0, 0, 0, 0);
-          const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-          const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+          const uint32_t gw[4] = {pg[v].x, pg[v].y, pg[v].z, pg[v].w};
+          const uint32_t uw[4] = {pu[v].x, pu[v].y, pu[v].z, pu[v].w};
           uint32_t pdg[4], pdu[4], pa[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -203,14 +223,22 @@ __device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, uint32_
         }
       }
     }
+    if (c + 32 < ce) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        pg[v] = ng[v];
+        pu[v] = nu[v];
+      }
+    }
   }
 }
 
 template <int EPI>
-__device__ __forceinline__ void epi_plain(const Prob& P, uint32_t tb, int row, int col0) {
+__device__ __forceinline__ void epi_plain(const Prob& P, uint32_t tb, int row, int col0, int cb,
+                                          int ce) {
   const bool row_ok = row < P.M;
 #pragma unroll 1
-  for (int c = 0; c < 256; c += 32) {
+  for (int c = cb; c < ce; c += 32) {
     uint32_t d[32];
     __syncwarp();
     tmem_ld32(tb + c, d);
@@ -250,23 +278,81 @@ __device__ __forceinline__ void epi_plain(const Prob& P, uint32_t tb, int row, i
 }
 
 // -------------------------------------------------------------------- kernel
-template <int EPI, bool A_MN, bool B_MN>
+// Per-CTA-group constants.  CG = 1: one CTA computes a 128 x 256 tile and
+// stages all 256 B rows.  CG = 2: a CTA pair computes a 256 x 256 tile with
+// one tcgen05.mma.cta_group::2; each CTA stages its own 128 A rows and 128
+// of the 256 B rows, so a stage is 32 KB and six fit in shared memory.
+template <int CG>
+struct Cfg {
+  static constexpr int B_ROWS = CG == 2 ? 128 : 256;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = CG == 2 ? 6 : 4;
+  static constexpr int TILE_M = BM * CG;
+  static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 1024 /*barriers, ring*/;
+};
+
+// Issues the TMA boxes of one k-block into this CTA's stage (A at sA, B at
+// sB), completing on barrier `full` (for a pair: the leader's barrier).
+//   A K-major: one box {64 k, 128 rows};  A MN-major: two boxes {64 m, 64 k}.
+//   B gated:   CG=1 the gate and the up rows (two {64, 128} boxes);
+//              CG=2 the leader stages the gate rows, the peer the up rows.
+//   B K-major: one box {64, 256 / CG};      B MN-major: 4 / CG boxes {64 n, 64 k}.
+template <int EPI, bool A_MN, bool B_MN, int CG>
+__device__ __forceinline__ void load_stage(const Params& p, const Prob& P, const Work& w, int seg,
+                                           int kc, uint32_t sA, uint32_t sB, uint32_t full,
+                                           uint32_t rank, uint64_t pol) {
+  auto ld = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+    if constexpr (CG == 2) tma_load_2d_pair(dst, m, c0, c1, full, pol);
+    else tma_load_2d(dst, m, c0, c1, full, pol);
+  };
+  const CUtensorMap* mA = &p.maps[seg == 0 ? P.mapA0 : P.mapA1];
+  const int m0 = w.tm * (BM * CG) + static_cast<int>(rank) * BM;
+  if constexpr (!A_MN) {
+    ld(sA, mA, kc, m0);
+  } else {
+    ld(sA, mA, m0, kc);
+    ld(sA + 8192, mA, m0 + 64, kc);
+  }
+  if constexpr (EPI == EPI_GATED_FWD) {
+    if constexpr (CG == 1) {
+      ld(sB, &p.maps[P.mapB0], kc, w.tn * 128);
+      ld(sB + 16384, &p.maps[P.mapB1], kc, w.tn * 128);
+    } else {
+      ld(sB, &p.maps[rank == 0 ? P.mapB0 : P.mapB1], kc, w.tn * 128);
+    }
+  } else {
+    const CUtensorMap* mB = &p.maps[seg == 0 ? P.mapB0 : P.mapB1];
+    const int n0 = w.tn * MMA_N + static_cast<int>(rank) * (MMA_N / CG);
+    if constexpr (!B_MN) {
+      ld(sB, mB, kc, n0);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4 / CG; ++j) ld(sB + j * 8192, mB, n0 + j * 64, kc);
+    }
+  }
+}
+
+template <int EPI, bool A_MN, bool B_MN, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
+  using C = Cfg<CG>;
+  constexpr bool PAIR = CG == 2;
   constexpr int TILE_N = EpiTraits<EPI>::TILE_N;
-  constexpr uint32_t IDESC = idesc_bf16(BM, MMA_N, A_MN, B_MN);
+  constexpr uint32_t IDESC = idesc_bf16(C::TILE_M, MMA_N, A_MN, B_MN);
 
   // 1024-byte aligned stage ring (the 128-byte swizzle repeats every 1 KB)
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
   uint8_t* base_g = smem_raw + (base_s - raw_s);
-  uint8_t* ctrl = base_g + STAGES * STAGE_BYTES;
+  uint8_t* ctrl = base_g + C::STAGES * C::STAGE;
   uint64_t* bar = reinterpret_cast<uint64_t*>(ctrl);
-  // barrier indices
-  const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, TEMPTY = 2 * STAGES + 2,
-            SFULL = 2 * STAGES + 4, SEMPTY = 2 * STAGES + 4 + SCHED_SLOTS,
-            DRAIN = 2 * STAGES + 4 + 2 * SCHED_SLOTS;
-  const int NBAR = DRAIN + 1;
+  // barrier indices (same offsets in both CTAs of a pair)
+  constexpr int FULL = 0, EMPTY = C::STAGES, TFULL = 2 * C::STAGES, TEMPTY = 2 * C::STAGES + 2,
+                SFULL = 2 * C::STAGES + 4, SEMPTY = 2 * C::STAGES + 4 + SCHED_SLOTS,
+                DRAIN = 2 * C::STAGES + 4 + 2 * SCHED_SLOTS;
+  constexpr int NBAR = DRAIN + 1;
   int* sched = reinterpret_cast<int*>(ctrl + 8 * NBAR);
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sched + SCHED_SLOTS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
@@ -274,19 +360,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  // the leader's copy of a barrier / ring slot, as a shared::cluster address
+  auto lead = [&](uint32_t local) { return PAIR ? mapa_shared(local, 0) : local; };
+  auto peer = [&](uint32_t local) { return mapa_shared(local, 1); };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(bar_s(FULL + i), 1);
       mbar_init(bar_s(EMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s(TFULL + i), 1);
-      mbar_init(bar_s(TEMPTY + i), 4);
+      mbar_init(bar_s(TEMPTY + i), CG * NUM_EPI_WARPS);
     }
     for (int i = 0; i < SCHED_SLOTS; ++i) {
       mbar_init(bar_s(SFULL + i), 1);
-      mbar_init(bar_s(SEMPTY + i), 5);
+      // MMA issuer + every epilogue warp of the pair + the peer's producer
+      mbar_init(bar_s(SEMPTY + i), 1 + CG * NUM_EPI_WARPS + (CG - 1));
     }
     mbar_init(bar_s(DRAIN), 1);
     *abort_flag = 0;
@@ -296,11 +388,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
     for (int i = 0; i < MAX_MAPS; ++i) prefetch_tmap(&p.maps[i]);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_base_s), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<CG>(smem_u32(tmem_base_s), TMEM_COLS);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // barriers of both CTAs initialised before remote use
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
 
@@ -309,6 +402,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
   pdl_launch_dependents();
 
   const uint64_t lim = p.timeout_ns;
+  const int ncl = gridDim.x / CG;          // clusters (CTA groups) in the grid
+  const int cl = blockIdx.x / CG;          // this CTA group
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -319,71 +414,91 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       int slot = 0;
       uint32_t sphase = 0;
       int issued = 0;  // k-blocks issued (for the drain on abort)
-      int unit = blockIdx.x;
+      int unit = cl;
       bool ok = true;
       while (ok) {
-        const bool done = unit >= p.total_units;
-        const int next = done ? unit : (int)gridDim.x + atomicAdd(p.counter, 1);
-        if (!mbar_wait(bar_s(SEMPTY + slot), sphase ^ 1u, lim, abort_flag)) {
-          ok = false;
-          break;
-        }
-        sched[slot] = done ? -1 : unit;
-        mbar_arrive(bar_s(SFULL + slot));
-        if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
-        if (done) break;
-        const Work w = decode_unit(p, unit);
-        const Prob& P = p.prob[w.prob];
-        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
-          if (!mbar_wait(bar_s(EMPTY + stage), phase ^ 1u, lim, abort_flag)) {
+        if (leader) {
+          // fetch the next unit early; publish this one to the pair's rings
+          const bool done = unit >= p.total_units;
+          const int next = done ? unit : ncl + atomicAdd(p.counter, 1);
+          if (!mbar_wait<PAIR>(bar_s(SEMPTY + slot), sphase ^ 1u, lim, abort_flag)) {
             ok = false;
             break;
           }
-          const uint32_t full = bar_s(FULL + stage);
-          mbar_expect_tx(full, STAGE_BYTES);
-          const int seg = kb < P.kb0 ? 0 : 1;
-          const int kc = (seg == 0 ? kb : kb - P.kb0) * BK;
-          const CUtensorMap* mA = &p.maps[seg == 0 ? P.mapA0 : P.mapA1];
-          const uint32_t sA = base_s + stage * STAGE_BYTES;
-          const uint32_t sB = sA + A_STAGE_BYTES;
-          if constexpr (!A_MN) {
-            tma_load_2d(sA, mA, kc, w.tm * BM, full, pol);
-          } else {
-            tma_load_2d(sA, mA, w.tm * BM, kc, full, pol);
-            tma_load_2d(sA + 8192, mA, w.tm * BM + 64, kc, full, pol);
+          const int v = done ? -1 : unit;
+          sched[slot] = v;
+          if constexpr (PAIR) {
+            st_shared_cluster_u32(peer(smem_u32(sched + slot)), static_cast<uint32_t>(v));
+            mbar_arrive_cluster(peer(bar_s(SFULL + slot)));
           }
-          if constexpr (EPI == EPI_GATED_FWD) {
-            tma_load_2d(sB, &p.maps[P.mapB0], kc, w.tn * 128, full, pol);
-            tma_load_2d(sB + 16384, &p.maps[P.mapB1], kc, w.tn * 128, full, pol);
-          } else {
-            const CUtensorMap* mB = &p.maps[seg == 0 ? P.mapB0 : P.mapB1];
-            if constexpr (!B_MN) {
-              tma_load_2d(sB, mB, kc, w.tn * MMA_N, full, pol);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * 8192, mB, w.tn * MMA_N + j * 64, kc, full, pol);
+          mbar_arrive(bar_s(SFULL + slot));
+          if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
+          if (done) break;
+          const Work w = decode_unit(p, unit);
+          const Prob& P = p.prob[w.prob];
+          for (int kb = w.kb_begin; kb < w.kb_end && ok; ++kb) {
+            if (!mbar_wait<PAIR>(bar_s(EMPTY + stage), phase ^ 1u, lim, abort_flag)) {
+              ok = false;
+              break;
             }
+            const uint32_t full = bar_s(FULL + stage);
+            // the leader's full barrier expects the bytes of both CTAs of a pair
+            mbar_expect_tx(full, CG * C::STAGE);
+            const int seg = kb < P.kb0 ? 0 : 1;
+            const int kc = (seg == 0 ? kb : kb - P.kb0) * BK;
+            const uint32_t sA = base_s + stage * C::STAGE;
+            load_stage<EPI, A_MN, B_MN, CG>(p, P, w, seg, kc, sA, sA + C::A_BYTES, full, rank, pol);
+            ++issued;
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
           }
-          ++issued;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          unit = next;
+        } else {
+          // peer of a pair: take units from the ring the leader fills
+          if (!mbar_wait<PAIR>(bar_s(SFULL + slot), sphase, lim, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int v = sched[slot];
+          mbar_arrive_cluster(lead(bar_s(SEMPTY + slot)));
+          if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
+          if (v < 0) break;
+          const Work w = decode_unit(p, v);
+          const Prob& P = p.prob[w.prob];
+          const uint32_t full_lead = lead(bar_s(FULL));
+          for (int kb = w.kb_begin; kb < w.kb_end && ok; ++kb) {
+            if (!mbar_wait<PAIR>(bar_s(EMPTY + stage), phase ^ 1u, lim, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const int seg = kb < P.kb0 ? 0 : 1;
+            const int kc = (seg == 0 ? kb : kb - P.kb0) * BK;
+            const uint32_t sA = base_s + stage * C::STAGE;
+            load_stage<EPI, A_MN, B_MN, CG>(p, P, w, seg, kc, sA, sA + C::A_BYTES,
+                                            full_lead + 8u * stage, rank, pol);
+            ++issued;
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+          }
         }
-        unit = next;
       }
       if (!ok) {
         record_timeout(p, abort_flag);
-        // let the copies already in flight land before shared memory is released
-        int s = stage;
-        uint32_t ph = phase;
-        for (int i = 0; i < STAGES && i < issued; ++i) {
-          if (--s < 0) { s = STAGES - 1; ph ^= 1u; }
-          volatile int never = 0;
-          mbar_wait(bar_s(FULL + s), ph, 10000000ull, &never);
+        if (leader) {
+          // let the copies already in flight land before shared memory is released
+          int s = stage;
+          uint32_t ph = phase;
+          for (int i = 0; i < C::STAGES && i < issued; ++i) {
+            if (--s < 0) { s = C::STAGES - 1; ph ^= 1u; }
+            volatile int never = 0;
+            mbar_wait<PAIR>(bar_s(FULL + s), ph, 10000000ull, &never);
+          }
+        } else {
+          __nanosleep(100000);  // the peer's copies signal the leader's barriers
         }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int slot = 0;
@@ -393,126 +508,187 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       bool ok = true;
       bool any = false;
       while (ok) {
-        if (!mbar_wait(bar_s(SFULL + slot), sphase, lim, abort_flag)) { ok = false; break; }
+        if (!mbar_wait<PAIR>(bar_s(SFULL + slot), sphase, lim, abort_flag)) { ok = false; break; }
         const int unit = sched[slot];
         mbar_arrive(bar_s(SEMPTY + slot));
         if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
         if (unit < 0) break;
         const Work w = decode_unit(p, unit);
-        if (!mbar_wait(bar_s(TEMPTY + acc), aphase ^ 1u, lim, abort_flag)) { ok = false; break; }
+        if (!mbar_wait<PAIR>(bar_s(TEMPTY + acc), aphase ^ 1u, lim, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + acc * MMA_N;
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
-          if (!mbar_wait(bar_s(FULL + stage), phase, lim, abort_flag)) { ok = false; break; }
+          if (!mbar_wait<PAIR>(bar_s(FULL + stage), phase, lim, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sA = base_s + stage * STAGE_BYTES;
-          const uint32_t sB = sA + A_STAGE_BYTES;
+          const uint32_t sA = base_s + stage * C::STAGE;
+          const uint32_t sB = sA + C::A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = A_MN ? sdesc_sw128(sA + k * 2048, 8192, 1024)
                                      : sdesc_sw128(sA + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(sB + k * 2048, 8192, 1024)
                                      : sdesc_sw128(sB + k * 32, 16, 1024);
-            tc_mma_bf16(d, ad, bd, IDESC, (kb > w.kb_begin || k > 0) ? 1u : 0u);
+            const uint32_t accum = (kb > w.kb_begin || k > 0) ? 1u : 0u;
+            if constexpr (PAIR) tc_mma_bf16_pair(d, ad, bd, IDESC, accum);
+            else tc_mma_bf16(d, ad, bd, IDESC, accum);
           }
           any = true;
-          tc_commit(bar_s(EMPTY + stage));
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if constexpr (PAIR) tc_commit_pair(bar_s(EMPTY + stage), 3);
+          else tc_commit(bar_s(EMPTY + stage));
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(bar_s(TFULL + acc));
+        if constexpr (PAIR) tc_commit_pair(bar_s(TFULL + acc), 3);
+        else tc_commit(bar_s(TFULL + acc));
         acc ^= 1;
         if (acc == 0) aphase ^= 1u;
       }
       if (!ok) {
         record_timeout(p, abort_flag);
         if (any) {  // wait for the MMAs already issued before TMEM is freed
-          tc_commit(bar_s(DRAIN));
+          if constexpr (PAIR) tc_commit_pair(bar_s(DRAIN), 1);
+          else tc_commit(bar_s(DRAIN));
           volatile int never = 0;
-          mbar_wait(bar_s(DRAIN), 0, 10000000ull, &never);
+          mbar_wait<PAIR>(bar_s(DRAIN), 0, 10000000ull, &never);
         }
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const int row_in_tile = q * 32 + lane;
+    const int q = warp & 3;            // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns
+    const int row_in_tile = static_cast<int>(rank) * BM + q * 32 + lane;
+    const int cb = half * (TILE_N / 2), ce = cb + TILE_N / 2;
     int slot = 0;
     uint32_t sphase = 0;
     int acc = 0;
     uint32_t aphase = 0;
     while (true) {
-      if (!mbar_wait(bar_s(SFULL + slot), sphase, lim, abort_flag)) {
+      if (!mbar_wait<PAIR>(bar_s(SFULL + slot), sphase, lim, abort_flag)) {
         record_timeout(p, abort_flag);
         break;
       }
       const int unit = sched[slot];
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_s(SEMPTY + slot));
+      if (lane == 0) {
+        if (leader) mbar_arrive(bar_s(SEMPTY + slot));
+        else mbar_arrive_cluster(lead(bar_s(SEMPTY + slot)));
+      }
       if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
       if (unit < 0) break;
       const Work w = decode_unit(p, unit);
       const Prob& P = p.prob[w.prob];
-      if (!mbar_wait(bar_s(TFULL + acc), aphase, lim, abort_flag)) {
+      const int row = w.tm * C::TILE_M + row_in_tile;
+      const int col0 = w.tn * TILE_N;
+      uint4 pg[4], pu[4];
+      if constexpr (EPI == EPI_DGATED || EPI == EPI_DACT) {
+        // the saved preacts do not depend on the MMAs: fetch the first chunk now
+        dact_load<EPI == EPI_DGATED>(P, row, col0 + cb, pg, pu);
+      }
+      if (!mbar_wait<PAIR>(bar_s(TFULL + acc), aphase, lim, abort_flag)) {
         record_timeout(p, abort_flag);
         break;
       }
       tc_fence_after();
       const uint32_t tb = tmem + acc * MMA_N + (static_cast<uint32_t>(q * 32) << 16);
-      const int row = w.tm * BM + row_in_tile;
-      const int col0 = w.tn * TILE_N;
       if constexpr (EPI == EPI_GATED_FWD) {
-        epi_gated_fwd<ACT_SILU>(p, P, tb, row, col0);
+        epi_gated_fwd<ACT_SILU>(p, P, tb, row, col0, cb, ce);
       } else if constexpr (EPI == EPI_ACT_FWD) {
-        if (p.act == ACT_RELU_SQ) epi_act_fwd<ACT_RELU_SQ>(p, P, tb, row, col0);
-        else epi_act_fwd<ACT_GELU_TANH>(p, P, tb, row, col0);
+        if (p.act == ACT_RELU_SQ) epi_act_fwd<ACT_RELU_SQ>(p, P, tb, row, col0, cb, ce);
+        else epi_act_fwd<ACT_GELU_TANH>(p, P, tb, row, col0, cb, ce);
       } else if constexpr (EPI == EPI_DGATED) {
-        epi_dact<ACT_SILU, true>(p, P, tb, row, col0);
+        epi_dact<ACT_SILU, true>(p, P, tb, row, col0, cb, ce, pg, pu);
       } else if constexpr (EPI == EPI_DACT) {
-        if (p.act == ACT_RELU_SQ) epi_dact<ACT_RELU_SQ, false>(p, P, tb, row, col0);
-        else epi_dact<ACT_GELU_TANH, false>(p, P, tb, row, col0);
+        if (p.act == ACT_RELU_SQ) epi_dact<ACT_RELU_SQ, false>(p, P, tb, row, col0, cb, ce, pg, pu);
+        else epi_dact<ACT_GELU_TANH, false>(p, P, tb, row, col0, cb, ce, pg, pu);
       } else {
-        epi_plain<EPI>(P, tb, row, col0);
+        epi_plain<EPI>(P, tb, row, col0, cb, ce);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_s(TEMPTY + acc));
+      if (lane == 0) {
+        if (leader) mbar_arrive(bar_s(TEMPTY + acc));
+        else mbar_arrive_cluster(lead(bar_s(TEMPTY + acc)));
+      }
       acc ^= 1;
       if (acc == 0) aphase ^= 1u;
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // no remote arrival or copy may target an exited CTA
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc<CG>(tmem, TMEM_COLS);
   }
 }
 
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, int CG>
 cudaError_t launch_gemm(const Params& p, int grid, cudaStream_t stream, bool pdl) {
-  auto kern = k_mlp_gemm<EPI, A_MN, B_MN>;
+  auto kern = k_mlp_gemm<EPI, A_MN, B_MN, CG>;
   static std::atomic<unsigned> configured_dev_mask{0};  // devices that got the smem attribute
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 31 || !(configured_dev_mask.load() & (1u << dev))) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<CG>::SMEM);
     if (e != cudaSuccess) return e;
+    if (CG == 2) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      (void)e;
+    }
     if (dev < 31) configured_dev_mask.fetch_or(1u << dev);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<CG>::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (CG == 2) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// Largest number of CTA pairs that can be co-resident (0 on error).
+template <int EPI, bool A_MN, bool B_MN, int CG>
+int max_groups() {
+  auto kern = k_mlp_gemm<EPI, A_MN, B_MN, CG>;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (CG == 1) return sms;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<CG>::SMEM) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<CG>::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+  return n;
 }
 
 }  // namespace mlpk

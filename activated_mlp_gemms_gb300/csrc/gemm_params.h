@@ -7,20 +7,17 @@
 
 namespace mlpk {
 
-// CTA tile: BM x (MMA N = 256) x BK, bf16 operands, fp32 accumulators.
+// Tile: (128 x CTA-group size) x (MMA N = 256) x BK, bf16 operands, fp32
+// accumulators; each CTA owns BM = 128 accumulator rows.
 constexpr int BM = 128;
 constexpr int MMA_N = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;      // 16 KB
-constexpr int B_STAGE_BYTES = MMA_N * BK * 2;   // 32 KB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int SCHED_SLOTS = 8;
-constexpr int NUM_THREADS = 192;                // producer, MMA, 4 epilogue warps
+constexpr int NUM_EPI_WARPS = 8;                // two per TMEM lane quadrant (column halves)
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;  // producer, MMA, epilogue warps
 constexpr int TMEM_COLS = 512;                  // two 256-column accumulators
 constexpr int MAX_PROBS = 3;
 constexpr int MAX_MAPS = 12;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 1024 /*barriers*/;
 
 // What the epilogue does with the accumulator tile.
 enum Epi : int {
@@ -66,9 +63,13 @@ struct Params {  // 64-byte aligned through CUtensorMap
   unsigned long long timeout_ns;
 };
 
-// Host-side launcher, explicitly instantiated in the kernel translation units.
-template <int EPI, bool A_MN, bool B_MN>
+// Host-side launcher and co-residency query, explicitly instantiated in the
+// kernel translation units.  CG = CTA-group size (1: single CTA, 2: CTA
+// pair with tcgen05 cta_group::2); `grid` is in CTAs (a multiple of CG).
+template <int EPI, bool A_MN, bool B_MN, int CG>
 cudaError_t launch_gemm(const Params& p, int grid, cudaStream_t stream, bool pdl);
+template <int EPI, bool A_MN, bool B_MN, int CG>
+int max_groups();
 
 // Elementwise postact a = s*act(G)*U (U == nullptr: non-gated), n elements.
 cudaError_t launch_postact(const void* G, const void* U, void* a, long long n, int act,

@@ -19,6 +19,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 #include <vector>
@@ -132,11 +133,22 @@ unsigned long long wait_limit_ns() {
 // ------------------------------------------------------------ launch builder
 // Operand roles: a K-major operand [rows, K] is loaded with boxes
 // {64, rows-per-box}; an MN-major operand [K, MN] with boxes {64, 64}.
+std::atomic<int> g_tile_policy{0};  // 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles
+
+// CTA-group size for a GEMM whose output has `rows` rows: pairs (256-row
+// tiles) unless the output fits one 128-row tile.
+int pick_cg(int rows) {
+  const int pol = g_tile_policy.load();
+  if (pol == 1 || pol == 2) return pol;
+  return rows > BM ? 2 : 1;
+}
+
 struct Gemm {
   Params p;
   int nmaps = 0;
+  int cg = 1;
   bool ok = true;
-  Gemm(const mlp_problem_t& pr, int* counter, int* status) {
+  Gemm(const mlp_problem_t& pr, int* counter, int* status, int cg_) : cg(cg_) {
     std::memset(&p, 0, sizeof(p));
     p.act = pr.act;
     p.scale = pr.gate_mult * pr.down_mult;
@@ -163,7 +175,7 @@ struct Gemm {
     P.N = N;
     P.kb0 = (K0 + BK - 1) / BK;
     P.kb1 = (K1 + BK - 1) / BK;
-    P.tiles_m = (M + BM - 1) / BM;
+    P.tiles_m = (M + BM * cg - 1) / (BM * cg);
     P.tiles_n = (N + tile_n - 1) / tile_n;
     const int kbt = P.kb0 + P.kb1;
     if (ksplit < 1) ksplit = 1;
@@ -176,11 +188,8 @@ struct Gemm {
     P.ld = N;
     return P;
   }
-  int grid() const {
-    int sms = num_sms();
-    int g = p.total_units < sms ? p.total_units : sms;
-    return g < 1 ? 1 : g;
-  }
+  // B rows per K-major box: a CTA stages 256 / cg of the 256 B rows
+  int b_rows() const { return MMA_N / cg; }
 };
 
 struct Call {
@@ -234,12 +243,37 @@ int traced(int tag, cudaStream_t s, F&& launch) {
   return cuda_err(e);
 }
 
+// Co-resident CTA groups of a kernel instance on the current device (cached).
+template <int EPI, bool A_MN, bool B_MN, int CG>
+int groups_cached() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) {
+    int v = cache[dev].load();
+    if (v > 0) return v;
+  }
+  int v = max_groups<EPI, A_MN, B_MN, CG>();
+  if (v > 0 && dev >= 0 && dev < 64) cache[dev].store(v);
+  return v;
+}
+
 template <int EPI, bool A_MN, bool B_MN>
 int run(Gemm& g, Call& c, int tag) {
   if (!g.ok) return MLP_ERR_CUDA;
   if (g.p.total_units == 0) return MLP_OK;
   const bool pdl = c.pdl();
-  return traced(tag, c.stream, [&] { return launch_gemm<EPI, A_MN, B_MN>(g.p, g.grid(), c.stream, pdl); });
+  if (g.cg == 2) {
+    const int groups = groups_cached<EPI, A_MN, B_MN, 2>();
+    if (groups <= 0) return MLP_ERR_CUDA;
+    const int n = g.p.total_units < groups ? g.p.total_units : groups;
+    return traced(tag, c.stream,
+                  [&] { return launch_gemm<EPI, A_MN, B_MN, 2>(g.p, 2 * n, c.stream, pdl); });
+  }
+  const int sms = num_sms();
+  const int n = g.p.total_units < sms ? g.p.total_units : sms;
+  return traced(tag, c.stream,
+                [&] { return launch_gemm<EPI, A_MN, B_MN, 1>(g.p, n < 1 ? 1 : n, c.stream, pdl); });
 }
 
 // ------------------------------------------------------------ validation
@@ -307,7 +341,7 @@ int begin_call(Call& c, void* ws, void* stream) {
 //   a_out: postact (may be null), G_out/U_out: preact stores (may be null)
 int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* Wg, const void* Wu,
                    void* a_out, void* G_out, void* U_out) {
-  Gemm g(*p, c.counter(), c.status);
+  Gemm g(*p, c.counter(), c.status, pick_cg(p->M));
   const int mA = g.kmajor(x, p->M, p->H, BM);
   if (gated(p)) {
     const int mG = g.kmajor(Wg, p->I, p->H, 128);
@@ -321,7 +355,7 @@ int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* W
     P.out2 = U_out;
     return run<EPI_GATED_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
   }
-  const int mW = g.kmajor(Wg, p->I, p->H, MMA_N);
+  const int mW = g.kmajor(Wg, p->I, p->H, g.b_rows());
   Prob& P = g.add(p->M, p->I, p->H, 0, MMA_N);
   P.mapA0 = mA;
   P.mapB0 = mW;
@@ -332,9 +366,9 @@ int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* W
 
 // out = a Wd^T
 int launch_down(const mlp_problem_t* p, Call& c, const void* a, const void* Wd, void* out) {
-  Gemm g(*p, c.counter(), c.status);
+  Gemm g(*p, c.counter(), c.status, pick_cg(p->M));
   const int mA = g.kmajor(a, p->M, p->I, BM);
-  const int mB = g.kmajor(Wd, p->H, p->I, MMA_N);
+  const int mB = g.kmajor(Wd, p->H, p->I, g.b_rows());
   Prob& P = g.add(p->M, p->H, p->I, 0, MMA_N);
   P.mapA0 = mA;
   P.mapB0 = mB;
@@ -394,14 +428,16 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
   if (recompute) {
     G = base + inter_bytes(p);
     U = gated(p) ? base + 2 * inter_bytes(p) : nullptr;
-    // stage 0: recompute the preacts (quack MLPRecomputeFunc: preact = x W1^T)
-    MLP_TRY(launch_fwd_act(p, c, x, Wg, Wu, nullptr, G, U));
+    // stage 0: recompute the preacts (quack MLPRecomputeFunc: preact = x W1^T);
+    // the postact needed by dWd comes straight from the fp32 accumulators
+    MLP_TRY(launch_fwd_act(p, c, x, Wg, Wu, dWd ? a : nullptr, G, U));
   }
   const int M = p->M, H = p->H, I = p->I;
 
   if (need_dact) {
-    // stage 1: dh = dout Wd (K = H); epilogue writes dG, dU over G, U and the postact a
-    Gemm g(*p, c.counter(), c.status);
+    // stage 1: dh = dout Wd (K = H); epilogue writes dG, dU over G, U (and the
+    // postact a when the saved preacts are the only source of it)
+    Gemm g(*p, c.counter(), c.status, pick_cg(M));
     const int mA = g.kmajor(dout, M, H, BM);
     const int mB = g.mnmajor(Wd, H, I);  // Wd [H,I]: B(n=i, k=h) is N-contiguous
     Prob& P = g.add(M, I, H, 0, MMA_N);
@@ -411,10 +447,10 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     P.in1 = U;
     P.out0 = G;
     P.out1 = U;
-    P.out2 = dWd ? a : nullptr;
+    P.out2 = (dWd && !recompute) ? a : nullptr;
     MLP_TRY(gated(p) ? run<EPI_DGATED, false, true>(g, c, MLP_KERNEL_DGATED)
                      : run<EPI_DACT, false, true>(g, c, MLP_KERNEL_DGATED));
-  } else {
+  } else if (!recompute) {
     // only dWd requested: rebuild the postact without the derivative
     const bool pdl = c.pdl();
     MLP_TRY(traced(MLP_KERNEL_POSTACT, c.stream, [&] {
@@ -427,7 +463,7 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
 
   if (dx) {
     // stage 2: dx = [dG|dU] [Wg;Wu], one accumulator over K = 2I (non-gated: K = I)
-    Gemm g(*p, c.counter(), c.status);
+    Gemm g(*p, c.counter(), c.status, pick_cg(M));
     const int mA0 = g.kmajor(dG, M, I, BM);
     const int mB0 = g.mnmajor(Wg, I, H);  // Wg [I,H]: B(n=h, k=i) is N-contiguous
     int mA1 = 0, mB1 = 0;
@@ -447,7 +483,7 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
   if (dWg || dWu || dWd) {
     // stage 3: weight gradients in one grouped launch, reduced over the M tokens:
     //   dWg = dG^T x, dWu = dU^T x  ([I,H])   dWd = dout^T a  ([H,I])
-    Gemm g(*p, c.counter(), c.status);
+    Gemm g(*p, c.counter(), c.status, pick_cg(H < I ? H : I));
     struct W { const void* A; int rows; const void* B; int cols; void* out; };
     W list[3];
     int n = 0;
@@ -456,14 +492,15 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     if (dWd) list[n++] = {dout, H, a, I, dWd};
     long long tiles = 0;
     for (int i = 0; i < n; ++i)
-      tiles += (long long)((list[i].rows + BM - 1) / BM) * ((list[i].cols + MMA_N - 1) / MMA_N);
+      tiles += (long long)((list[i].rows + BM * g.cg - 1) / (BM * g.cg)) *
+               ((list[i].cols + MMA_N - 1) / MMA_N);
     // split the token reduction when the output tiles cannot fill the GPU
     // (fp32 accumulation only: partial sums meet through atomic adds)
     int ksplit = 1;
-    const int sms = num_sms();
+    const int slots = num_sms() / g.cg;
     const int kb = (M + BK - 1) / BK;
-    if (fuse && tiles < sms) {
-      ksplit = (int)(sms / tiles);
+    if (fuse && tiles < slots) {
+      ksplit = (int)(slots / tiles);
       while (ksplit > 1 && kb / ksplit < 8) --ksplit;
     }
     for (int i = 0; i < n; ++i) {
@@ -541,6 +578,12 @@ int mlp_device_status(const void* ws, void* stream) {
 }
 
 const char* mlp_version(void) { return "0.1.0"; }
+
+int mlp_set_tile_policy(int policy) {
+  if (policy < 0 || policy > 2) return MLP_ERR_INVALID_ARG;
+  g_tile_policy.store(policy);
+  return MLP_OK;
+}
 
 int mlp_trace_enable(int on) {
   std::lock_guard<std::mutex> lk(g_trace_mu);

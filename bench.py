@@ -1,0 +1,500 @@
+#!/usr/bin/env python
+"""Fused transformer MLP fwd+bwd throughput on GB300 (bf16 in, fp32 accumulate).
+
+One step = one training forward (mlp_fwd) plus one backward (mlp_bwd from
+saved preacts, or mlp_bwd_recompute) of the selected workload, on seeded
+synthetic inputs already resident in HBM.  The L2 cache is flushed (a
+512 MiB write) before every timed step, outside the step's events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host cores
+
+Prints one JSON line.  Under torchrun (N > 1) every rank runs an independent
+replica of the workload (the MLP path has no collective of its own); the
+step time is the maximum over ranks and `value` sums all ranks' work.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLP fwd+bwd TFLOP/s (bf16) and % of GB300 dense-BF16 peak, 1 GPU"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama7b_swiglu")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-trace", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def mode_of(w):
+    return "bwd_recompute" if w.recompute else "bwd"
+
+
+def flops_of(w, mode):
+    """GEMM flops (2 x multiply-adds) of one pass; gated: fwd 6MHI, bwd 12MHI,
+    recompute +4MHI; non-gated: 4, 8, +2."""
+    mhi = float(w.M) * w.H * w.I
+    g = w.gated
+    if mode in ("fwd", "infer"):
+        return (6 if g else 4) * mhi
+    if mode == "bwd":
+        return (12 if g else 8) * mhi
+    if mode == "bwd_recompute":
+        return (16 if g else 10) * mhi
+    raise ValueError(mode)
+
+
+def kernel_flops(w):
+    """Algorithmic flops per launch of each kernel of a step."""
+    mhi = float(w.M) * w.H * w.I
+    g = w.gated
+    return {
+        "gate_up_act": (4 if g else 2) * mhi,
+        "down_proj": 2 * mhi,
+        "dgated": 2 * mhi,
+        "dx": (4 if g else 2) * mhi,
+        "wgrad": (6 if g else 4) * mhi,
+    }
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "activated_mlp_gemms_gb300", "csrc")
+    for n in sorted(os.listdir(d)):
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(n.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the
+    current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload, {}).get(kernel)
+        if e and e.get("csrc_hash") == csrc_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._t = threading.Thread(target=self._run, daemon=True)
+
+    def _one(self):
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                               timeout=10)
+            if r.returncode == 0 and r.stdout.strip():
+                self.samples.append([x.strip() for x in r.stdout.strip().split(",")])
+        except Exception:
+            pass
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._one()
+            self._stop.wait(0.05)
+
+    def __enter__(self):
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        self._t.join(timeout=15)
+        if not self.samples:
+            self._one()
+
+    def summary(self):
+        if not self.samples:
+            return None
+        sm, mx = [], []
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            try:
+                sm.append(float(s[0]))
+                mx.append(float(s[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, s[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- ours
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import activated_mlp_gemms_gb300 as m
+    from activated_mlp_gemms_gb300.workloads import WORKLOADS, workload_inputs
+
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    from activated_mlp_gemms_gb300 import _build
+    _build.build()
+
+    t = workload_inputs(w)
+    g = {k: (v.to(dev) if v is not None else None) for k, v in t.items()}
+    bf = torch.bfloat16
+    M, H, I = w.M, w.H, w.I
+    prob = m.problem(M, H, I, w.act, w.gate_mult, w.down_mult)
+    out = torch.empty(M, H, dtype=bf, device=dev)
+    dx = torch.empty(M, H, dtype=bf, device=dev)
+    wdt = torch.float32 if w.fuse_grad_accum else bf
+    dWg = torch.zeros(I, H, dtype=wdt, device=dev)
+    dWu = torch.zeros(I, H, dtype=wdt, device=dev) if w.gated else None
+    dWd = torch.zeros(H, I, dtype=wdt, device=dev)
+    if w.fuse_grad_accum:
+        dWg.copy_(t["dWg_prev"])
+        dWd.copy_(t["dWd_prev"])
+        if dWu is not None:
+            dWu.copy_(t["dWu_prev"])
+    saved = not w.recompute
+    G = torch.empty(M, I, dtype=bf, device=dev) if saved else None
+    U = torch.empty(M, I, dtype=bf, device=dev) if (saved and w.gated) else None
+    ws_f = m.alloc_workspace(prob, m.MODE_FWD, dev)
+    ws_b = m.alloc_workspace(prob, m.MODE_BWD_RECOMPUTE if w.recompute else m.MODE_BWD, dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        m.mlp_fwd(prob, g["x"], g["Wg"], g["Wu"], g["Wd"], out, G, U, ws=ws_f)
+
+    def bwd():
+        if saved:
+            m.mlp_bwd(prob, g["dout"], g["x"], g["Wg"], g["Wu"], g["Wd"], G, U, dx, dWg, dWu, dWd,
+                      fuse_grad_accum=w.fuse_grad_accum, ws=ws_b)
+        else:
+            m.mlp_bwd_recompute(prob, g["dout"], g["x"], g["Wg"], g["Wu"], g["Wd"], dx, dWg, dWu,
+                                dWd, fuse_grad_accum=w.fuse_grad_accum, ws=ws_b)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+    if m.mlp_device_status(ws_b) != 0 or m.mlp_device_status(ws_f) != 0:
+        raise RuntimeError("device status error during warm-up")
+    if world > 1:
+        dist.barrier()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    trace = not args.no_trace
+    cvd = [c for c in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if c.strip()]
+    sampler = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else local_rank)
+    if trace:
+        m.mlp_trace_read()
+        m.mlp_trace_enable(True)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    wall0 = time.perf_counter()
+    with sampler:
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            bwd()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if trace:
+        m.mlp_trace_enable(False)
+        recs = m.mlp_trace_read(capacity=64 * (K + 1))
+    else:
+        recs = []
+    if world > 1:
+        dist.barrier()
+    status = m.mlp_device_status(ws_b)
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    step_ms = [a + b for a, b in zip(fwd_ms, bwd_ms)]
+    tot_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([tot_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        tot_ms = float(tt.item())
+    ms_per_step = tot_ms / K
+    f_fwd = flops_of(w, "fwd")
+    f_bwd = flops_of(w, mode_of(w))
+    f_step = f_fwd + f_bwd
+    value = world * f_step / (ms_per_step * 1e-3) / 1e12
+
+    # per-kernel device times from the launch trace of the timed region
+    per = {}
+    for name, ms in recs:
+        per.setdefault(name, []).append(ms)
+    peaks, peaks_src = load_peaks()
+    kf = kernel_flops(w)
+    kernels = {}
+    for name, v in per.items():
+        fl = kf.get(name)
+        # the recompute backward runs the gate/up kernel twice per step
+        kernels[name] = {"launches": len(v), "avg_ms": sum(v) / len(v), "total_ms": sum(v),
+                         "tflops": (fl / (sum(v) / len(v) * 1e-3) / 1e12) if fl else None}
+    roof = None
+    if kernels:
+        dom = max(kernels, key=lambda k: kernels[k]["total_ms"])
+        d = kernels[dom]
+        peak = float(peaks["bf16_tflops"])
+        ach = d["tflops"]
+        traffic = load_traffic(dom, w.name)
+        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": (ach / peak) if ach else None, "traffic": traffic,
+                "peak_source": f"{peaks_src} bf16 burst ({'MEASURED_PEAKS.json' if peaks_src == 'measured' else 'recipe fallback'})"}
+    clocks = sampler.summary()
+
+    # end to end through the C ABI with host buffers: H2D of x and dout from
+    # pinned memory, the step, D2H of out and dx
+    e2e = None
+    if not args.no_e2e:
+        hx = t["x"].pin_memory()
+        hd = t["dout"].pin_memory()
+        ho = torch.empty(M, H, dtype=bf).pin_memory()
+        hdx = torch.empty(M, H, dtype=bf).pin_memory()
+        ke = max(3, min(K, 50))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        tms = 0.0
+        for i in range(ke + 2):
+            flush.zero_()
+            e0.record(stream)
+            g["x"].copy_(hx, non_blocking=True)
+            g["dout"].copy_(hd, non_blocking=True)
+            fwd()
+            bwd()
+            ho.copy_(out, non_blocking=True)
+            hdx.copy_(dx, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 2:
+                tms += e0.elapsed_time(e1)
+        tms /= ke
+        if world > 1:
+            tt = torch.tensor([tms], device=dev, dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            tms = float(tt.item())
+        nb = M * H * 2
+        e2e = {"value": world * f_step / (tms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": tms,
+               "h2d_bytes_per_step": 2 * nb, "d2h_bytes_per_step": 2 * nb}
+
+    # extra: the no-grad inference forward of workloads that name it
+    infer = None
+    if w.infer:
+        ei0 = torch.cuda.Event(enable_timing=True)
+        ei1 = torch.cuda.Event(enable_timing=True)
+        ws_i = m.alloc_workspace(prob, m.MODE_INFER, dev)
+        for _ in range(3):
+            m.mlp_fwd_infer(prob, g["x"], g["Wg"], g["Wu"], g["Wd"], out, ws=ws_i)
+        ims = []
+        for _ in range(max(3, min(K, 50))):
+            flush.zero_()
+            ei0.record(stream)
+            m.mlp_fwd_infer(prob, g["x"], g["Wg"], g["Wu"], g["Wd"], out, ws=ws_i)
+            ei1.record(stream)
+            torch.cuda.synchronize(dev)
+            ims.append(ei0.elapsed_time(ei1))
+        im = sum(ims) / len(ims)
+        infer = {"ms": im, "tflops": flops_of(w, "infer") / (im * 1e-3) / 1e12}
+
+    peak = float(peaks["bf16_tflops"])
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, nn.Linear Kaiming-uniform weights)",
+        "config": {"workload": w.name, "M": M, "H": H, "I": I, "act": w.act,
+                   "gate_mult": w.gate_mult, "down_mult": w.down_mult,
+                   "backward": "recompute (save only x)" if w.recompute else "saved G/U",
+                   "fuse_grad_accum": w.fuse_grad_accum,
+                   "l2": "flushed before every timed step (512 MiB write, outside the step events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_peak": 100.0 * value / world / peak,
+        "peak_tflops": peak, "peak_source": peaks_src,
+        "breakdown": {"fwd_ms": sum(fwd_ms) / K, "bwd_ms": sum(bwd_ms) / K,
+                      "fwd_tflops": f_fwd / (sum(fwd_ms) / K * 1e-3) / 1e12,
+                      "bwd_tflops": f_bwd / (sum(bwd_ms) / K * 1e-3) / 1e12,
+                      "model_flops_per_step": flops_of(w, "fwd") + flops_of(w, "bwd"),
+                      "executed_flops_per_step": f_step, "kernels": kernels,
+                      "infer": infer},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": len(recs) if trace else None,
+        "clocks": clocks,
+        "device_status": status,
+        "wall_s_timed_region": wall,
+    }
+    return res, w
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, seconds, steps=1):
+    """Time the fp64 oracle on a bounded token sample of the workload."""
+    import numpy as np
+
+    from activated_mlp_gemms_gb300.workloads import to_f64, workload_inputs
+    from oracle import mlp_backward
+
+    t = workload_inputs(w)
+    a = {k: to_f64(v) for k, v in t.items() if v is not None}
+    Wu = a.get("Wu")
+    prev = None
+    if w.fuse_grad_accum:
+        prev = {"dWg": a["dWg_prev"], "dWu": a.get("dWu_prev"), "dWd": a["dWd_prev"]}
+
+    def one(n):
+        t0 = time.perf_counter()
+        mlp_backward(a["dout"][:n], a["x"][:n], a["Wg"], Wu, a["Wd"], w.act, w.gate_mult,
+                     w.down_mult, dW_prev=prev)  # runs the forward internally
+        return time.perf_counter() - t0
+
+    # calibrate on 16 tokens, then size the sample to the time budget per step
+    n0 = min(16, w.M)
+    t0 = one(n0)
+    per_tok = t0 / n0
+    n = int(max(8, min(w.M, seconds / max(per_tok, 1e-9))))
+    times = [one(n) for _ in range(steps)]
+    # flops of the oracle pass: forward + backward (saved-preact arithmetic)
+    f = flops_of(type("W", (), {"M": n, "H": w.H, "I": w.I, "gated": w.gated})(), "fwd") + \
+        flops_of(type("W", (), {"M": n, "H": w.H, "I": w.I, "gated": w.gated})(), "bwd")
+    tpt = sum(times) / len(times)
+    cores = os.cpu_count()
+    return {"value": f / tpt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.M} tokens (full H={w.H}, I={w.I}), oracle forward+backward in "
+                      f"numpy fp64, {len(times)} pass(es), {tpt:.2f} s each",
+            "seconds_per_pass": tpt, "tokens": n}, tpt
+
+
+def run_reference(args, rank, world):
+    from activated_mlp_gemms_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    budget = 150.0  # seconds for the whole reference run
+    per_step = max(0.5, budget / max(1, K + W))
+    cb, _ = oracle_sample(w, per_step, steps=1)
+    n = cb["tokens"]
+    import numpy as np  # noqa: F401
+
+    from activated_mlp_gemms_gb300.workloads import to_f64, workload_inputs
+    from oracle import mlp_backward
+    t = workload_inputs(w)
+    a = {k: to_f64(v) for k, v in t.items() if v is not None}
+    prev = None
+    if w.fuse_grad_accum:
+        prev = {"dWg": a["dWg_prev"], "dWu": a.get("dWu_prev"), "dWd": a["dWd_prev"]}
+
+    def step():
+        mlp_backward(a["dout"][:n], a["x"][:n], a["Wg"], a.get("Wu"), a["Wd"], w.act, w.gate_mult,
+                     w.down_mult, dW_prev=prev)
+
+    for _ in range(W):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        step()
+    sec = (time.perf_counter() - t0) / max(1, K)
+    W_ = type("W", (), {"M": n, "H": w.H, "I": w.I, "gated": w.gated})()
+    f = flops_of(W_, "fwd") + flops_of(W_, "bwd")
+    val = f / sec / 1e12
+    cpu = {"value": val, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"{n} of {w.M} tokens per step (full H={w.H}, I={w.I}), oracle "
+                     f"forward+backward in numpy fp64"}
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "H": w.H, "I": w.I, "act": w.act,
+                       "gate_mult": w.gate_mult, "down_mult": w.down_mult,
+                       "backward": "recompute (save only x)" if w.recompute else "saved G/U",
+                       "fuse_grad_accum": w.fuse_grad_accum},
+            "cpu_baseline": cpu,
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res, w = run_ours(args, rank, world, local_rank)
+    if rank == 0 and not args.no_cpu_baseline:
+        cb, _ = oracle_sample(w, args.cpu_seconds, steps=1)
+        cb.pop("seconds_per_pass", None)
+        cb.pop("tokens", None)
+        res["cpu_baseline"] = cb
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -169,6 +169,15 @@ int mlp_device_status(const void* ws, void* stream);
 /* Library version, e.g. "0.1.0". */
 const char* mlp_version(void);
 
+/* Tile policy (a tuning and testing knob; no counterpart on the pages):
+ * 0 = automatic (default): GEMMs whose output has more than 128 rows use
+ *     256 x 256 tiles computed by a CTA pair (tcgen05 cta_group::2), the
+ *     others 128 x 256 tiles on one CTA;
+ * 1 = always single-CTA tiles;  2 = always CTA-pair tiles.
+ * Process-wide; returns MLP_ERR_INVALID_ARG for other values.  Results of
+ * the two tile shapes agree to rounding (same fp32 accumulation order). */
+int mlp_set_tile_policy(int policy);
+
 /* ---- Tracing (timing support; no counterpart on the pages) ----
  * With tracing on, every kernel launch of the calls above is bracketed by
  * a pair of CUDA events recorded on the call's stream (this may keep

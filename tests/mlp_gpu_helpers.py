@@ -8,7 +8,15 @@ from activated_mlp_gemms_gb300.workloads import to_f64
 from oracle import mlp_backward, mlp_forward, rel_err, sampled_inter_units, sampled_token_rows
 
 TOL_BF16 = 2e-2   # max|err| / max|ref| for bf16 outputs (out, dx, bf16 dW)
-TOL_F32 = 5e-3    # for fp32-accumulated dW
+TOL_F32 = 5e-3    # for fp32-accumulated dW (the workloads' sizes)
+# Below F32_TOL_MIN_TOKENS tokens the fp32-accumulated weight gradients are
+# held to TOL_F32_SMALL instead: there the error floor is set by the bf16
+# storage of the intermediates (G, U, dG, dU, postact), not by the
+# accumulation.  Emulating exactly those roundings in fp64 gives
+# max|err|/max|ref| up to 6.0e-3 (relu_sq dWd, M = 257; SwiGLU dWg 5.1e-3
+# at M = 64), and 1.6e-3 .. 4.4e-3 for M >= 1024.
+F32_TOL_MIN_TOKENS = 1024
+TOL_F32_SMALL = 1e-2
 GUARD = 64        # guard elements after every output buffer
 SENTINEL = float("nan")
 
@@ -96,7 +104,7 @@ def oracle_full(tc, act, gm, dm, dW_prev=None):
     return {"out": fw["out"], **bw}
 
 
-def compare_full(got, ref, fuse):
+def compare_full(got, ref, fuse, M=None):
     errs = {}
     for k, v in got.items():
         if v is None or ref.get(k) is None:
@@ -105,7 +113,10 @@ def compare_full(got, ref, fuse):
         assert np.all(np.isfinite(g)), f"{k}: non-finite values (untouched tile?)"
         errs[k] = rel_err(g, ref[k])
     for k, e in errs.items():
-        tol = TOL_F32 if (fuse and k.startswith("dW")) else TOL_BF16
+        if fuse and k.startswith("dW"):
+            tol = TOL_F32 if (M is None or M >= F32_TOL_MIN_TOKENS) else TOL_F32_SMALL
+        else:
+            tol = TOL_BF16
         assert e <= tol, f"{k}: rel err {e:.3e} > {tol} (all: {errs})"
     return errs
 

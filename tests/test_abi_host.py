@@ -33,7 +33,7 @@ def test_header_declares_the_abi():
     assert names == sorted(["mlp_workspace_size", "mlp_fwd", "mlp_fwd_infer", "mlp_bwd",
                             "mlp_bwd_recompute", "mlp_status_string", "mlp_device_status",
                             "mlp_version", "mlp_trace_enable", "mlp_trace_read",
-                            "mlp_kernel_name"])
+                            "mlp_kernel_name", "mlp_set_tile_policy"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -111,3 +111,10 @@ def test_kernel_names_and_empty_trace(L):
     assert m.mlp_kernel_name(2) == "dgated"
     assert m.mlp_kernel_name(99) == "unknown"
     assert m.mlp_trace_read() == []  # nothing recorded: no CUDA call is made
+
+
+def test_tile_policy_values(L):
+    assert L.mlp_set_tile_policy(3) == -1
+    assert L.mlp_set_tile_policy(-1) == -1
+    for v in (1, 2, 0):
+        assert L.mlp_set_tile_policy(v) == 0
