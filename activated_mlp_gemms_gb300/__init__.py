@@ -22,7 +22,8 @@ __all__ = [
     "ACTS", "MlpError", "Problem", "lib", "mlp_workspace_size", "mlp_fwd", "mlp_fwd_infer",
     "mlp_bwd", "mlp_bwd_recompute", "mlp_status_string", "mlp_device_status", "mlp_version",
     "MODE_FWD", "MODE_INFER", "MODE_BWD", "MODE_BWD_RECOMPUTE", "mlp_trace_enable",
-    "mlp_trace_read", "mlp_kernel_name", "mlp_set_tile_policy",
+    "mlp_trace_read", "mlp_kernel_name", "mlp_set_tile_policy", "mlp_fwd_infer_noalloc",
+    "NOALLOC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,6 +31,7 @@ LIB_PATH = os.path.join(_HERE, "libmlp.so")
 
 ACTS = {"swiglu": 0, "relu_sq": 1, "gelu_tanh_approx": 2}
 MODE_FWD, MODE_INFER, MODE_BWD, MODE_BWD_RECOMPUTE = 0, 1, 2, 3
+NOALLOC_SCRATCH_BYTES = 16 << 20  # MLP_NOALLOC_SCRATCH_BYTES
 
 
 class MlpError(RuntimeError):
@@ -75,6 +77,8 @@ def lib():
     L.mlp_device_status.restype = ctypes.c_int
     L.mlp_version.argtypes = []
     L.mlp_version.restype = ctypes.c_char_p
+    L.mlp_fwd_infer_noalloc.argtypes = [P] + [_VP] * 5 + [_VP]
+    L.mlp_fwd_infer_noalloc.restype = ctypes.c_int
     L.mlp_set_tile_policy.argtypes = [ctypes.c_int]
     L.mlp_set_tile_policy.restype = ctypes.c_int
     L.mlp_trace_enable.argtypes = [ctypes.c_int]
@@ -230,3 +234,16 @@ def mlp_trace_read(capacity: int = 4096):
 def mlp_set_tile_policy(policy: int) -> None:
     """0 = automatic, 1 = single-CTA 128x256 tiles, 2 = CTA-pair 256x256 tiles."""
     _check(lib().mlp_set_tile_policy(int(policy)), "mlp_set_tile_policy")
+
+
+def mlp_fwd_infer_noalloc(prob: Problem, x, Wg, Wu, Wd, out, stream=None) -> None:
+    """Inference forward for callers that may not allocate device memory: the
+    scratch is a fixed array inside the library (NOALLOC_SCRATCH_BYTES), shared
+    by all calls, so calls must be ordered (e.g. one stream).  The first call
+    on a device looks up the array's address; make it before any stream
+    capture.  Raises MlpError(MLP_ERR_WORKSPACE_TOO_SMALL) for problems whose
+    inference workspace exceeds the array."""
+    rc = lib().mlp_fwd_infer_noalloc(ctypes.byref(prob), _ptr(x, name="x"), _ptr(Wg, name="Wg"),
+                                     _ptr(Wu, name="Wu"), _ptr(Wd, name="Wd"),
+                                     _ptr(out, name="out"), _stream(stream))
+    _check(rc, "mlp_fwd_infer_noalloc")

@@ -169,6 +169,30 @@ int mlp_device_status(const void* ws, void* stream);
 /* Library version, e.g. "0.1.0". */
 const char* mlp_version(void);
 
+/* ---- Inference forward without a caller workspace (no counterpart in the
+ * paper: an addition of this library) ----
+ * For callers that may not allocate device memory when they run the MLP
+ * (for example a C runtime whose device memory is planned once at start-up,
+ * or a serving loop that must not call cudaMalloc because it synchronises
+ * the device and has no caching allocator to draw from).  Same arguments and
+ * results as mlp_fwd_infer, minus the workspace: the scratch is a fixed
+ * device array of MLP_NOALLOC_SCRATCH_BYTES inside the library, present on
+ * every GPU that loads the library until the process exits.
+ *   - Returns MLP_ERR_WORKSPACE_TOO_SMALL, enqueueing nothing, when
+ *     mlp_workspace_size(p, MLP_MODE_INFER) exceeds
+ *     MLP_NOALLOC_SCRATCH_BYTES (about M * I <= 8.3 million elements).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array: it keeps the last call's contents, and
+ *     each call clears the parts that must start at zero.  Calls whose work
+ *     overlaps on the GPU (different streams, or without ordering) race on
+ *     it; order them, e.g. on one stream. */
+#define MLP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int mlp_fwd_infer_noalloc(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu,
+                          const void* Wd, void* out, void* stream);
+
 /* Tile policy (a tuning and testing knob; no counterpart on the pages):
  * 0 = automatic (default): GEMMs whose output has more than 128 rows use
  *     256 x 256 tiles computed by a CTA pair (tcgen05 cta_group::2), the

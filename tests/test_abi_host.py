@@ -33,7 +33,8 @@ def test_header_declares_the_abi():
     assert names == sorted(["mlp_workspace_size", "mlp_fwd", "mlp_fwd_infer", "mlp_bwd",
                             "mlp_bwd_recompute", "mlp_status_string", "mlp_device_status",
                             "mlp_version", "mlp_trace_enable", "mlp_trace_read",
-                            "mlp_kernel_name", "mlp_set_tile_policy"])
+                            "mlp_kernel_name", "mlp_set_tile_policy",
+                            "mlp_fwd_infer_noalloc"])
 
 
 def test_library_exports_every_declared_symbol(L):
