@@ -23,7 +23,7 @@ __all__ = [
     "mlp_bwd", "mlp_bwd_recompute", "mlp_status_string", "mlp_device_status", "mlp_version",
     "MODE_FWD", "MODE_INFER", "MODE_BWD", "MODE_BWD_RECOMPUTE", "mlp_trace_enable",
     "mlp_trace_read", "mlp_kernel_name", "mlp_set_tile_policy", "mlp_fwd_infer_noalloc",
-    "NOALLOC_SCRATCH_BYTES",
+    "NOALLOC_SCRATCH_BYTES", "mlp_set_wait_timeout_ms", "mlp_debug_set_flags", "DEBUG_NO_WORK",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -32,6 +32,7 @@ LIB_PATH = os.path.join(_HERE, "libmlp.so")
 ACTS = {"swiglu": 0, "relu_sq": 1, "gelu_tanh_approx": 2}
 MODE_FWD, MODE_INFER, MODE_BWD, MODE_BWD_RECOMPUTE = 0, 1, 2, 3
 NOALLOC_SCRATCH_BYTES = 16 << 20  # MLP_NOALLOC_SCRATCH_BYTES
+DEBUG_NO_WORK = 1  # MLP_DEBUG_NO_WORK
 
 
 class MlpError(RuntimeError):
@@ -79,6 +80,10 @@ def lib():
     L.mlp_version.restype = ctypes.c_char_p
     L.mlp_fwd_infer_noalloc.argtypes = [P] + [_VP] * 5 + [_VP]
     L.mlp_fwd_infer_noalloc.restype = ctypes.c_int
+    L.mlp_set_wait_timeout_ms.argtypes = [ctypes.c_uint]
+    L.mlp_set_wait_timeout_ms.restype = ctypes.c_int
+    L.mlp_debug_set_flags.argtypes = [ctypes.c_int]
+    L.mlp_debug_set_flags.restype = ctypes.c_int
     L.mlp_set_tile_policy.argtypes = [ctypes.c_int]
     L.mlp_set_tile_policy.restype = ctypes.c_int
     L.mlp_trace_enable.argtypes = [ctypes.c_int]
@@ -247,3 +252,13 @@ def mlp_fwd_infer_noalloc(prob: Problem, x, Wg, Wu, Wd, out, stream=None) -> Non
                                      _ptr(Wu, name="Wu"), _ptr(Wd, name="Wd"),
                                      _ptr(out, name="out"), _stream(stream))
     _check(rc, "mlp_fwd_infer_noalloc")
+
+
+def mlp_set_wait_timeout_ms(ms: int) -> None:
+    """Bound of the kernels' device-side waits for later calls (0 = default)."""
+    _check(lib().mlp_set_wait_timeout_ms(int(ms)), "mlp_set_wait_timeout_ms")
+
+
+def mlp_debug_set_flags(flags: int) -> None:
+    """Testing hook: DEBUG_NO_WORK makes later calls time out on purpose."""
+    _check(lib().mlp_debug_set_flags(int(flags)), "mlp_debug_set_flags")

@@ -416,7 +416,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       int issued = 0;  // k-blocks issued (for the drain on abort)
       int unit = cl;
       bool ok = true;
-      while (ok) {
+      // testing hook: publish no work, so the consumers' bounded waits expire
+      const bool publish_nothing = leader && (p.debug_flags & 1);
+      while (ok && !publish_nothing) {
         if (leader) {
           // fetch the next unit early; publish this one to the pair's rings
           const bool done = unit >= p.total_units;

@@ -58,6 +58,8 @@ struct Params {  // 64-byte aligned through CUtensorMap
   int group_m;            // L2 raster: tiles are visited in groups of group_m tile rows
   float scale;            // gate_mult * down_mult (activation epilogues)
   int pad_;
+  int debug_flags;        // MLP_DEBUG_* (testing only; 0 in normal use)
+  int pad2_;
   int* counter;           // dynamic tile scheduler counter, zero at launch
   int* status;            // device status word (MLP_ERR_TIMEOUT on a bounded-wait expiry)
   unsigned long long timeout_ns;

@@ -120,14 +120,18 @@ int num_sms() {
   return n;
 }
 
+std::atomic<unsigned long long> g_wait_ms{0};  // 0: the default below
+std::atomic<int> g_debug_flags{0};
+
 unsigned long long wait_limit_ns() {
-  static unsigned long long v = [] {
+  static unsigned long long env_ms = [] {
     const char* e = std::getenv("MLP_WAIT_TIMEOUT_MS");
-    unsigned long long ms = e ? std::strtoull(e, nullptr, 10) : 0ull;
-    if (ms == 0) ms = 2000;  // 2 s: far above any legitimate wait (tiles take microseconds)
-    return ms * 1000000ull;
+    return e ? std::strtoull(e, nullptr, 10) : 0ull;
   }();
-  return v;
+  unsigned long long ms = g_wait_ms.load();
+  if (ms == 0) ms = env_ms;
+  if (ms == 0) ms = 2000;  // 2 s: far above any legitimate wait (tiles take microseconds)
+  return ms * 1000000ull;
 }
 
 // ------------------------------------------------------------ launch builder
@@ -156,6 +160,7 @@ struct Gemm {
     p.counter = counter;
     p.status = status;
     p.timeout_ns = wait_limit_ns();
+    p.debug_flags = g_debug_flags.load();
   }
   // K-major operand: array [rows, K] (row pitch K), box {64, box_rows}
   int kmajor(const void* ptr, int rows, int K, int box_rows) {
@@ -582,6 +587,17 @@ const char* mlp_version(void) { return "0.1.0"; }
 int mlp_set_tile_policy(int policy) {
   if (policy < 0 || policy > 2) return MLP_ERR_INVALID_ARG;
   g_tile_policy.store(policy);
+  return MLP_OK;
+}
+
+int mlp_set_wait_timeout_ms(unsigned int ms) {
+  g_wait_ms.store(ms);
+  return MLP_OK;
+}
+
+int mlp_debug_set_flags(int flags) {
+  if (flags & ~MLP_DEBUG_NO_WORK) return MLP_ERR_INVALID_ARG;
+  g_debug_flags.store(flags);
   return MLP_OK;
 }
 

@@ -202,6 +202,20 @@ int mlp_fwd_infer_noalloc(const mlp_problem_t* p, const void* x, const void* Wg,
  * the two tile shapes agree to rounding (same fp32 accumulation order). */
 int mlp_set_tile_policy(int policy);
 
+/* ---- Failure-detection hooks (testing; no counterpart on the pages) ----
+ * Every device-side wait of the kernels is bounded; when one expires the
+ * kernel records MLP_ERR_TIMEOUT in the workspace status word, stops its
+ * work and returns, leaving the CUDA context usable.
+ * mlp_set_wait_timeout_ms sets the bound for later calls (0 = default:
+ * the MLP_WAIT_TIMEOUT_MS environment variable, else 2000 ms).
+ * mlp_debug_set_flags(MLP_DEBUG_NO_WORK) makes the kernels' tile schedulers
+ * publish no work, so the bounded waits of every later call expire (a test
+ * of the timeout path that issues no copy and no MMA); 0 restores normal
+ * operation.  Both settings are process-wide. */
+#define MLP_DEBUG_NO_WORK 1
+int mlp_set_wait_timeout_ms(unsigned int ms);
+int mlp_debug_set_flags(int flags);
+
 /* ---- Tracing (timing support; no counterpart on the pages) ----
  * With tracing on, every kernel launch of the calls above is bracketed by
  * a pair of CUDA events recorded on the call's stream (this may keep

@@ -34,7 +34,8 @@ def test_header_declares_the_abi():
                             "mlp_bwd_recompute", "mlp_status_string", "mlp_device_status",
                             "mlp_version", "mlp_trace_enable", "mlp_trace_read",
                             "mlp_kernel_name", "mlp_set_tile_policy",
-                            "mlp_fwd_infer_noalloc"])
+                            "mlp_fwd_infer_noalloc", "mlp_set_wait_timeout_ms",
+                            "mlp_debug_set_flags"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -119,3 +120,9 @@ def test_tile_policy_values(L):
     assert L.mlp_set_tile_policy(-1) == -1
     for v in (1, 2, 0):
         assert L.mlp_set_tile_policy(v) == 0
+
+
+def test_debug_hooks_validate(L):
+    assert L.mlp_debug_set_flags(2) == -1
+    assert L.mlp_debug_set_flags(0) == 0
+    assert L.mlp_set_wait_timeout_ms(0) == 0
