@@ -66,6 +66,13 @@ __device__ __forceinline__ Work decode_unit(const Params& p, int unit) {
 template <int EPI>
 struct EpiTraits {
   static constexpr int TILE_N = (EPI == EPI_GATED_FWD) ? 128 : 256;
+  // outputs staged per chunk (gated fwd: a, G, U; act fwd: a, P; dgated: dG,
+  // dU, a; dact: dP, a; plain: D) and bytes of one staged 32 x 32 box
+  static constexpr int NOUT = (EPI == EPI_GATED_FWD || EPI == EPI_DGATED) ? 3
+                              : (EPI == EPI_ACT_FWD || EPI == EPI_DACT)   ? 2
+                                                                          : 1;
+  static constexpr int OUT_BYTES = (EPI == EPI_ACCUM_F32) ? 4096 : 2048;
+  static constexpr int STG_WARP = NOUT * OUT_BYTES;
 };
 
 __device__ __forceinline__ void record_timeout(const Params& p, volatile int* abort_flag) {
@@ -74,80 +81,119 @@ __device__ __forceinline__ void record_timeout(const Params& p, volatile int* ab
 }
 
 // ---------------------------------------------------------------- epilogues
-// Each thread owns one output row `row` of the tile and walks its columns in
-// chunks of 32 (one tcgen05.ld 32x32b.x32).  tcgen05.ld is warp-collective,
-// so every lane issues it whatever its row's validity.
+// Each thread owns one output row of the tile (TMEM lane = row) and walks its
+// columns in chunks of 32 (one tcgen05.ld 32x32b.x32).  A warp's 32 rows x
+// 32 columns of each output are staged in shared memory and written with
+// one TMA store per output: bf16 boxes (64 B rows) use the 64-byte swizzle,
+// fp32 boxes (128 B rows) the 128-byte swizzle, so that the row-per-thread
+// 16-byte shared stores are free of bank conflicts.  TMA clips the boxes at
+// the tensor's edges.  tcgen05.ld is warp-collective, so every lane issues
+// it whatever its row's validity.
+
+struct EpiWarp {
+  uint32_t stg;  // this warp's staging buffers
+  int lane;
+  int row0;      // first of the warp's 32 rows
+  bool rows_ok;  // any of the 32 rows inside the output
+};
+
+// Stage this lane's 32 bf16 (16 packed words) into a 64B-swizzled 32x32 box.
+__device__ __forceinline__ void stage_bf16(uint32_t buf, int r, const uint32_t (&w)[16]) {
+  const uint32_t rb = buf + static_cast<uint32_t>(r) * 64u;
+  const uint32_t x = (static_cast<uint32_t>(r) >> 1) & 3u;
+#pragma unroll
+  for (uint32_t j = 0; j < 4; ++j)
+    st_shared_v4(rb + ((j ^ x) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+}
+
+// Stage this lane's 32 fp32 values into a 128B-swizzled 32x32 box.
+__device__ __forceinline__ void stage_f32(uint32_t buf, int r, const uint32_t (&w)[32]) {
+  const uint32_t rb = buf + static_cast<uint32_t>(r) * 128u;
+  const uint32_t x = static_cast<uint32_t>(r) & 7u;
+#pragma unroll
+  for (uint32_t j = 0; j < 8; ++j)
+    st_shared_v4(rb + ((j ^ x) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+}
+
+// The staging buffers may be overwritten once the previous chunk's stores
+// have read them.
+__device__ __forceinline__ void staging_acquire(const EpiWarp& e) {
+  if (e.lane == 0) bulk_wait_read_all();
+  __syncwarp();
+}
+
+// Store the staged boxes of outputs whose map exists at (col, row0).
+template <int NOUT, int OUT_BYTES, bool REDUCE>
+__device__ __forceinline__ void flush_chunk(const Params& p, const Prob& P, const EpiWarp& e,
+                                            int col) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (e.lane == 0) {
+#pragma unroll
+    for (int o = 0; o < NOUT; ++o) {
+      if (P.mapO[o] >= 0) {
+        const CUtensorMap* m = &p.maps[P.mapO[o]];
+        if constexpr (REDUCE) tma_reduce_add_2d(m, e.stg + o * OUT_BYTES, col, e.row0);
+        else tma_store_2d(m, e.stg + o * OUT_BYTES, col, e.row0);
+      }
+    }
+    bulk_commit();
+  }
+}
 
 template <int ACT>
-__device__ __forceinline__ void epi_gated_fwd(const Params& p, const Prob& P, uint32_t tb, int row,
-                                              int col0, int cb, int ce) {
-  const bool row_ok = row < P.M;
+__device__ __forceinline__ void epi_gated_fwd(const Params& p, const Prob& P, const EpiWarp& e,
+                                              uint32_t tb, int col0, int cb, int ce) {
   const float s = p.scale;
-  __nv_bfloat16* a_out = static_cast<__nv_bfloat16*>(P.out0);
-  __nv_bfloat16* g_out = static_cast<__nv_bfloat16*>(P.out1);
-  __nv_bfloat16* u_out = static_cast<__nv_bfloat16*>(P.out2);
 #pragma unroll 1
   for (int c = cb; c < ce; c += 32) {
+    const int col = col0 + c;
+    if (col >= P.N) break;  // warp-uniform
     uint32_t g[32], u[32];
     __syncwarp();
     tmem_ld32(tb + c, g);
     tmem_ld32(tb + 128 + c, u);
     tmem_wait_ld();
-    const int col = col0 + c;
-    if (row_ok && col < P.N) {
-      const size_t off = static_cast<size_t>(row) * P.ld + col;
+    uint32_t pa[16], pg[16], pu[16];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        if (col + 8 * v < P.N) {
-          uint32_t pa[4], pg[4], pu[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float g0 = __uint_as_float(g[8 * v + 2 * j]), g1 = __uint_as_float(g[8 * v + 2 * j + 1]);
-            float u0 = __uint_as_float(u[8 * v + 2 * j]), u1 = __uint_as_float(u[8 * v + 2 * j + 1]);
-            pa[j] = pack_bf16x2(s * act_f<ACT>(g0) * u0, s * act_f<ACT>(g1) * u1);
-            pg[j] = pack_bf16x2(g0, g1);
-            pu[j] = pack_bf16x2(u0, u1);
-          }
-          if (a_out) st_global_v4(a_out + off + 8 * v, make_uint4(pa[0], pa[1], pa[2], pa[3]));
-          if (g_out) st_global_v4(g_out + off + 8 * v, make_uint4(pg[0], pg[1], pg[2], pg[3]));
-          if (u_out) st_global_v4(u_out + off + 8 * v, make_uint4(pu[0], pu[1], pu[2], pu[3]));
-        }
-      }
+    for (int j = 0; j < 16; ++j) {
+      const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+      const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+      pa[j] = pack_bf16x2(s * act_f<ACT>(g0) * u0, s * act_f<ACT>(g1) * u1);
+      pg[j] = pack_bf16x2(g0, g1);
+      pu[j] = pack_bf16x2(u0, u1);
     }
+    staging_acquire(e);
+    stage_bf16(e.stg, e.lane, pa);
+    if (P.mapO[1] >= 0) stage_bf16(e.stg + 2048, e.lane, pg);
+    if (P.mapO[2] >= 0) stage_bf16(e.stg + 4096, e.lane, pu);
+    flush_chunk<3, 2048, false>(p, P, e, col);
   }
 }
 
 template <int ACT>
-__device__ __forceinline__ void epi_act_fwd(const Params& p, const Prob& P, uint32_t tb, int row,
-                                            int col0, int cb, int ce) {
-  const bool row_ok = row < P.M;
+__device__ __forceinline__ void epi_act_fwd(const Params& p, const Prob& P, const EpiWarp& e,
+                                            uint32_t tb, int col0, int cb, int ce) {
   const float s = p.scale;
-  __nv_bfloat16* a_out = static_cast<__nv_bfloat16*>(P.out0);
-  __nv_bfloat16* p_out = static_cast<__nv_bfloat16*>(P.out1);
 #pragma unroll 1
   for (int c = cb; c < ce; c += 32) {
+    const int col = col0 + c;
+    if (col >= P.N) break;
     uint32_t z[32];
     __syncwarp();
     tmem_ld32(tb + c, z);
     tmem_wait_ld();
-    const int col = col0 + c;
-    if (row_ok && col < P.N) {
-      const size_t off = static_cast<size_t>(row) * P.ld + col;
+    uint32_t pa[16], pp[16];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        if (col + 8 * v < P.N) {
-          uint32_t pa[4], pp[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float z0 = __uint_as_float(z[8 * v + 2 * j]), z1 = __uint_as_float(z[8 * v + 2 * j + 1]);
-            pa[j] = pack_bf16x2(s * act_f<ACT>(z0), s * act_f<ACT>(z1));
-            pp[j] = pack_bf16x2(z0, z1);
-          }
-          if (a_out) st_global_v4(a_out + off + 8 * v, make_uint4(pa[0], pa[1], pa[2], pa[3]));
-          if (p_out) st_global_v4(p_out + off + 8 * v, make_uint4(pp[0], pp[1], pp[2], pp[3]));
-        }
-      }
+    for (int j = 0; j < 16; ++j) {
+      const float z0 = __uint_as_float(z[2 * j]), z1 = __uint_as_float(z[2 * j + 1]);
+      pa[j] = pack_bf16x2(s * act_f<ACT>(z0), s * act_f<ACT>(z1));
+      pp[j] = pack_bf16x2(z0, z1);
     }
+    staging_acquire(e);
+    stage_bf16(e.stg, e.lane, pa);
+    if (P.mapO[1] >= 0) stage_bf16(e.stg + 2048, e.lane, pp);
+    flush_chunk<2, 2048, false>(p, P, e, col);
   }
 }
 
@@ -167,62 +213,65 @@ __device__ __forceinline__ void dact_load(const Prob& P, int row, int col, uint4
   }
 }
 
-// GATED = true: in0 = G, in1 = U -> out0 = dG, out1 = dU, out2 = a (optional)
-// GATED = false: in0 = P -> out0 = dP, out2 = a (optional)
+// GATED = true: in0 = G, in1 = U -> outputs dG, dU, a (maps 0, 1, 2)
+// GATED = false: in0 = P -> outputs dP, a (maps 0, 1)
 // The saved preacts of chunk c+1 are loaded while chunk c is computed; the
 // caller has already loaded chunk `cb` into (pg, pu) before waiting for the
-// accumulator.  In-place outputs are safe: each thread reads an element
-// before it writes it, and no other thread touches it.
+// accumulator.  In-place outputs are safe: every element is read (global
+// load) before the TMA store of its chunk is issued, and chunks do not
+// overlap.
 template <int ACT, bool GATED>
-__device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, uint32_t tb, int row,
-                                         int col0, int cb, int ce, uint4 (&pg)[4],
+__device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, const EpiWarp& e,
+                                         uint32_t tb, int col0, int cb, int ce, uint4 (&pg)[4],
                                          uint4 (&pu)[4]) {
-  const bool row_ok = row < P.M;
   const float s = p.scale;
-  __nv_bfloat16* dg_out = static_cast<__nv_bfloat16*>(P.out0);
-  __nv_bfloat16* du_out = static_cast<__nv_bfloat16*>(P.out1);
-  __nv_bfloat16* a_out = static_cast<__nv_bfloat16*>(P.out2);
+  const int row = e.row0 + e.lane;
+  constexpr int NOUT = GATED ? 3 : 2;
+  const uint32_t a_buf = e.stg + (NOUT - 1) * 2048;
 #pragma unroll 1
   for (int c = cb; c < ce; c += 32) {
+    const int col = col0 + c;
+    if (col >= P.N) break;
     uint4 ng[4], nu[4];
-    if (c + 32 < ce) dact_load<GATED>(P, row, col0 + c + 32, ng, nu);
+    if (c + 32 < ce) dact_load<GATED>(P, row, col + 32, ng, nu);
     uint32_t d[32];
     __syncwarp();
     tmem_ld32(tb + c, d);
     tmem_wait_ld();
-    const int col = col0 + c;
-    if (row_ok && col < P.N) {
-      const size_t off = static_cast<size_t>(row) * P.ld + col;
+    // one 8-column group (one swizzled 16-byte unit per output) at a time
+    staging_acquire(e);
+    const bool want_a = P.mapO[NOUT - 1] >= 0;
+    const uint32_t rb = static_cast<uint32_t>(e.lane) * 64u;
+    const uint32_t x = (static_cast<uint32_t>(e.lane) >> 1) & 3u;
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        if (col + 8 * v < P.N) {
-          const uint32_t gw[4] = {pg[v].x, pg[v].y, pg[v].z, pg[v].w};
-          const uint32_t uw[4] = {pu[v].x, pu[v].y, pu[v].z, pu[v].w};
-          uint32_t pdg[4], pdu[4], pa[4];
+    for (int v = 0; v < 4; ++v) {
+      const uint32_t gw[4] = {pg[v].x, pg[v].y, pg[v].z, pg[v].w};
+      const uint32_t uw[4] = {pu[v].x, pu[v].y, pu[v].z, pu[v].w};
+      uint32_t pdg[4], pdu[4], pa[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float2 gg = unpack_bf16x2(gw[j]);
-            float dh0 = s * __uint_as_float(d[8 * v + 2 * j]);
-            float dh1 = s * __uint_as_float(d[8 * v + 2 * j + 1]);
-            float a0, da0, a1, da1;
-            act_and_grad<ACT>(gg.x, a0, da0);
-            act_and_grad<ACT>(gg.y, a1, da1);
-            if (GATED) {
-              float2 uu = unpack_bf16x2(uw[j]);
-              pdg[j] = pack_bf16x2(dh0 * uu.x * da0, dh1 * uu.y * da1);
-              pdu[j] = pack_bf16x2(dh0 * a0, dh1 * a1);
-              pa[j] = pack_bf16x2(s * a0 * uu.x, s * a1 * uu.y);
-            } else {
-              pdg[j] = pack_bf16x2(dh0 * da0, dh1 * da1);
-              pa[j] = pack_bf16x2(s * a0, s * a1);
-            }
-          }
-          st_global_v4(dg_out + off + 8 * v, make_uint4(pdg[0], pdg[1], pdg[2], pdg[3]));
-          if (GATED) st_global_v4(du_out + off + 8 * v, make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]));
-          if (a_out) st_global_v4(a_out + off + 8 * v, make_uint4(pa[0], pa[1], pa[2], pa[3]));
+      for (int j = 0; j < 4; ++j) {
+        const float2 gg = unpack_bf16x2(gw[j]);
+        const float dh0 = s * __uint_as_float(d[8 * v + 2 * j]);
+        const float dh1 = s * __uint_as_float(d[8 * v + 2 * j + 1]);
+        float a0, da0, a1, da1;
+        act_and_grad<ACT>(gg.x, a0, da0);
+        act_and_grad<ACT>(gg.y, a1, da1);
+        if (GATED) {
+          const float2 uu = unpack_bf16x2(uw[j]);
+          pdg[j] = pack_bf16x2(dh0 * uu.x * da0, dh1 * uu.y * da1);
+          pdu[j] = pack_bf16x2(dh0 * a0, dh1 * a1);
+          pa[j] = pack_bf16x2(s * a0 * uu.x, s * a1 * uu.y);
+        } else {
+          pdg[j] = pack_bf16x2(dh0 * da0, dh1 * da1);
+          pa[j] = pack_bf16x2(s * a0, s * a1);
         }
       }
+      const uint32_t unit = rb + ((static_cast<uint32_t>(v) ^ x) << 4);
+      st_shared_v4(e.stg + unit, pdg[0], pdg[1], pdg[2], pdg[3]);
+      if (GATED) st_shared_v4(e.stg + 2048 + unit, pdu[0], pdu[1], pdu[2], pdu[3]);
+      if (want_a) st_shared_v4(a_buf + unit, pa[0], pa[1], pa[2], pa[3]);
     }
+    flush_chunk<NOUT, 2048, false>(p, P, e, col);
     if (c + 32 < ce) {
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
@@ -234,45 +283,27 @@ __device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, uint32_
 }
 
 template <int EPI>
-__device__ __forceinline__ void epi_plain(const Prob& P, uint32_t tb, int row, int col0, int cb,
-                                          int ce) {
-  const bool row_ok = row < P.M;
+__device__ __forceinline__ void epi_plain(const Params& p, const Prob& P, const EpiWarp& e,
+                                          uint32_t tb, int col0, int cb, int ce) {
 #pragma unroll 1
   for (int c = cb; c < ce; c += 32) {
+    const int col = col0 + c;
+    if (col >= P.N) break;
     uint32_t d[32];
     __syncwarp();
     tmem_ld32(tb + c, d);
     tmem_wait_ld();
-    const int col = col0 + c;
-    if (row_ok && col < P.N) {
-      const size_t off = static_cast<size_t>(row) * P.ld + col;
-      if constexpr (EPI == EPI_STORE_BF16) {
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(P.out0);
+    staging_acquire(e);
+    if constexpr (EPI == EPI_STORE_BF16) {
+      uint32_t q[16];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          if (col + 8 * v < P.N) {
-            uint32_t q[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              q[j] = pack_bf16x2(__uint_as_float(d[8 * v + 2 * j]),
-                                 __uint_as_float(d[8 * v + 2 * j + 1]));
-            st_global_v4(o + off + 8 * v, make_uint4(q[0], q[1], q[2], q[3]));
-          }
-        }
-      } else {
-        float* o = static_cast<float*>(P.out0);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          if (col + 8 * v < P.N) {
-            red_add_v4_f32(o + off + 8 * v, __uint_as_float(d[8 * v + 0]),
-                           __uint_as_float(d[8 * v + 1]), __uint_as_float(d[8 * v + 2]),
-                           __uint_as_float(d[8 * v + 3]));
-            red_add_v4_f32(o + off + 8 * v + 4, __uint_as_float(d[8 * v + 4]),
-                           __uint_as_float(d[8 * v + 5]), __uint_as_float(d[8 * v + 6]),
-                           __uint_as_float(d[8 * v + 7]));
-          }
-        }
-      }
+      for (int j = 0; j < 16; ++j)
+        q[j] = pack_bf16x2(__uint_as_float(d[2 * j]), __uint_as_float(d[2 * j + 1]));
+      stage_bf16(e.stg, e.lane, q);
+      flush_chunk<1, 2048, false>(p, P, e, col);
+    } else {
+      stage_f32(e.stg, e.lane, d);
+      flush_chunk<1, 4096, true>(p, P, e, col);
     }
   }
 }
@@ -282,15 +313,22 @@ __device__ __forceinline__ void epi_plain(const Prob& P, uint32_t tb, int row, i
 // stages all 256 B rows.  CG = 2: a CTA pair computes a 256 x 256 tile with
 // one tcgen05.mma.cta_group::2; each CTA stages its own 128 A rows and 128
 // of the 256 B rows, so a stage is 32 KB and six fit in shared memory.
-template <int CG>
+// After the stage ring come the epilogue warps' staging buffers; the ring
+// takes as many stages as fit beside them in the 227 KB of shared memory.
+template <int EPI, int CG>
 struct Cfg {
   static constexpr int B_ROWS = CG == 2 ? 128 : 256;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = CG == 2 ? 6 : 4;
+  static constexpr int STG = NUM_EPI_WARPS * EpiTraits<EPI>::STG_WARP;
+  static constexpr int MAX_SMEM = 232448;  // per-block opt-in limit
+  static constexpr int FIT = (MAX_SMEM - 2048 - STG) / STAGE;
+  static constexpr int STAGES = FIT < 8 ? FIT : 8;
   static constexpr int TILE_M = BM * CG;
-  static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 1024 /*barriers, ring*/;
+  static constexpr int SMEM = STAGES * STAGE + STG + 1024 /*align*/ + 1024 /*barriers, ring*/;
+  static_assert(STAGES >= 2, "stage ring too small");
+  static_assert(SMEM <= MAX_SMEM, "shared memory over the limit");
 };
 
 // Issues the TMA boxes of one k-block into this CTA's stage (A at sA, B at
@@ -337,7 +375,7 @@ __device__ __forceinline__ void load_stage(const Params& p, const Prob& P, const
 template <int EPI, bool A_MN, bool B_MN, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
-  using C = Cfg<CG>;
+  using C = Cfg<EPI, CG>;
   constexpr bool PAIR = CG == 2;
   constexpr int TILE_N = EpiTraits<EPI>::TILE_N;
   constexpr uint32_t IDESC = idesc_bf16(C::TILE_M, MMA_N, A_MN, B_MN);
@@ -346,7 +384,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
   uint8_t* base_g = smem_raw + (base_s - raw_s);
-  uint8_t* ctrl = base_g + C::STAGES * C::STAGE;
+  const uint32_t stg_s = base_s + C::STAGES * C::STAGE;  // epilogue staging
+  uint8_t* ctrl = base_g + C::STAGES * C::STAGE + C::STG;
   uint64_t* bar = reinterpret_cast<uint64_t*>(ctrl);
   // barrier indices (same offsets in both CTAs of a pair)
   constexpr int FULL = 0, EMPTY = C::STAGES, TFULL = 2 * C::STAGES, TEMPTY = 2 * C::STAGES + 2,
@@ -559,8 +598,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quadrant this warp may access
     const int half = (warp - 2) >> 2;  // which half of the tile's columns
-    const int row_in_tile = static_cast<int>(rank) * BM + q * 32 + lane;
     const int cb = half * (TILE_N / 2), ce = cb + TILE_N / 2;
+    EpiWarp e;
+    e.stg = stg_s + static_cast<uint32_t>(warp - 2) * EpiTraits<EPI>::STG_WARP;
+    e.lane = lane;
     int slot = 0;
     uint32_t sphase = 0;
     int acc = 0;
@@ -580,12 +621,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       if (unit < 0) break;
       const Work w = decode_unit(p, unit);
       const Prob& P = p.prob[w.prob];
-      const int row = w.tm * C::TILE_M + row_in_tile;
+      e.row0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
+      e.rows_ok = e.row0 < P.M;
       const int col0 = w.tn * TILE_N;
       uint4 pg[4], pu[4];
       if constexpr (EPI == EPI_DGATED || EPI == EPI_DACT) {
         // the saved preacts do not depend on the MMAs: fetch the first chunk now
-        dact_load<EPI == EPI_DGATED>(P, row, col0 + cb, pg, pu);
+        if (e.rows_ok) dact_load<EPI == EPI_DGATED>(P, e.row0 + lane, col0 + cb, pg, pu);
       }
       if (!mbar_wait<PAIR>(bar_s(TFULL + acc), aphase, lim, abort_flag)) {
         record_timeout(p, abort_flag);
@@ -593,18 +635,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       }
       tc_fence_after();
       const uint32_t tb = tmem + acc * MMA_N + (static_cast<uint32_t>(q * 32) << 16);
-      if constexpr (EPI == EPI_GATED_FWD) {
-        epi_gated_fwd<ACT_SILU>(p, P, tb, row, col0, cb, ce);
-      } else if constexpr (EPI == EPI_ACT_FWD) {
-        if (p.act == ACT_RELU_SQ) epi_act_fwd<ACT_RELU_SQ>(p, P, tb, row, col0, cb, ce);
-        else epi_act_fwd<ACT_GELU_TANH>(p, P, tb, row, col0, cb, ce);
-      } else if constexpr (EPI == EPI_DGATED) {
-        epi_dact<ACT_SILU, true>(p, P, tb, row, col0, cb, ce, pg, pu);
-      } else if constexpr (EPI == EPI_DACT) {
-        if (p.act == ACT_RELU_SQ) epi_dact<ACT_RELU_SQ, false>(p, P, tb, row, col0, cb, ce, pg, pu);
-        else epi_dact<ACT_GELU_TANH, false>(p, P, tb, row, col0, cb, ce, pg, pu);
-      } else {
-        epi_plain<EPI>(P, tb, row, col0, cb, ce);
+      if (e.rows_ok) {  // warp-uniform: rows past the output need no epilogue
+        if constexpr (EPI == EPI_GATED_FWD) {
+          epi_gated_fwd<ACT_SILU>(p, P, e, tb, col0, cb, ce);
+        } else if constexpr (EPI == EPI_ACT_FWD) {
+          if (p.act == ACT_RELU_SQ) epi_act_fwd<ACT_RELU_SQ>(p, P, e, tb, col0, cb, ce);
+          else epi_act_fwd<ACT_GELU_TANH>(p, P, e, tb, col0, cb, ce);
+        } else if constexpr (EPI == EPI_DGATED) {
+          epi_dact<ACT_SILU, true>(p, P, e, tb, col0, cb, ce, pg, pu);
+        } else if constexpr (EPI == EPI_DACT) {
+          if (p.act == ACT_RELU_SQ) epi_dact<ACT_RELU_SQ, false>(p, P, e, tb, col0, cb, ce, pg, pu);
+          else epi_dact<ACT_GELU_TANH, false>(p, P, e, tb, col0, cb, ce, pg, pu);
+        } else {
+          epi_plain<EPI>(p, P, e, tb, col0, cb, ce);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -615,6 +659,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       acc ^= 1;
       if (acc == 0) aphase ^= 1u;
     }
+    // the last stores must finish before the kernel (and its shared memory) ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -634,7 +681,7 @@ cudaError_t launch_gemm(const Params& p, int grid, cudaStream_t stream, bool pdl
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 31 || !(configured_dev_mask.load() & (1u << dev))) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<CG>::SMEM);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<EPI, CG>::SMEM);
     if (e != cudaSuccess) return e;
     if (CG == 2) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
@@ -645,7 +692,7 @@ cudaError_t launch_gemm(const Params& p, int grid, cudaStream_t stream, bool pdl
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<CG>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<EPI, CG>::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int na = 0;
@@ -674,13 +721,13 @@ int max_groups() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   if (CG == 1) return sms;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<CG>::SMEM) !=
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<EPI, CG>::SMEM) !=
       cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<CG>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<EPI, CG>::SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;

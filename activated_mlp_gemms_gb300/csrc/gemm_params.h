@@ -41,7 +41,7 @@ struct Prob {
   int mapA0, mapB0;       // tensor maps of segment 0
   int mapA1, mapB1;       // segment 1 (EPI_GATED_FWD: mapB1 = the up weight)
   int ld;                 // row pitch (elements) of the epilogue's outputs and inputs
-  int pad_;
+  int mapO[3];            // tensor maps of the epilogue's outputs (-1: output not written)
   void* out0;
   void* out1;
   void* out2;

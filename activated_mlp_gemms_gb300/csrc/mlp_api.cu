@@ -58,9 +58,10 @@ struct MapKey {
   const void* ptr;
   uint64_t inner, outer, stride;
   uint32_t box0, box1;
+  int dtype, swizzle;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && inner == o.inner && outer == o.outer && stride == o.stride &&
-           box0 == o.box0 && box1 == o.box1;
+           box0 == o.box0 && box1 == o.box1 && dtype == o.dtype && swizzle == o.swizzle;
   }
 };
 struct MapKeyHash {
@@ -70,18 +71,22 @@ struct MapKeyHash {
     h = h * 1000003u ^ k.outer;
     h = h * 1000003u ^ k.stride;
     h = h * 1000003u ^ (static_cast<size_t>(k.box0) << 16 | k.box1);
+    h = h * 1000003u ^ (static_cast<size_t>(k.dtype) << 8 | static_cast<size_t>(k.swizzle));
     return h;
   }
 };
 std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
 
-// 2-D bf16 tensor map over a row-major [outer, inner] array with row pitch
-// `pitch` elements, box {box0 (inner), box1 (outer)}, 128-byte swizzle,
-// out-of-bounds elements read as zero.
+// 2-D tensor map over a row-major [outer, inner] array with row pitch `pitch`
+// elements, box {box0 (inner), box1 (outer)}; out-of-bounds elements read as
+// zero and are not written.  bf16 operands use the 128-byte swizzle; the
+// epilogue's 32 x 32 output boxes use the 64-byte (bf16) or 128-byte (fp32)
+// swizzle of the staging buffers.
 bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch,
-              uint32_t box0, uint32_t box1) {
-  MapKey key{ptr, inner, outer, pitch, box0, box1};
+              uint32_t box0, uint32_t box1, bool f32 = false,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+  MapKey key{ptr, inner, outer, pitch, box0, box1, f32 ? 1 : 0, static_cast<int>(swz)};
   {
     std::lock_guard<std::mutex> lk(g_map_mu);
     auto it = g_map_cache.find(key);
@@ -91,14 +96,15 @@ bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
     }
   }
   if (!encode_fn_ok()) return false;
+  const uint64_t esize = f32 ? 4 : 2;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {pitch * 2};
+  cuuint64_t strides[1] = {pitch * esize};
   cuuint32_t box[2] = {box0, box1};
   cuuint32_t estr[2] = {1, 1};
   CUtensorMap m;
-  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  CUresult r = g_encode(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   std::lock_guard<std::mutex> lk(g_map_mu);
@@ -174,6 +180,16 @@ struct Gemm {
     if (!make_map(&p.maps[nmaps], ptr, MN, K, MN, 64, BK)) ok = false;
     return nmaps++;
   }
+  // Epilogue output [rows, cols] (row pitch cols), stored in 32 x 32 boxes;
+  // -1 when the output is not requested.
+  int output(void* ptr, int rows, int cols, bool f32 = false) {
+    if (!ptr) return -1;
+    if (nmaps >= MAX_MAPS) { ok = false; return -1; }
+    if (!make_map(&p.maps[nmaps], ptr, cols, rows, cols, 32, 32, f32,
+                  f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+      ok = false;
+    return nmaps++;
+  }
   Prob& add(int M, int N, int K0, int K1, int tile_n, int ksplit = 1) {
     Prob& P = p.prob[p.nprob++];
     P.M = M;
@@ -191,6 +207,7 @@ struct Gemm {
     P.units = P.tiles_m * P.tiles_n * P.ksplit;
     p.total_units += P.units;
     P.ld = N;
+    P.mapO[0] = P.mapO[1] = P.mapO[2] = -1;
     return P;
   }
   // B rows per K-major box: a CTA stages 256 / cg of the 256 B rows
@@ -351,21 +368,26 @@ int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* W
   if (gated(p)) {
     const int mG = g.kmajor(Wg, p->I, p->H, 128);
     const int mU = g.kmajor(Wu, p->I, p->H, 128);
+    const int oA = g.output(a_out, p->M, p->I);
+    const int oG = g.output(G_out, p->M, p->I);
+    const int oU = g.output(U_out, p->M, p->I);
     Prob& P = g.add(p->M, p->I, p->H, 0, 128);
     P.mapA0 = mA;
     P.mapB0 = mG;
     P.mapB1 = mU;
-    P.out0 = a_out;
-    P.out1 = G_out;
-    P.out2 = U_out;
+    P.mapO[0] = oA;
+    P.mapO[1] = oG;
+    P.mapO[2] = oU;
     return run<EPI_GATED_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
   }
   const int mW = g.kmajor(Wg, p->I, p->H, g.b_rows());
+  const int oA = g.output(a_out, p->M, p->I);
+  const int oP = g.output(G_out, p->M, p->I);
   Prob& P = g.add(p->M, p->I, p->H, 0, MMA_N);
   P.mapA0 = mA;
   P.mapB0 = mW;
-  P.out0 = a_out;
-  P.out1 = G_out;
+  P.mapO[0] = oA;
+  P.mapO[1] = oP;
   return run<EPI_ACT_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
 }
 
@@ -374,10 +396,11 @@ int launch_down(const mlp_problem_t* p, Call& c, const void* a, const void* Wd, 
   Gemm g(*p, c.counter(), c.status, pick_cg(p->M));
   const int mA = g.kmajor(a, p->M, p->I, BM);
   const int mB = g.kmajor(Wd, p->H, p->I, g.b_rows());
+  const int oO = g.output(out, p->M, p->H);
   Prob& P = g.add(p->M, p->H, p->I, 0, MMA_N);
   P.mapA0 = mA;
   P.mapB0 = mB;
-  P.out0 = out;
+  P.mapO[0] = oO;
   return run<EPI_STORE_BF16, false, false>(g, c, MLP_KERNEL_DOWN);
 }
 
@@ -445,14 +468,23 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     Gemm g(*p, c.counter(), c.status, pick_cg(M));
     const int mA = g.kmajor(dout, M, H, BM);
     const int mB = g.mnmajor(Wd, H, I);  // Wd [H,I]: B(n=i, k=h) is N-contiguous
+    void* a_out = (dWd && !recompute) ? a : nullptr;
+    const int oG = g.output(G, M, I);
+    const int oU = gated(p) ? g.output(U, M, I) : -1;
+    const int oA = g.output(a_out, M, I);
     Prob& P = g.add(M, I, H, 0, MMA_N);
     P.mapA0 = mA;
     P.mapB0 = mB;
     P.in0 = G;
     P.in1 = U;
-    P.out0 = G;
-    P.out1 = U;
-    P.out2 = (dWd && !recompute) ? a : nullptr;
+    // gated: dG, dU, a;  non-gated: dP, a
+    P.mapO[0] = oG;
+    if (gated(p)) {
+      P.mapO[1] = oU;
+      P.mapO[2] = oA;
+    } else {
+      P.mapO[1] = oA;
+    }
     MLP_TRY(gated(p) ? run<EPI_DGATED, false, true>(g, c, MLP_KERNEL_DGATED)
                      : run<EPI_DACT, false, true>(g, c, MLP_KERNEL_DGATED));
   } else if (!recompute) {
@@ -476,12 +508,13 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
       mA1 = g.kmajor(dU, M, I, BM);
       mB1 = g.mnmajor(Wu, I, H);
     }
+    const int oX = g.output(dx, M, H);
     Prob& P = g.add(M, H, I, gated(p) ? I : 0, MMA_N);
     P.mapA0 = mA0;
     P.mapB0 = mB0;
     P.mapA1 = mA1;
     P.mapB1 = mB1;
-    P.out0 = dx;
+    P.mapO[0] = oX;
     MLP_TRY((run<EPI_STORE_BF16, false, true>(g, c, MLP_KERNEL_DX)));
   }
 
@@ -511,10 +544,11 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     for (int i = 0; i < n; ++i) {
       const int mA = g.mnmajor(list[i].A, M, list[i].rows);
       const int mB = g.mnmajor(list[i].B, M, list[i].cols);
+      const int oW = g.output(list[i].out, list[i].rows, list[i].cols, fuse != 0);
       Prob& P = g.add(list[i].rows, list[i].cols, M, 0, MMA_N, ksplit);
       P.mapA0 = mA;
       P.mapB0 = mB;
-      P.out0 = list[i].out;
+      P.mapO[0] = oW;
     }
     if (fuse) {
       MLP_TRY((run<EPI_ACCUM_F32, true, true>(g, c, MLP_KERNEL_WGRAD)));
