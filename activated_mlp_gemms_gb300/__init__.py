@@ -29,7 +29,9 @@ __all__ = [
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmlp.so")
 
-ACTS = {"swiglu": 0, "relu_sq": 1, "gelu_tanh_approx": 2}
+ACTS = {"swiglu": 0, "relu_sq": 1, "gelu_tanh_approx": 2, "relu": 3, "reglu": 4, "geglu": 5,
+        "glu": 6}
+GATED_ACTS = ("swiglu", "reglu", "geglu", "glu")
 MODE_FWD, MODE_INFER, MODE_BWD, MODE_BWD_RECOMPUTE = 0, 1, 2, 3
 NOALLOC_SCRATCH_BYTES = 16 << 20  # MLP_NOALLOC_SCRATCH_BYTES
 DEBUG_NO_WORK = 1  # MLP_DEBUG_NO_WORK

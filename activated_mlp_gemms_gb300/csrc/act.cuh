@@ -4,6 +4,8 @@
 //   relu2(z) = max(z,0)^2                relu2'(z) = 2 max(z,0)
 //   gelu_tanh(z) = 0.5 z (1 + t),  t = tanh(c (z + 0.044715 z^3)),  c = sqrt(2/pi)
 //   gelu_tanh'(z) = 0.5 (1 + t) + 0.5 z (1 - t^2) c (1 + 3*0.044715 z^2)
+//   relu(z)  = max(z,0)                  relu'(z)  = 1 for z > 0, else 0
+//   sigmoid(z) = 1 / (1 + e^-z)          sigmoid'(z) = s (1 - s)
 // (tanh approximation of GELU: Hendrycks & Gimpel, 2016).  sigmoid uses
 // CUDA's __expf; tanh uses CUDA's tanhf.
 #pragma once
@@ -22,6 +24,10 @@ __device__ __forceinline__ float act_f(float z) {
   } else if constexpr (ACT == ACT_RELU_SQ) {
     float r = fmaxf(z, 0.0f);
     return r * r;
+  } else if constexpr (ACT == ACT_RELU) {
+    return fmaxf(z, 0.0f);
+  } else if constexpr (ACT == ACT_SIGMOID) {
+    return sigmoid_f(z);
   } else {
     const float c = 0.7978845608028654f;  // sqrt(2/pi)
     float t = tanhf(c * fmaf(0.044715f * z, z * z, z));
@@ -40,6 +46,13 @@ __device__ __forceinline__ void act_and_grad(float z, float& a, float& da) {
     float r = fmaxf(z, 0.0f);
     a = r * r;
     da = 2.0f * r;
+  } else if constexpr (ACT == ACT_RELU) {
+    a = fmaxf(z, 0.0f);
+    da = z > 0.0f ? 1.0f : 0.0f;
+  } else if constexpr (ACT == ACT_SIGMOID) {
+    const float s = sigmoid_f(z);
+    a = s;
+    da = s * (1.0f - s);
   } else {
     const float c = 0.7978845608028654f;
     const float k = 0.044715f;

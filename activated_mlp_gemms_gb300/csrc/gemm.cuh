@@ -72,6 +72,7 @@ struct EpiTraits {
                               : (EPI == EPI_ACT_FWD || EPI == EPI_DACT)   ? 2
                                                                           : 1;
   static constexpr int OUT_BYTES = (EPI == EPI_ACCUM_F32) ? 4096 : 2048;
+  static constexpr bool DACT = (EPI == EPI_DGATED || EPI == EPI_DACT);
   static constexpr int STG_WARP = NOUT * OUT_BYTES;
 };
 
@@ -372,7 +373,8 @@ __device__ __forceinline__ void load_stage(const Params& p, const Prob& P, const
   }
 }
 
-template <int EPI, bool A_MN, bool B_MN, int CG>
+// ACT: the activation of the activation epilogues (Act; 0 for the others).
+template <int EPI, bool A_MN, bool B_MN, int CG, int ACT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   using C = Cfg<EPI, CG>;
@@ -625,7 +627,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       e.rows_ok = e.row0 < P.M;
       const int col0 = w.tn * TILE_N;
       uint4 pg[4], pu[4];
-      if constexpr (EPI == EPI_DGATED || EPI == EPI_DACT) {
+      if constexpr (EpiTraits<EPI>::DACT) {
         // the saved preacts do not depend on the MMAs: fetch the first chunk now
         if (e.rows_ok) dact_load<EPI == EPI_DGATED>(P, e.row0 + lane, col0 + cb, pg, pu);
       }
@@ -637,15 +639,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       const uint32_t tb = tmem + acc * MMA_N + (static_cast<uint32_t>(q * 32) << 16);
       if (e.rows_ok) {  // warp-uniform: rows past the output need no epilogue
         if constexpr (EPI == EPI_GATED_FWD) {
-          epi_gated_fwd<ACT_SILU>(p, P, e, tb, col0, cb, ce);
+          epi_gated_fwd<ACT>(p, P, e, tb, col0, cb, ce);
         } else if constexpr (EPI == EPI_ACT_FWD) {
-          if (p.act == ACT_RELU_SQ) epi_act_fwd<ACT_RELU_SQ>(p, P, e, tb, col0, cb, ce);
-          else epi_act_fwd<ACT_GELU_TANH>(p, P, e, tb, col0, cb, ce);
+          epi_act_fwd<ACT>(p, P, e, tb, col0, cb, ce);
         } else if constexpr (EPI == EPI_DGATED) {
-          epi_dact<ACT_SILU, true>(p, P, e, tb, col0, cb, ce, pg, pu);
+          epi_dact<ACT, true>(p, P, e, tb, col0, cb, ce, pg, pu);
         } else if constexpr (EPI == EPI_DACT) {
-          if (p.act == ACT_RELU_SQ) epi_dact<ACT_RELU_SQ, false>(p, P, e, tb, col0, cb, ce, pg, pu);
-          else epi_dact<ACT_GELU_TANH, false>(p, P, e, tb, col0, cb, ce, pg, pu);
+          epi_dact<ACT, false>(p, P, e, tb, col0, cb, ce, pg, pu);
         } else {
           epi_plain<EPI>(p, P, e, tb, col0, cb, ce);
         }
@@ -673,9 +673,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
   }
 }
 
-template <int EPI, bool A_MN, bool B_MN, int CG>
+template <int EPI, bool A_MN, bool B_MN, int CG, int ACT>
 cudaError_t launch_gemm(const Params& p, int grid, cudaStream_t stream, bool pdl) {
-  auto kern = k_mlp_gemm<EPI, A_MN, B_MN, CG>;
+  auto kern = k_mlp_gemm<EPI, A_MN, B_MN, CG, ACT>;
   static std::atomic<unsigned> configured_dev_mask{0};  // devices that got the smem attribute
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -714,9 +714,9 @@ cudaError_t launch_gemm(const Params& p, int grid, cudaStream_t stream, bool pdl
 }
 
 // Largest number of CTA pairs that can be co-resident (0 on error).
-template <int EPI, bool A_MN, bool B_MN, int CG>
+template <int EPI, bool A_MN, bool B_MN, int CG, int ACT>
 int max_groups() {
-  auto kern = k_mlp_gemm<EPI, A_MN, B_MN, CG>;
+  auto kern = k_mlp_gemm<EPI, A_MN, B_MN, CG, ACT>;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;

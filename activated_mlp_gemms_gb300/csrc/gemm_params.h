@@ -29,7 +29,8 @@ enum Epi : int {
   EPI_ACCUM_F32 = 5    // D += acc (fp32, atomic add; split-K safe)
 };
 
-enum Act : int { ACT_SILU = 0, ACT_RELU_SQ = 1, ACT_GELU_TANH = 2 };
+// The function applied to the gate (gated MLPs) or to the preact (non-gated).
+enum Act : int { ACT_SILU = 0, ACT_RELU_SQ = 1, ACT_GELU_TANH = 2, ACT_RELU = 3, ACT_SIGMOID = 4 };
 
 // One GEMM D[M,N] = sum_k A[m,k] B[n,k] of a (possibly grouped) launch.
 struct Prob {
@@ -68,12 +69,14 @@ struct Params {  // 64-byte aligned through CUtensorMap
 // Host-side launcher and co-residency query, explicitly instantiated in the
 // kernel translation units.  CG = CTA-group size (1: single CTA, 2: CTA
 // pair with tcgen05 cta_group::2); `grid` is in CTAs (a multiple of CG).
-template <int EPI, bool A_MN, bool B_MN, int CG>
+// ACT is the activation of the activation epilogues (0 for the others).
+template <int EPI, bool A_MN, bool B_MN, int CG, int ACT>
 cudaError_t launch_gemm(const Params& p, int grid, cudaStream_t stream, bool pdl);
-template <int EPI, bool A_MN, bool B_MN, int CG>
+template <int EPI, bool A_MN, bool B_MN, int CG, int ACT>
 int max_groups();
 
-// Elementwise postact a = s*act(G)*U (U == nullptr: non-gated), n elements.
+// Elementwise postact a = s*act(G)*U (U == nullptr: non-gated), n elements;
+// `act` is a device activation (Act).
 cudaError_t launch_postact(const void* G, const void* U, void* a, long long n, int act,
                            float scale, cudaStream_t stream, bool pdl);
 

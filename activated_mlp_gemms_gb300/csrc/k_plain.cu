@@ -1,0 +1,14 @@
+// Plain bf16-store GEMM instances: the down projection (both operands
+// K-major) and dx ([dG|dU] x [Wg;Wu], B read N-contiguous).
+#include "gemm.cuh"
+
+namespace mlpk {
+template cudaError_t launch_gemm<EPI_STORE_BF16, false, false, 1, 0>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_STORE_BF16, false, false, 1, 0>();
+template cudaError_t launch_gemm<EPI_STORE_BF16, false, false, 2, 0>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_STORE_BF16, false, false, 2, 0>();
+template cudaError_t launch_gemm<EPI_STORE_BF16, false, true, 1, 0>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_STORE_BF16, false, true, 1, 0>();
+template cudaError_t launch_gemm<EPI_STORE_BF16, false, true, 2, 0>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_STORE_BF16, false, true, 2, 0>();
+}  // namespace mlpk

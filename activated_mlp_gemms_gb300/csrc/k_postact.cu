@@ -1,4 +1,4 @@
-// Elementwise postact a = s * act(G) * U (non-gated: s * act(G)), used when
+// Elementwise postact a = s * act(G) * U (U == nullptr: s * act(G)), used when
 // the backward pass needs only dWd: the postact is rebuilt from the saved or
 // recomputed preacts without the activation derivative.  HBM-bound: 8 bf16
 // per thread per step (16-byte loads and stores), grid-stride loop.
@@ -57,9 +57,19 @@ cudaError_t launch_postact(const void* G, const void* U, void* a, long long n, i
   auto g = static_cast<const __nv_bfloat16*>(G);
   auto u = static_cast<const __nv_bfloat16*>(U);
   auto o = static_cast<__nv_bfloat16*>(a);
-  if (act == ACT_SILU) return cudaLaunchKernelEx(&cfg, k_postact<ACT_SILU, true>, g, u, o, n8, scale);
-  if (act == ACT_RELU_SQ) return cudaLaunchKernelEx(&cfg, k_postact<ACT_RELU_SQ, false>, g, u, o, n8, scale);
-  return cudaLaunchKernelEx(&cfg, k_postact<ACT_GELU_TANH, false>, g, u, o, n8, scale);
+  // `act` is the device activation (see Act); `gated` selects the times-U form
+  if (U) {
+    if (act == ACT_RELU) return cudaLaunchKernelEx(&cfg, k_postact<ACT_RELU, true>, g, u, o, n8, scale);
+    if (act == ACT_GELU_TANH)
+      return cudaLaunchKernelEx(&cfg, k_postact<ACT_GELU_TANH, true>, g, u, o, n8, scale);
+    if (act == ACT_SIGMOID)
+      return cudaLaunchKernelEx(&cfg, k_postact<ACT_SIGMOID, true>, g, u, o, n8, scale);
+    return cudaLaunchKernelEx(&cfg, k_postact<ACT_SILU, true>, g, u, o, n8, scale);
+  }
+  if (act == ACT_RELU) return cudaLaunchKernelEx(&cfg, k_postact<ACT_RELU, false>, g, u, o, n8, scale);
+  if (act == ACT_GELU_TANH)
+    return cudaLaunchKernelEx(&cfg, k_postact<ACT_GELU_TANH, false>, g, u, o, n8, scale);
+  return cudaLaunchKernelEx(&cfg, k_postact<ACT_RELU_SQ, false>, g, u, o, n8, scale);
 }
 
 }  // namespace mlpk

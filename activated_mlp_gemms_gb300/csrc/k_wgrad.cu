@@ -4,12 +4,12 @@
 #include "gemm.cuh"
 
 namespace mlpk {
-template cudaError_t launch_gemm<EPI_STORE_BF16, true, true, 1>(const Params&, int, cudaStream_t, bool);
-template int max_groups<EPI_STORE_BF16, true, true, 1>();
-template cudaError_t launch_gemm<EPI_STORE_BF16, true, true, 2>(const Params&, int, cudaStream_t, bool);
-template int max_groups<EPI_STORE_BF16, true, true, 2>();
-template cudaError_t launch_gemm<EPI_ACCUM_F32, true, true, 1>(const Params&, int, cudaStream_t, bool);
-template int max_groups<EPI_ACCUM_F32, true, true, 1>();
-template cudaError_t launch_gemm<EPI_ACCUM_F32, true, true, 2>(const Params&, int, cudaStream_t, bool);
-template int max_groups<EPI_ACCUM_F32, true, true, 2>();
+template cudaError_t launch_gemm<EPI_STORE_BF16, true, true, 1, 0>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_STORE_BF16, true, true, 1, 0>();
+template cudaError_t launch_gemm<EPI_STORE_BF16, true, true, 2, 0>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_STORE_BF16, true, true, 2, 0>();
+template cudaError_t launch_gemm<EPI_ACCUM_F32, true, true, 1, 0>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_ACCUM_F32, true, true, 1, 0>();
+template cudaError_t launch_gemm<EPI_ACCUM_F32, true, true, 2, 0>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_ACCUM_F32, true, true, 2, 0>();
 }  // namespace mlpk

@@ -143,6 +143,20 @@ unsigned long long wait_limit_ns() {
 // ------------------------------------------------------------ launch builder
 // Operand roles: a K-major operand [rows, K] is loaded with boxes
 // {64, rows-per-box}; an MN-major operand [K, MN] with boxes {64, 64}.
+// The device activation (Act) an ABI activation applies to the gate or preact.
+int device_act(int act) {
+  switch (act) {
+    case MLP_ACT_SWIGLU: return ACT_SILU;
+    case MLP_ACT_RELU_SQ: return ACT_RELU_SQ;
+    case MLP_ACT_GELU_TANH: return ACT_GELU_TANH;
+    case MLP_ACT_RELU: return ACT_RELU;
+    case MLP_ACT_REGLU: return ACT_RELU;
+    case MLP_ACT_GEGLU: return ACT_GELU_TANH;
+    case MLP_ACT_GLU: return ACT_SIGMOID;
+    default: return ACT_SILU;
+  }
+}
+
 std::atomic<int> g_tile_policy{0};  // 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles
 
 // CTA-group size for a GEMM whose output has `rows` rows: pairs (256-row
@@ -160,7 +174,7 @@ struct Gemm {
   bool ok = true;
   Gemm(const mlp_problem_t& pr, int* counter, int* status, int cg_) : cg(cg_) {
     std::memset(&p, 0, sizeof(p));
-    p.act = pr.act;
+    p.act = device_act(pr.act);
     p.scale = pr.gate_mult * pr.down_mult;
     p.group_m = 16;
     p.counter = counter;
@@ -266,7 +280,7 @@ int traced(int tag, cudaStream_t s, F&& launch) {
 }
 
 // Co-resident CTA groups of a kernel instance on the current device (cached).
-template <int EPI, bool A_MN, bool B_MN, int CG>
+template <int EPI, bool A_MN, bool B_MN, int CG, int ACT>
 int groups_cached() {
   static std::atomic<int> cache[64];
   int dev = 0;
@@ -275,34 +289,60 @@ int groups_cached() {
     int v = cache[dev].load();
     if (v > 0) return v;
   }
-  int v = max_groups<EPI, A_MN, B_MN, CG>();
+  int v = max_groups<EPI, A_MN, B_MN, CG, ACT>();
   if (v > 0 && dev >= 0 && dev < 64) cache[dev].store(v);
   return v;
 }
 
-template <int EPI, bool A_MN, bool B_MN>
-int run(Gemm& g, Call& c, int tag) {
+template <int EPI, bool A_MN, bool B_MN, int ACT>
+int run_act(Gemm& g, Call& c, int tag) {
   if (!g.ok) return MLP_ERR_CUDA;
   if (g.p.total_units == 0) return MLP_OK;
   const bool pdl = c.pdl();
   if (g.cg == 2) {
-    const int groups = groups_cached<EPI, A_MN, B_MN, 2>();
+    const int groups = groups_cached<EPI, A_MN, B_MN, 2, ACT>();
     if (groups <= 0) return MLP_ERR_CUDA;
     const int n = g.p.total_units < groups ? g.p.total_units : groups;
     return traced(tag, c.stream,
-                  [&] { return launch_gemm<EPI, A_MN, B_MN, 2>(g.p, 2 * n, c.stream, pdl); });
+                  [&] { return launch_gemm<EPI, A_MN, B_MN, 2, ACT>(g.p, 2 * n, c.stream, pdl); });
   }
   const int sms = num_sms();
   const int n = g.p.total_units < sms ? g.p.total_units : sms;
-  return traced(tag, c.stream,
-                [&] { return launch_gemm<EPI, A_MN, B_MN, 1>(g.p, n < 1 ? 1 : n, c.stream, pdl); });
+  return traced(tag, c.stream, [&] {
+    return launch_gemm<EPI, A_MN, B_MN, 1, ACT>(g.p, n < 1 ? 1 : n, c.stream, pdl);
+  });
+}
+
+// Kernels without an activation epilogue.
+template <int EPI, bool A_MN, bool B_MN>
+int run(Gemm& g, Call& c, int tag) {
+  return run_act<EPI, A_MN, B_MN, 0>(g, c, tag);
+}
+
+// Activation epilogues: one kernel instance per activation.
+template <int EPI, bool A_MN, bool B_MN>
+int run_gated(Gemm& g, Call& c, int tag) {
+  switch (g.p.act) {
+    case ACT_RELU: return run_act<EPI, A_MN, B_MN, ACT_RELU>(g, c, tag);
+    case ACT_GELU_TANH: return run_act<EPI, A_MN, B_MN, ACT_GELU_TANH>(g, c, tag);
+    case ACT_SIGMOID: return run_act<EPI, A_MN, B_MN, ACT_SIGMOID>(g, c, tag);
+    default: return run_act<EPI, A_MN, B_MN, ACT_SILU>(g, c, tag);
+  }
+}
+template <int EPI, bool A_MN, bool B_MN>
+int run_nongated(Gemm& g, Call& c, int tag) {
+  switch (g.p.act) {
+    case ACT_RELU: return run_act<EPI, A_MN, B_MN, ACT_RELU>(g, c, tag);
+    case ACT_GELU_TANH: return run_act<EPI, A_MN, B_MN, ACT_GELU_TANH>(g, c, tag);
+    default: return run_act<EPI, A_MN, B_MN, ACT_RELU_SQ>(g, c, tag);
+  }
 }
 
 // ------------------------------------------------------------ validation
 int check_problem(const mlp_problem_t* p) {
   if (!p) return MLP_ERR_INVALID_ARG;
   if (p->M <= 0 || p->H <= 0 || p->I <= 0) return MLP_ERR_INVALID_ARG;
-  if (p->act < MLP_ACT_SWIGLU || p->act > MLP_ACT_GELU_TANH) return MLP_ERR_INVALID_ARG;
+  if (p->act < MLP_ACT_SWIGLU || p->act > MLP_ACT_GLU) return MLP_ERR_INVALID_ARG;
   if (!std::isfinite(p->gate_mult) || !std::isfinite(p->down_mult)) return MLP_ERR_INVALID_ARG;
   if (p->H % 8 || p->I % 8) return MLP_ERR_ALIGNMENT;
   // TMA coordinates and tile counts are 32-bit
@@ -311,7 +351,10 @@ int check_problem(const mlp_problem_t* p) {
   return MLP_OK;
 }
 
-bool gated(const mlp_problem_t* p) { return p->act == MLP_ACT_SWIGLU; }
+bool gated(const mlp_problem_t* p) {
+  return p->act == MLP_ACT_SWIGLU || p->act == MLP_ACT_REGLU || p->act == MLP_ACT_GEGLU ||
+         p->act == MLP_ACT_GLU;
+}
 
 size_t inter_bytes(const mlp_problem_t* p) { return round256((size_t)p->M * p->I * 2); }
 
@@ -378,7 +421,7 @@ int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* W
     P.mapO[0] = oA;
     P.mapO[1] = oG;
     P.mapO[2] = oU;
-    return run<EPI_GATED_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
+    return run_gated<EPI_GATED_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
   }
   const int mW = g.kmajor(Wg, p->I, p->H, g.b_rows());
   const int oA = g.output(a_out, p->M, p->I);
@@ -388,7 +431,7 @@ int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* W
   P.mapB0 = mW;
   P.mapO[0] = oA;
   P.mapO[1] = oP;
-  return run<EPI_ACT_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
+  return run_nongated<EPI_ACT_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
 }
 
 // out = a Wd^T
@@ -485,14 +528,14 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     } else {
       P.mapO[1] = oA;
     }
-    MLP_TRY(gated(p) ? run<EPI_DGATED, false, true>(g, c, MLP_KERNEL_DGATED)
-                     : run<EPI_DACT, false, true>(g, c, MLP_KERNEL_DGATED));
+    MLP_TRY(gated(p) ? run_gated<EPI_DGATED, false, true>(g, c, MLP_KERNEL_DGATED)
+                     : run_nongated<EPI_DACT, false, true>(g, c, MLP_KERNEL_DGATED));
   } else if (!recompute) {
     // only dWd requested: rebuild the postact without the derivative
     const bool pdl = c.pdl();
     MLP_TRY(traced(MLP_KERNEL_POSTACT, c.stream, [&] {
-      return launch_postact(G, U, a, (long long)M * I, p->act, p->gate_mult * p->down_mult,
-                            c.stream, pdl);
+      return launch_postact(G, U, a, (long long)M * I, device_act(p->act),
+                            p->gate_mult * p->down_mult, c.stream, pdl);
     }));
   }
   void* dG = G;

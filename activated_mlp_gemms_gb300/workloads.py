@@ -20,13 +20,17 @@ import math
 import torch
 
 
+# activations with a gate and an up projection (the others take one fc1 weight)
+GATED_ACTS = ("swiglu", "reglu", "geglu", "glu")
+
+
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
     M: int
     H: int
     I: int
-    act: str = "swiglu"          # swiglu | relu_sq | gelu_tanh_approx
+    act: str = "swiglu"          # swiglu | reglu | geglu | glu | relu_sq | gelu_tanh_approx | relu
     gate_mult: float = 1.0
     down_mult: float = 1.0
     recompute: bool = False      # backward recomputes G/U from x
@@ -36,7 +40,7 @@ class Workload:
 
     @property
     def gated(self) -> bool:
-        return self.act == "swiglu"
+        return self.act in GATED_ACTS
 
 
 # The five workloads (token count M = batch * sequence).
@@ -63,7 +67,7 @@ def make_inputs(M, H, I, act="swiglu", seed=0, dW_prev=False):
     dWg_prev, dWu_prev, dWd_prev."""
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
-    gated = act == "swiglu"
+    gated = act in GATED_ACTS
     bf = torch.bfloat16
     x = torch.randn((M, H), generator=gen, dtype=torch.float32).to(bf)
     Wg = _uniform(gen, (I, H), 1.0 / math.sqrt(H)).to(bf)
@@ -107,6 +111,6 @@ def closed_form_inputs(M, H, I, act="swiglu"):
         c = torch.arange(cols, dtype=torch.float64)[None, :]
         return (torch.remainder(5 * r + 11 * c + k, 17) - 8) / 32
 
-    gated = act == "swiglu"
+    gated = act in GATED_ACTS
     return {"x": x.to(bf), "Wg": w(I, H, 0).to(bf), "Wu": w(I, H, 1).to(bf) if gated else None,
             "Wd": w(H, I, 2).to(bf), "dout": dout.to(bf)}

@@ -72,15 +72,26 @@ typedef enum {
   MLP_ERR_TIMEOUT = -6             /* device side: a bounded wait expired (see mlp_device_status) */
 } mlp_status_t;
 
-/* Activation (quack mlp.py, the Activation literal).  SWIGLU is the gated
- * case (act = silu on the gate, times the up projection); RELU_SQ
- * (relu(z)^2) and GELU_TANH (the tanh approximation of GELU,
- * 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))) are non-gated: there is
- * one fc1 weight, passed as Wg, and Wu must be NULL. */
+/* Activation (quack mlp.py, the Activation literal).
+ * Gated (a gate and an up weight, h = gate_mult * f(x Wg^T) * (x Wu^T)):
+ *   SWIGLU f = silu(z) = z sigmoid(z)      REGLU f = relu(z) = max(z, 0)
+ *   GEGLU  f = the tanh GELU below          GLU   f = sigmoid(z) = 1/(1+e^-z)
+ * Non-gated (one fc1 weight, passed as Wg, and Wu must be NULL;
+ * h = gate_mult * f(x Wg^T)):
+ *   RELU_SQ f = relu(z)^2 (modded-nanogpt gpt.py, ReLUSqrdMLP)
+ *   GELU_TANH f = 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))
+ *   RELU f = max(z, 0)
+ * The pages name reglu, geglu, glu and relu without formulas; these are the
+ * plain readings (GLU: Dauphin et al. 2017; GLU variants: Shazeer 2020).
+ * relu'(0) is taken as 0.  swiglu_oai, also named there, is not provided. */
 typedef enum {
   MLP_ACT_SWIGLU = 0,
   MLP_ACT_RELU_SQ = 1,
-  MLP_ACT_GELU_TANH = 2
+  MLP_ACT_GELU_TANH = 2,
+  MLP_ACT_RELU = 3,
+  MLP_ACT_REGLU = 4,
+  MLP_ACT_GEGLU = 5,
+  MLP_ACT_GLU = 6
 } mlp_act_t;
 
 /* Problem description.  M = tokens (batch * sequence), H = hidden (model

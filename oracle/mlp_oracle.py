@@ -26,6 +26,13 @@ What is computed, and where the pages define it
   default activation of ``MLP``).  Its formula is not on the pages; the
   published tanh approximation of GELU (Hendrycks & Gimpel, 2016) is used:
   ``0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))``.
+* The same literal names ``relu`` (non-gated) and the gated ``reglu``,
+  ``geglu`` and ``glu`` without formulas.  Plain readings: relu(z) =
+  max(z, 0); the gated variants apply relu, the tanh-approximated GELU above,
+  and the logistic sigmoid (GLU, Dauphin et al. 2017) to the gate, times the
+  up projection, exactly as swiglu applies silu (Shazeer 2020, "GLU variants
+  improve Transformer").  ``swiglu_oai`` is left out: nothing on the pages
+  defines it.
 
 Readings where the pages are silent (each also listed in the design notes):
 * ``gate_multiplier`` multiplies ``act(g)`` outside the activation, exactly
@@ -44,8 +51,10 @@ from __future__ import annotations
 
 import numpy as np
 
-ACTIVATIONS = ("swiglu", "relu_sq", "gelu_tanh_approx")
-GATED = ("swiglu",)
+ACTIVATIONS = ("swiglu", "relu_sq", "gelu_tanh_approx", "relu", "reglu", "geglu", "glu")
+GATED = ("swiglu", "reglu", "geglu", "glu")
+# the function a gated activation applies to the gate
+GATE_FN = {"swiglu": "silu", "reglu": "relu", "geglu": "gelu_tanh_approx", "glu": "sigmoid"}
 
 # Hendrycks & Gimpel (2016), tanh approximation of GELU.
 _GELU_C = np.sqrt(2.0 / np.pi)
@@ -62,33 +71,54 @@ def _sigmoid(z):
     return 1.0 / (1.0 + np.exp(-z))
 
 
-def act_fn(act: str, z):
-    """The activation applied to the gate (gated) or to the preact (non-gated)."""
-    z = np.asarray(z, dtype=np.float64)
-    if act == "swiglu":  # silu(z) = z * sigmoid(z)
+def _base_fn(name, z):
+    if name == "silu":  # z * sigmoid(z)
         return z * _sigmoid(z)
-    if act == "relu_sq":  # relu(z)^2
+    if name == "sigmoid":
+        return _sigmoid(z)
+    if name == "relu":
+        return np.maximum(z, 0.0)
+    if name == "relu_sq":  # relu(z)^2
         r = np.maximum(z, 0.0)
         return r * r
-    if act == "gelu_tanh_approx":
+    if name == "gelu_tanh_approx":
         t = np.tanh(_GELU_C * (z + _GELU_A * z ** 3))
         return 0.5 * z * (1.0 + t)
-    raise ValueError(f"unknown activation {act!r}")
+    raise ValueError(f"unknown activation {name!r}")
 
 
-def act_grad(act: str, z):
-    """d act / dz, differentiated by hand from ``act_fn``."""
-    z = np.asarray(z, dtype=np.float64)
-    if act == "swiglu":
+def _base_grad(name, z):
+    if name == "silu":
         s = _sigmoid(z)
         return s * (1.0 + z * (1.0 - s))
-    if act == "relu_sq":
+    if name == "sigmoid":
+        s = _sigmoid(z)
+        return s * (1.0 - s)
+    if name == "relu":
+        return np.where(z > 0.0, 1.0, 0.0)
+    if name == "relu_sq":
         return 2.0 * np.maximum(z, 0.0)
-    if act == "gelu_tanh_approx":
+    if name == "gelu_tanh_approx":
         t = np.tanh(_GELU_C * (z + _GELU_A * z ** 3))
         dinner = _GELU_C * (1.0 + 3.0 * _GELU_A * z * z)
         return 0.5 * (1.0 + t) + 0.5 * z * (1.0 - t * t) * dinner
-    raise ValueError(f"unknown activation {act!r}")
+    raise ValueError(f"unknown activation {name!r}")
+
+
+def _fn_name(act):
+    if act not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {act!r}")
+    return GATE_FN.get(act, act)
+
+
+def act_fn(act: str, z):
+    """The activation applied to the gate (gated) or to the preact (non-gated)."""
+    return _base_fn(_fn_name(act), np.asarray(z, dtype=np.float64))
+
+
+def act_grad(act: str, z):
+    """d act / dz, differentiated by hand from ``act_fn`` (relu: 0 at z = 0)."""
+    return _base_grad(_fn_name(act), np.asarray(z, dtype=np.float64))
 
 
 def _check(x, Wg, Wu, Wd, act):

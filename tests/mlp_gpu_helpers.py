@@ -43,7 +43,7 @@ def run_gpu(t, M, H, I, act, gm, dm, mode="saved", fuse=False, want=("dx", "dWg"
             dW_prev=None):
     """Runs mlp_fwd (+ mlp_bwd or mlp_bwd_recompute) on the CUDA tensors `t`.
     Returns a dict of CPU fp64 arrays and a list of guard-band violations."""
-    gated = act == "swiglu"
+    gated = act in m.GATED_ACTS
     prob = m.problem(M, H, I, act, gm, dm)
     bf = torch.bfloat16
     out, out_f = guarded((M, H), bf)

@@ -75,7 +75,7 @@ def test_small_parity(act, gm, dm, shape, mode, fuse, tile_policy):
     compare_full(got, ref, fuse, M=M)
 
 
-@pytest.mark.parametrize("act", ["swiglu", "relu_sq", "gelu_tanh_approx"])
+@pytest.mark.parametrize("act", list(m.ACTS))
 def test_infer_equals_train_forward_bitwise(act):
     M, H, I = 300, 264, 392
     t = dev_tensors(make_inputs(M, H, I, act, seed=2))
@@ -83,7 +83,7 @@ def test_infer_equals_train_forward_bitwise(act):
     o1 = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
     o2 = torch.empty_like(o1)
     G = torch.empty(M, I, dtype=torch.bfloat16, device="cuda")
-    U = torch.empty_like(G) if act == "swiglu" else None
+    U = torch.empty_like(G) if act in m.GATED_ACTS else None
     m.mlp_fwd(prob, t["x"], t["Wg"], t["Wu"], t["Wd"], o1, G, U)
     m.mlp_fwd_infer(prob, t["x"], t["Wg"], t["Wu"], t["Wd"], o2)
     torch.cuda.synchronize()
@@ -226,3 +226,31 @@ def test_full_size_sampled(name):
                         dt["x"], dt["Wg"], dt["Wu"], dt["Wd"], out2)
         torch.cuda.synchronize()
         assert torch.equal(out2, got["out"])
+
+
+@pytest.mark.parametrize("tile_policy", [1, 2], indirect=True)
+@pytest.mark.parametrize("act", ["relu", "reglu", "geglu", "glu"])
+@pytest.mark.parametrize("shape", [(64, 128, 352), (300, 200, 392)])
+@pytest.mark.parametrize("mode,fuse", [("saved", False), ("recompute", True)])
+def test_more_activations_parity(act, shape, mode, fuse, tile_policy):
+    """The further activations of quack's Activation literal (relu, and the
+    gated reglu, geglu, glu) through the same kernels."""
+    M, H, I = shape
+    t = make_inputs(M, H, I, act, seed=8, dW_prev=fuse)
+    tc = {k: v for k, v in t.items() if not k.endswith("_prev")}
+    prev = {k: v for k, v in t.items() if k.endswith("_prev")} if fuse else None
+    got, bad, _ = run_gpu(dev_tensors(tc), M, H, I, act, 1.125, 2.0, mode=mode, fuse=fuse,
+                          dW_prev=prev)
+    assert not bad
+    ref = oracle_full(tc, act, 1.125, 2.0, dW_prev=prev)
+    compare_full(got, ref, fuse, M=M)
+
+
+@pytest.mark.parametrize("act", ["reglu", "glu", "relu"])
+def test_dwd_only_postact_kernel(act):
+    # only dWd requested in saved mode: the elementwise postact kernel path
+    M, H, I = 200, 136, 264
+    t = make_inputs(M, H, I, act, seed=9)
+    got, bad, _ = run_gpu(dev_tensors(t), M, H, I, act, 1.125, 2.0, mode="saved", want=("dWd",))
+    assert not bad
+    compare_full(got, oracle_full(t, act, 1.125, 2.0), fuse=False)

@@ -14,7 +14,7 @@ import scipy.special as sp
 
 import oracle.mlp_oracle as O
 
-ACTS = ["swiglu", "relu_sq", "gelu_tanh_approx"]
+ACTS = list(O.ACTIVATIONS)  # swiglu, relu_sq, gelu_tanh_approx, relu, reglu, geglu, glu
 
 
 def _rand_problem(rng, M, H, I, act):
@@ -30,10 +30,14 @@ def _rand_problem(rng, M, H, I, act):
 
 def check_act_zero(mod):
     for a in ACTS:
-        assert mod.act_fn(a, 0.0) == 0.0
+        expect = 0.5 if a == "glu" else 0.0  # sigmoid(0) = 1/2; the others vanish at 0
+        assert mod.act_fn(a, 0.0) == expect, a
     assert abs(mod.act_grad("swiglu", 0.0) - 0.5) < 1e-15          # sigma(0) = 1/2
     assert abs(mod.act_grad("gelu_tanh_approx", 0.0) - 0.5) < 1e-15  # (1+tanh 0)/2
+    assert abs(mod.act_grad("geglu", 0.0) - 0.5) < 1e-15
+    assert abs(mod.act_grad("glu", 0.0) - 0.25) < 1e-15             # s (1 - s)
     assert mod.act_grad("relu_sq", 0.0) == 0.0                     # 2 relu(0)
+    assert mod.act_grad("relu", 0.0) == 0.0 and mod.act_grad("reglu", 0.0) == 0.0
 
 
 def test_act_at_zero():
@@ -50,6 +54,18 @@ def test_silu_closed_form():
     # limits: silu(z) -> z for z >> 0, -> 0 for z << 0
     assert abs(O.act_fn("swiglu", 40.0) - 40.0) < 1e-12
     assert abs(O.act_fn("swiglu", -40.0)) < 1e-12
+
+
+def test_sigmoid_and_relu_closed_forms():
+    L = math.log(3.0)
+    assert abs(O.act_fn("glu", L) - 0.75) < 1e-15 and abs(O.act_fn("glu", -L) - 0.25) < 1e-15
+    assert abs(O.act_grad("glu", L) - 0.1875) < 1e-15  # 3/4 * 1/4
+    z = np.array([-2.0, -1e-12, 0.0, 0.25, 3.0])
+    for a in ("relu", "reglu"):
+        np.testing.assert_array_equal(O.act_fn(a, z), [0.0, 0.0, 0.0, 0.25, 3.0])
+        np.testing.assert_array_equal(O.act_grad(a, z), [0.0, 0.0, 0.0, 1.0, 1.0])
+    # geglu applies the same tanh-approximated GELU as gelu_tanh_approx
+    np.testing.assert_array_equal(O.act_fn("geglu", z), O.act_fn("gelu_tanh_approx", z))
 
 
 def test_relu_sq_closed_form():
@@ -70,7 +86,7 @@ def test_gelu_tanh_close_to_exact_gelu():
     check_gelu_vs_exact(O)
 
 
-@pytest.mark.parametrize("act", ["swiglu", "gelu_tanh_approx"])
+@pytest.mark.parametrize("act", ["swiglu", "gelu_tanh_approx", "geglu"])
 def test_odd_part_identity(act):
     # z*s(z) with s(z)+s(-z)=1  =>  act(z) - act(-z) = z
     z = np.linspace(-6, 6, 1001)
@@ -124,6 +140,26 @@ def test_finite_difference_gradients(act):
 
 # ------------------------------------------------------ structured weight cases
 
+def _gate_closed_form(act, z):
+    """The gate function written out independently of the oracle (exact GELU
+    for the tanh-approximated one: they agree within 4.8e-4)."""
+    name = O.GATE_FN.get(act, act)
+    if name == "silu":
+        return z / (1 + np.exp(-z))
+    if name == "sigmoid":
+        return 1 / (1 + np.exp(-z))
+    if name == "relu":
+        return np.where(z > 0, z, 0.0)
+    if name == "relu_sq":
+        return np.where(z > 0, z * z, 0.0)
+    return z * sp.ndtr(z)
+
+
+def _tol(act, scale):
+    gelu = O.GATE_FN.get(act, act) == "gelu_tanh_approx"
+    return 4.8e-4 * scale if gelu else 1e-13
+
+
 @pytest.mark.parametrize("act", ACTS)
 def test_identity_weights(act):
     rng = np.random.default_rng(2)
@@ -131,15 +167,10 @@ def test_identity_weights(act):
     x = rng.standard_normal((M, H))
     E = np.eye(H)
     gm, dm = 1.125, 2.0
-    fw = O.mlp_forward(x, E, E if O.is_gated(act) else None, E, act, gm, dm)
-    if act == "swiglu":
-        # silu(x) * x, written out from silu(z) = z / (1 + e^-z)
-        expect = gm * dm * (x / (1 + np.exp(-x))) * x
-    elif act == "relu_sq":
-        expect = gm * dm * np.where(x > 0, x * x, 0.0)
-    else:
-        expect = gm * dm * x * sp.ndtr(x)  # exact GELU; tanh form within 4.8e-4 * |s|
-    tol = 1e-13 if act != "gelu_tanh_approx" else 4.8e-4 * gm * dm
+    gated = O.is_gated(act)
+    fw = O.mlp_forward(x, E, E if gated else None, E, act, gm, dm)
+    expect = gm * dm * _gate_closed_form(act, x) * (x if gated else 1.0)
+    tol = _tol(act, gm * dm * (np.abs(x).max() if gated else 1.0))
     np.testing.assert_allclose(fw["out"], expect, atol=tol, rtol=0)
 
 
@@ -168,13 +199,10 @@ def test_permutation_weights_forward(act):
         for j in range(H):
             i = tau[j]
             z = x[m, pi[i]]
-            if act == "swiglu":
-                hv = gm * (z / (1 + math.exp(-z))) * x[m, sg[i]]
-            elif act == "relu_sq":
-                hv = gm * max(z, 0.0) ** 2
-            else:
-                hv = gm * z * sp.ndtr(z)
-            tol = 1e-13 if act != "gelu_tanh_approx" else 4.8e-4 * gm * dm
+            hv = gm * float(_gate_closed_form(act, np.array(z)))
+            if gated:
+                hv *= x[m, sg[i]]
+            tol = _tol(act, gm * dm * (abs(x[m, sg[i]]) if gated else 1.0))
             assert abs(fw["out"][m, j] - dm * hv) <= tol
 
 
@@ -207,6 +235,20 @@ def test_zero_gate_weight_swiglu():
     u = x @ Wu.T
     np.testing.assert_allclose(bw["dWg"], 0.5 * gm * dm * ((dout @ Wd) * u).T @ x,
                                rtol=1e-12, atol=1e-14)
+
+
+def test_zero_gate_weight_glu():
+    # Wg = 0: sigmoid(0) = 1/2, so out = (gm dm / 2) (x Wu^T) Wd^T, and dU = gm/2 dh.
+    rng = np.random.default_rng(15)
+    x, Wg, Wu, Wd, dout = _rand_problem(rng, 9, 8, 6, "glu")
+    Wg = np.zeros_like(Wg)
+    gm, dm = 1.125, 2.0
+    fw = O.mlp_forward(x, Wg, Wu, Wd, "glu", gm, dm)
+    np.testing.assert_allclose(fw["out"], 0.5 * gm * dm * (x @ Wu.T) @ Wd.T, rtol=1e-12,
+                               atol=1e-14)
+    bw = O.mlp_backward(dout, x, Wg, Wu, Wd, "glu", gm, dm)
+    np.testing.assert_allclose(bw["dWu"], (0.5 * gm * dm * (dout @ Wd)).T @ x, rtol=1e-12,
+                               atol=1e-14)
 
 
 def test_zero_fc1_relu_sq():
@@ -295,12 +337,14 @@ def test_torch_autograd_cross_check(act):
     tx, tg, td = t(x), t(Wg), t(Wd)
     tu = t(Wu) if Wu is not None else None
     z = tx @ tg.T
-    if act == "swiglu":
-        hh = gm * torch.nn.functional.silu(z) * (tx @ tu.T)
-    elif act == "relu_sq":
-        hh = gm * torch.relu(z) ** 2
-    else:
-        hh = gm * torch.nn.functional.gelu(z, approximate="tanh")
+    F = torch.nn.functional
+    fn = {"swiglu": F.silu, "relu_sq": lambda v: torch.relu(v) ** 2,
+          "gelu_tanh_approx": lambda v: F.gelu(v, approximate="tanh"), "relu": torch.relu,
+          "reglu": torch.relu, "geglu": lambda v: F.gelu(v, approximate="tanh"),
+          "glu": torch.sigmoid}[act]
+    hh = gm * fn(z)
+    if tu is not None:
+        hh = hh * (tx @ tu.T)
     out = dm * hh @ td.T
     out.backward(torch.tensor(dout))
     fw = O.mlp_forward(x, Wg, Wu, Wd, act, gm, dm)
