@@ -486,7 +486,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
             }
             const uint32_t full = bar_s(FULL + stage);
             // the leader's full barrier expects the bytes of both CTAs of a pair
-            mbar_expect_tx(full, CG * C::STAGE);
+            // (the A boxes of an output with few rows cover only those rows)
+            mbar_expect_tx(full, CG * (p.a_tx_bytes + C::B_BYTES));
             const int seg = kb < P.kb0 ? 0 : 1;
             const int kc = (seg == 0 ? kb : kb - P.kb0) * BK;
             const uint32_t sA = base_s + stage * C::STAGE;

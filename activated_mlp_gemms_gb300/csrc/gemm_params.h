@@ -60,7 +60,7 @@ struct Params {  // 64-byte aligned through CUtensorMap
   float scale;            // gate_mult * down_mult (activation epilogues)
   int pad_;
   int debug_flags;        // MLP_DEBUG_* (testing only; 0 in normal use)
-  int pad2_;
+  int a_tx_bytes;         // bytes one CTA's A boxes bring per k-block (K-major A: rows x 128 B)
   int* counter;           // dynamic tile scheduler counter, zero at launch
   int* status;            // device status word (MLP_ERR_TIMEOUT on a bounded-wait expiry)
   unsigned long long timeout_ns;
@@ -79,5 +79,9 @@ int max_groups();
 // `act` is a device activation (Act).
 cudaError_t launch_postact(const void* G, const void* U, void* a, long long n, int act,
                            float scale, cudaStream_t stream, bool pdl);
+
+// fp32 -> bf16 (round to nearest even), n elements (a multiple of 8).
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, long long n, cudaStream_t stream,
+                               bool pdl);
 
 }  // namespace mlpk

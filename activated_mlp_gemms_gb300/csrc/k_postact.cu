@@ -72,4 +72,43 @@ cudaError_t launch_postact(const void* G, const void* U, void* a, long long n, i
   return cudaLaunchKernelEx(&cfg, k_postact<ACT_RELU_SQ, false>, g, u, o, n8, scale);
 }
 
+// fp32 -> bf16 over n elements, 8 per thread per step (two 16-byte loads,
+// one 16-byte store); the split-K partial sums of a decode-sized output.
+__global__ void __launch_bounds__(256) k_f32_to_bf16(const float* __restrict__ src,
+                                                     __nv_bfloat16* __restrict__ dst, long long n8) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint4 a = ld_global_v4(src + 8 * i);
+    const uint4 b = ld_global_v4(src + 8 * i + 4);
+    st_global_v4(dst + 8 * i,
+                 make_uint4(pack_bf16x2(__uint_as_float(a.x), __uint_as_float(a.y)),
+                            pack_bf16x2(__uint_as_float(a.z), __uint_as_float(a.w)),
+                            pack_bf16x2(__uint_as_float(b.x), __uint_as_float(b.y)),
+                            pack_bf16x2(__uint_as_float(b.z), __uint_as_float(b.w))));
+  }
+}
+
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, long long n, cudaStream_t stream,
+                               bool pdl) {
+  const long long n8 = n / 8;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;
+  if (blocks < 1) blocks = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_f32_to_bf16, src, static_cast<__nv_bfloat16*>(dst), n8);
+}
+
 }  // namespace mlpk

@@ -174,6 +174,7 @@ struct Gemm {
   bool ok = true;
   Gemm(const mlp_problem_t& pr, int* counter, int* status, int cg_) : cg(cg_) {
     std::memset(&p, 0, sizeof(p));
+    p.a_tx_bytes = BM * BK * 2;
     p.act = device_act(pr.act);
     p.scale = pr.gate_mult * pr.down_mult;
     p.group_m = 16;
@@ -187,6 +188,15 @@ struct Gemm {
     if (nmaps >= MAX_MAPS) { ok = false; return 0; }
     if (!make_map(&p.maps[nmaps], ptr, K, rows, K, BK, box_rows)) ok = false;
     return nmaps++;
+  }
+  // K-major A operand [rows, K]: an output with fewer than 128 rows loads
+  // boxes of its rows only (rounded up to 16); the MMA's rows beyond them
+  // read stale shared memory and only produce accumulator rows past the
+  // output, which the epilogue never stores.
+  int kmajor_a(const void* ptr, int rows, int K) {
+    const int box = rows < BM ? ((rows + 15) / 16) * 16 : BM;
+    p.a_tx_bytes = box * BK * 2;
+    return kmajor(ptr, rows, K, box);
   }
   // MN-major operand: array [K, MN] (row pitch MN), box {64, 64}
   int mnmajor(const void* ptr, int K, int MN) {
@@ -358,11 +368,40 @@ bool gated(const mlp_problem_t* p) {
 
 size_t inter_bytes(const mlp_problem_t* p) { return round256((size_t)p->M * p->I * 2); }
 
+// Split-K factor of a bf16-output GEMM [rows, cols] x K whose output tiles
+// cannot fill the GPU (decode-sized token counts): the splits' fp32 partial
+// sums meet in a zeroed region of the workspace (TMA reduce-add) and one
+// elementwise pass converts it to bf16.  It depends on the shape only, so
+// the workspace size does too.  Aims at ~128 work units with at least 8
+// k-blocks each.
+int bf16_split(int rows, int cols, int K) {
+  const long long tiles =
+      (long long)((rows + BM - 1) / BM) * (long long)((cols + MMA_N - 1) / MMA_N);
+  const int kb = (K + BK - 1) / BK;
+  if (tiles > 32 || kb < 16) return 1;
+  int split = static_cast<int>(128 / tiles);
+  if (split > kb / 8) split = kb / 8;
+  return split < 2 ? 1 : split;
+}
+
+// K of the bf16-output GEMM of a mode: the down projection (forward) or dx.
+int split_k_of(const mlp_problem_t* p, int mode) {
+  if (mode == MLP_MODE_FWD || mode == MLP_MODE_INFER) return p->I;
+  return gated(p) ? 2 * p->I : p->I;
+}
+
+size_t split_bytes(const mlp_problem_t* p, int mode) {
+  return bf16_split(p->M, p->H, split_k_of(p, mode)) > 1 ? round256((size_t)p->M * p->H * 4) : 0;
+}
+
 size_t ws_size(const mlp_problem_t* p, int mode) {
   size_t n = CTRL_BYTES + inter_bytes(p);  // control block + postact a
   if (mode == MLP_MODE_BWD_RECOMPUTE) n += inter_bytes(p) * (gated(p) ? 2 : 1);
-  return n;
+  return n + split_bytes(p, mode);  // + the fp32 partial-sum region (small M only)
 }
+
+// Offset of the fp32 partial-sum region in the workspace.
+size_t split_offset(const mlp_problem_t* p, int mode) { return ws_size(p, mode) - split_bytes(p, mode); }
 
 // Required pointer present and 16-byte aligned; optional pointer aligned if present.
 int need(const void* ptr) {
@@ -407,7 +446,7 @@ int begin_call(Call& c, void* ws, void* stream) {
 int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* Wg, const void* Wu,
                    void* a_out, void* G_out, void* U_out) {
   Gemm g(*p, c.counter(), c.status, pick_cg(p->M));
-  const int mA = g.kmajor(x, p->M, p->H, BM);
+  const int mA = g.kmajor_a(x, p->M, p->H);
   if (gated(p)) {
     const int mG = g.kmajor(Wg, p->I, p->H, 128);
     const int mU = g.kmajor(Wu, p->I, p->H, 128);
@@ -434,11 +473,28 @@ int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* W
   return run_nongated<EPI_ACT_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
 }
 
-// out = a Wd^T
-int launch_down(const mlp_problem_t* p, Call& c, const void* a, const void* Wd, void* out) {
+// fp32 [n] -> bf16 [n] (the split-K partial-sum region to the output).
+int convert_out(Call& c, const float* part, void* out, long long n) {
+  const bool pdl = c.pdl();
+  return traced(MLP_KERNEL_CONVERT, c.stream,
+                [&] { return launch_f32_to_bf16(part, out, n, c.stream, pdl); });
+}
+
+// out = a Wd^T; with split > 1 through the zeroed fp32 region `part`.
+int launch_down(const mlp_problem_t* p, Call& c, const void* a, const void* Wd, void* out,
+                float* part, int split) {
   Gemm g(*p, c.counter(), c.status, pick_cg(p->M));
-  const int mA = g.kmajor(a, p->M, p->I, BM);
+  const int mA = g.kmajor_a(a, p->M, p->I);
   const int mB = g.kmajor(Wd, p->H, p->I, g.b_rows());
+  if (split > 1) {
+    const int oP = g.output(part, p->M, p->H, true);
+    Prob& P = g.add(p->M, p->H, p->I, 0, MMA_N, split);
+    P.mapA0 = mA;
+    P.mapB0 = mB;
+    P.mapO[0] = oP;
+    MLP_TRY(run<EPI_ACCUM_F32, false, false>(g, c, MLP_KERNEL_DOWN));
+    return convert_out(c, part, out, (long long)p->M * p->H);
+  }
   const int oO = g.output(out, p->M, p->H);
   Prob& P = g.add(p->M, p->H, p->I, 0, MMA_N);
   P.mapA0 = mA;
@@ -461,8 +517,12 @@ int forward(const mlp_problem_t* p, const void* x, const void* Wg, const void* W
   Call c;
   MLP_TRY(begin_call(c, ws, stream));
   void* a = static_cast<char*>(ws) + CTRL_BYTES;
+  const int split = bf16_split(p->M, p->H, split_k_of(p, mode));
+  float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + split_offset(p, mode));
+  if (split > 1)
+    MLP_TRY(cuda_err(cudaMemsetAsync(part, 0, (size_t)p->M * p->H * 4, c.stream)));
   MLP_TRY(launch_fwd_act(p, c, x, Wg, Wu, a, G_save, U_save));
-  return launch_down(p, c, a, Wd, out);
+  return launch_down(p, c, a, Wd, out, part, split);
 }
 
 int backward(const mlp_problem_t* p, const void* dout, const void* x, const void* Wg,
@@ -495,6 +555,10 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
   Call c;
   MLP_TRY(begin_call(c, ws, stream));
   char* base = static_cast<char*>(ws) + CTRL_BYTES;
+  const int dx_split = dx ? bf16_split(p->M, p->H, split_k_of(p, mode)) : 1;
+  float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + split_offset(p, mode));
+  if (dx_split > 1)
+    MLP_TRY(cuda_err(cudaMemsetAsync(part, 0, (size_t)p->M * p->H * 4, c.stream)));
   void* a = base;  // postact (input of dWd)
   if (recompute) {
     G = base + inter_bytes(p);
@@ -509,7 +573,7 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     // stage 1: dh = dout Wd (K = H); epilogue writes dG, dU over G, U (and the
     // postact a when the saved preacts are the only source of it)
     Gemm g(*p, c.counter(), c.status, pick_cg(M));
-    const int mA = g.kmajor(dout, M, H, BM);
+    const int mA = g.kmajor_a(dout, M, H);
     const int mB = g.mnmajor(Wd, H, I);  // Wd [H,I]: B(n=i, k=h) is N-contiguous
     void* a_out = (dWd && !recompute) ? a : nullptr;
     const int oG = g.output(G, M, I);
@@ -544,21 +608,26 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
   if (dx) {
     // stage 2: dx = [dG|dU] [Wg;Wu], one accumulator over K = 2I (non-gated: K = I)
     Gemm g(*p, c.counter(), c.status, pick_cg(M));
-    const int mA0 = g.kmajor(dG, M, I, BM);
+    const int mA0 = g.kmajor_a(dG, M, I);
     const int mB0 = g.mnmajor(Wg, I, H);  // Wg [I,H]: B(n=h, k=i) is N-contiguous
     int mA1 = 0, mB1 = 0;
     if (gated(p)) {
-      mA1 = g.kmajor(dU, M, I, BM);
+      mA1 = g.kmajor_a(dU, M, I);
       mB1 = g.mnmajor(Wu, I, H);
     }
-    const int oX = g.output(dx, M, H);
-    Prob& P = g.add(M, H, I, gated(p) ? I : 0, MMA_N);
+    const int oX = dx_split > 1 ? g.output(part, M, H, true) : g.output(dx, M, H);
+    Prob& P = g.add(M, H, I, gated(p) ? I : 0, MMA_N, dx_split);
     P.mapA0 = mA0;
     P.mapB0 = mB0;
     P.mapA1 = mA1;
     P.mapB1 = mB1;
     P.mapO[0] = oX;
-    MLP_TRY((run<EPI_STORE_BF16, false, true>(g, c, MLP_KERNEL_DX)));
+    if (dx_split > 1) {
+      MLP_TRY((run<EPI_ACCUM_F32, false, true>(g, c, MLP_KERNEL_DX)));
+      MLP_TRY(convert_out(c, part, dx, (long long)M * H));
+    } else {
+      MLP_TRY((run<EPI_STORE_BF16, false, true>(g, c, MLP_KERNEL_DX)));
+    }
   }
 
   if (dWg || dWu || dWd) {
@@ -713,6 +782,7 @@ const char* mlp_kernel_name(int tag) {
     case MLP_KERNEL_DX: return "dx";
     case MLP_KERNEL_WGRAD: return "wgrad";
     case MLP_KERNEL_POSTACT: return "postact";
+    case MLP_KERNEL_CONVERT: return "convert";
     default: return "unknown";
   }
 }

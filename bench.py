@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-trace", action="store_true")
+    ap.add_argument("--sweep-m", action="store_true",
+                    help="also time the inference forward at decode-sized token counts")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args()
@@ -369,6 +371,8 @@ def run_ours(args, rank, world, local_rank):
         im = sum(ims) / len(ims)
         infer = {"ms": im, "tflops": flops_of(w, "infer") / (im * 1e-3) / 1e12}
 
+    sweep = infer_m_sweep(m, w, g, dev, flush, peaks) if args.sweep_m else None
+
     peak = float(peaks["bf16_tflops"])
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -388,7 +392,7 @@ def run_ours(args, rank, world, local_rank):
                       "bwd_tflops": f_bwd / (sum(bwd_ms) / K * 1e-3) / 1e12,
                       "model_flops_per_step": flops_of(w, "fwd") + flops_of(w, "bwd"),
                       "executed_flops_per_step": f_step, "kernels": kernels,
-                      "infer": infer},
+                      "infer": infer, "infer_m_sweep": sweep},
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": len(recs) if trace else None,
@@ -397,6 +401,50 @@ def run_ours(args, rank, world, local_rank):
         "wall_s_timed_region": wall,
     }
     return res, w
+
+
+def infer_m_sweep(m, w, g, dev, flush, peaks):
+    """The no-grad forward at decode-sized token counts with the workload's
+    weights: direct calls and CUDA-graph replays, CUDA events per call, L2
+    flushed before each.  Reports time, TFLOP/s and the weight-streaming rate
+    (the three weight matrices are read once per call)."""
+    import torch
+    bf = torch.bfloat16
+    wbytes = (3 if w.gated else 2) * w.H * w.I * 2
+    rows = []
+    for M in (1, 16, 64, 128, 256, 512):
+        prob = m.problem(M, w.H, w.I, w.act, w.gate_mult, w.down_mult)
+        x = torch.randn(M, w.H, device=dev).to(bf)
+        out = torch.empty(M, w.H, dtype=bf, device=dev)
+        ws = m.alloc_workspace(prob, m.MODE_INFER, dev)
+
+        def call():
+            m.mlp_fwd_infer(prob, x, g["Wg"], g["Wu"], g["Wd"], out, ws=ws)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        res = {}
+        for name, fn in (("direct", call), ("graph", graph.replay)):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            ts = []
+            for _ in range(20):
+                flush.zero_()
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize(dev)
+                ts.append(e0.elapsed_time(e1))
+            res[name] = sorted(ts)[len(ts) // 2] * 1e3  # median, us
+        best = min(res.values())
+        rows.append({"M": M, "direct_us": res["direct"], "graph_us": res["graph"],
+                     "tflops": (6 if w.gated else 4) * M * w.H * w.I / (best * 1e-6) / 1e12,
+                     "weight_gbs": wbytes / (best * 1e-6) / 1e9,
+                     "hbm_frac": wbytes / (best * 1e-6) / 1e9 / float(peaks["hbm_gbs"])})
+    return rows
 
 
 # ------------------------------------------------------------ CPU oracle

@@ -115,7 +115,11 @@ typedef enum {
 /* Bytes of workspace a call in `mode` needs for problem `p` (0 on invalid
  * arguments).  FWD/INFER/BWD: the control block plus one bf16 [M,I] buffer
  * (the postact); BWD_RECOMPUTE: plus the recomputed preacts, two bf16
- * [M,I] buffers when gated, one when not. */
+ * [M,I] buffers when gated, one when not.  When the [M,H] output GEMM (the
+ * down projection, or dx) has too few output tiles to fill the GPU
+ * (decode-sized M: at most 32 tiles of 128 x 256 and K >= 1024), the GEMM
+ * splits K and the workspace also holds one fp32 [M,H] partial-sum region.
+ * The size depends on the problem and mode only. */
 size_t mlp_workspace_size(const mlp_problem_t* p, int mode);
 
 /* Training forward (flash-swiglu-mlp README "Design notes", forward fusion;
@@ -238,7 +242,8 @@ typedef enum {
   MLP_KERNEL_DGATED = 2,   /* dout Wd GEMM with the dgated / dact epilogue */
   MLP_KERNEL_DX = 3,       /* dx GEMM */
   MLP_KERNEL_WGRAD = 4,    /* grouped weight-gradient GEMMs */
-  MLP_KERNEL_POSTACT = 5   /* elementwise postact rebuild (dWd-only backward) */
+  MLP_KERNEL_POSTACT = 5,  /* elementwise postact rebuild (dWd-only backward) */
+  MLP_KERNEL_CONVERT = 6   /* fp32 -> bf16 of a split-K output (decode-sized M) */
 } mlp_kernel_t;
 
 /* on != 0 starts recording, 0 stops (records already taken are kept). */

@@ -60,6 +60,12 @@ def test_workspace_sizes(L):
     assert m.mlp_workspace_size(p, m.MODE_BWD_RECOMPUTE) == 1024 + 3 * inter
     q = m.problem(49152, 768, 3072, "relu_sq")
     assert m.mlp_workspace_size(q, m.MODE_BWD_RECOMPUTE) == 1024 + 2 * 49152 * 3072 * 2
+    # decode-sized M: the down projection splits K and needs an fp32 [M,H] region
+    d = m.problem(16, 4096, 14336)
+    r256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    assert m.mlp_workspace_size(d, m.MODE_INFER) == 1024 + r256(16 * 14336 * 2) + 16 * 4096 * 4
+    assert m.mlp_workspace_size(d, m.MODE_BWD) == 1024 + r256(16 * 14336 * 2) + 16 * 4096 * 4
+    assert m.mlp_workspace_size(m.problem(64, 128, 352), m.MODE_INFER) == 1024 + 64 * 352 * 2
     assert m.mlp_workspace_size(m.problem(0, 8, 8), 0) == 0
     assert m.mlp_workspace_size(m.problem(8, 12, 8), 0) == 0  # H % 8 != 0
     assert m.mlp_workspace_size(p, 7) == 0
@@ -111,6 +117,7 @@ def test_backward_validation(L):
 
 def test_kernel_names_and_empty_trace(L):
     assert m.mlp_kernel_name(2) == "dgated"
+    assert m.mlp_kernel_name(6) == "convert"
     assert m.mlp_kernel_name(99) == "unknown"
     assert m.mlp_trace_read() == []  # nothing recorded: no CUDA call is made
 

@@ -254,3 +254,49 @@ def test_dwd_only_postact_kernel(act):
     got, bad, _ = run_gpu(dev_tensors(t), M, H, I, act, 1.125, 2.0, mode="saved", want=("dWd",))
     assert not bad
     compare_full(got, oracle_full(t, act, 1.125, 2.0), fuse=False)
+
+
+# ------------------------------------------------ decode-sized token counts
+
+@pytest.mark.parametrize("act", ["swiglu", "relu_sq"])
+@pytest.mark.parametrize("M", [1, 16, 64, 200])
+def test_small_m_split_k(act, M):
+    """Few tokens: the down projection (and dx) split K so that their few
+    output tiles still use the whole GPU; the partial sums meet in fp32."""
+    H, I = 512, 2048  # 2 output tiles per 128 rows, K = 2048 (forward), 4096 (gated dx)
+    t = make_inputs(M, H, I, act, seed=12)
+    got, bad, _ = run_gpu(dev_tensors(t), M, H, I, act, 1.125, 2.0, mode="recompute")
+    assert not bad
+    compare_full(got, oracle_full(t, act, 1.125, 2.0), fuse=False)
+    # the inference path agrees bitwise with the training forward
+    d = dev_tensors(t)
+    o2 = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    m.mlp_fwd_infer(m.problem(M, H, I, act, 1.125, 2.0), d["x"], d["Wg"], d["Wu"], d["Wd"], o2)
+    torch.cuda.synchronize()
+    assert rel_err(to_f64(o2), to_f64(got["out"])) < 1e-2
+
+
+def test_inference_forward_in_a_cuda_graph():
+    """mlp_fwd_infer captured into a CUDA graph (after one direct call has
+    set up the library's caches) replays to the direct call's result."""
+    M, H, I = 16, 1024, 4096
+    t = dev_tensors(make_inputs(M, H, I, "swiglu", seed=13))
+    prob = m.problem(M, H, I)
+    ws = m.alloc_workspace(prob, m.MODE_INFER)
+    ref = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros_like(ref)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        m.mlp_fwd_infer(prob, t["x"], t["Wg"], t["Wu"], t["Wd"], ref, ws=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        m.mlp_fwd_infer(prob, t["x"], t["Wg"], t["Wu"], t["Wd"], out, ws=ws)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert m.mlp_device_status(ws) == 0
