@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < MAX_MAPS; ++i) prefetch_tmap(&p.maps[i]);
+    for (int i = 0; i < p.nmaps; ++i) prefetch_tmap(&p.maps[i]);
   }
   if (warp == 1) {
     tmem_alloc<CG>(smem_u32(tmem_base_s), TMEM_COLS);

@@ -61,6 +61,8 @@ struct Params {  // 64-byte aligned through CUtensorMap
   int pad_;
   int debug_flags;        // MLP_DEBUG_* (testing only; 0 in normal use)
   int a_tx_bytes;         // bytes one CTA's A boxes bring per k-block (K-major A: rows x 128 B)
+  int nmaps;              // tensor maps in use
+  int pad3_;
   int* counter;           // dynamic tile scheduler counter, zero at launch
   int* status;            // device status word (MLP_ERR_TIMEOUT on a bounded-wait expiry)
   unsigned long long timeout_ns;

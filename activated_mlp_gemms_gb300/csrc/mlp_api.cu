@@ -308,6 +308,7 @@ template <int EPI, bool A_MN, bool B_MN, int ACT>
 int run_act(Gemm& g, Call& c, int tag) {
   if (!g.ok) return MLP_ERR_CUDA;
   if (g.p.total_units == 0) return MLP_OK;
+  g.p.nmaps = g.nmaps;
   const bool pdl = c.pdl();
   if (g.cg == 2) {
     const int groups = groups_cached<EPI, A_MN, B_MN, 2, ACT>();

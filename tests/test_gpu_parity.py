@@ -278,7 +278,10 @@ def test_small_m_split_k(act, M):
 
 def test_inference_forward_in_a_cuda_graph():
     """mlp_fwd_infer captured into a CUDA graph (after one direct call has
-    set up the library's caches) replays to the direct call's result."""
+    set up the library's caches) replays to the direct call's result.  At
+    this token count the down projection splits K, and the fp32 partial sums
+    meet through atomic adds in no fixed order, so the replays agree with the
+    direct call to rounding, not bitwise."""
     M, H, I = 16, 1024, 4096
     t = dev_tensors(make_inputs(M, H, I, "swiglu", seed=13))
     prob = m.problem(M, H, I)
@@ -297,6 +300,7 @@ def test_inference_forward_in_a_cuda_graph():
     for _ in range(3):
         out.zero_()
         g.replay()
-    torch.cuda.synchronize()
-    assert torch.equal(out, ref)
+        torch.cuda.synchronize()
+        assert torch.isfinite(out.float()).all()
+        assert rel_err(to_f64(out), to_f64(ref)) < 1e-2
     assert m.mlp_device_status(ws) == 0
