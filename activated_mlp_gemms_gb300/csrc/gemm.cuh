@@ -73,7 +73,10 @@ struct EpiTraits {
                                                                           : 1;
   static constexpr int OUT_BYTES = (EPI == EPI_ACCUM_F32) ? 4096 : 2048;
   static constexpr bool DACT = (EPI == EPI_DGATED || EPI == EPI_DACT);
-  static constexpr int STG_WARP = NOUT * OUT_BYTES;
+  // staged boxes per warp: at most two (a third output reuses the first box
+  // once that box's store has read it), so the stage ring keeps 6 stages
+  static constexpr int STG_BUFS = NOUT < 2 ? NOUT : 2;
+  static constexpr int STG_WARP = STG_BUFS * OUT_BYTES;
 };
 
 __device__ __forceinline__ void record_timeout(const Params& p, volatile int* abort_flag) {
@@ -142,6 +145,24 @@ __device__ __forceinline__ void flush_chunk(const Params& p, const Prob& P, cons
   }
 }
 
+// Store staged box `buf` of output o (if its map exists) as a bulk group of its own.
+__device__ __forceinline__ void store_box(const Params& p, const Prob& P, const EpiWarp& e, int o,
+                                          uint32_t buf, int col) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (e.lane == 0) {
+    if (P.mapO[o] >= 0) tma_store_2d(&p.maps[P.mapO[o]], buf, col, e.row0);
+    bulk_commit();
+  }
+}
+
+// Wait until all but the newest of this warp's bulk store groups have read
+// their boxes (the oldest box may then be refilled).
+__device__ __forceinline__ void staging_wait_read_but_one(const EpiWarp& e) {
+  if (e.lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+  __syncwarp();
+}
+
 template <int ACT>
 __device__ __forceinline__ void epi_gated_fwd(const Params& p, const Prob& P, const EpiWarp& e,
                                               uint32_t tb, int col0, int cb, int ce) {
@@ -164,11 +185,17 @@ __device__ __forceinline__ void epi_gated_fwd(const Params& p, const Prob& P, co
       pg[j] = pack_bf16x2(g0, g1);
       pu[j] = pack_bf16x2(u0, u1);
     }
+    // a and G through the two boxes, then U through the first again
     staging_acquire(e);
     stage_bf16(e.stg, e.lane, pa);
     if (P.mapO[1] >= 0) stage_bf16(e.stg + 2048, e.lane, pg);
-    if (P.mapO[2] >= 0) stage_bf16(e.stg + 4096, e.lane, pu);
-    flush_chunk<3, 2048, false>(p, P, e, col);
+    store_box(p, P, e, 0, e.stg, col);
+    store_box(p, P, e, 1, e.stg + 2048, col);
+    if (P.mapO[2] >= 0) {
+      staging_wait_read_but_one(e);
+      stage_bf16(e.stg, e.lane, pu);
+      store_box(p, P, e, 2, e.stg, col);
+    }
   }
 }
 
@@ -228,7 +255,6 @@ __device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, const E
   const float s = p.scale;
   const int row = e.row0 + e.lane;
   constexpr int NOUT = GATED ? 3 : 2;
-  const uint32_t a_buf = e.stg + (NOUT - 1) * 2048;
 #pragma unroll 1
   for (int c = cb; c < ce; c += 32) {
     const int col = col0 + c;
@@ -239,16 +265,19 @@ __device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, const E
     __syncwarp();
     tmem_ld32(tb + c, d);
     tmem_wait_ld();
-    // one 8-column group (one swizzled 16-byte unit per output) at a time
+    // dG (dP) to the first box and dU (gated) or the postact (non-gated) to
+    // the second, one 8-column group at a time; a gated postact waits in
+    // registers for the first box to be read, then goes out through it
     staging_acquire(e);
     const bool want_a = P.mapO[NOUT - 1] >= 0;
     const uint32_t rb = static_cast<uint32_t>(e.lane) * 64u;
     const uint32_t x = (static_cast<uint32_t>(e.lane) >> 1) & 3u;
+    uint32_t pa[16];
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
       const uint32_t gw[4] = {pg[v].x, pg[v].y, pg[v].z, pg[v].w};
       const uint32_t uw[4] = {pu[v].x, pu[v].y, pu[v].z, pu[v].w};
-      uint32_t pdg[4], pdu[4], pa[4];
+      uint32_t pdg[4], pdu[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float2 gg = unpack_bf16x2(gw[j]);
@@ -261,18 +290,27 @@ __device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, const E
           const float2 uu = unpack_bf16x2(uw[j]);
           pdg[j] = pack_bf16x2(dh0 * uu.x * da0, dh1 * uu.y * da1);
           pdu[j] = pack_bf16x2(dh0 * a0, dh1 * a1);
-          pa[j] = pack_bf16x2(s * a0 * uu.x, s * a1 * uu.y);
+          pa[4 * v + j] = pack_bf16x2(s * a0 * uu.x, s * a1 * uu.y);
         } else {
           pdg[j] = pack_bf16x2(dh0 * da0, dh1 * da1);
-          pa[j] = pack_bf16x2(s * a0, s * a1);
+          pa[4 * v + j] = pack_bf16x2(s * a0, s * a1);
         }
       }
       const uint32_t unit = rb + ((static_cast<uint32_t>(v) ^ x) << 4);
       st_shared_v4(e.stg + unit, pdg[0], pdg[1], pdg[2], pdg[3]);
-      if (GATED) st_shared_v4(e.stg + 2048 + unit, pdu[0], pdu[1], pdu[2], pdu[3]);
-      if (want_a) st_shared_v4(a_buf + unit, pa[0], pa[1], pa[2], pa[3]);
+      if (GATED) {
+        st_shared_v4(e.stg + 2048 + unit, pdu[0], pdu[1], pdu[2], pdu[3]);
+      } else if (want_a) {
+        st_shared_v4(e.stg + 2048 + unit, pa[4 * v], pa[4 * v + 1], pa[4 * v + 2], pa[4 * v + 3]);
+      }
     }
-    flush_chunk<NOUT, 2048, false>(p, P, e, col);
+    store_box(p, P, e, 0, e.stg, col);
+    store_box(p, P, e, 1, e.stg + 2048, col);  // dU, or the non-gated postact
+    if (GATED && want_a) {
+      staging_wait_read_but_one(e);
+      stage_bf16(e.stg, e.lane, pa);
+      store_box(p, P, e, 2, e.stg, col);
+    }
     if (c + 32 < ce) {
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
