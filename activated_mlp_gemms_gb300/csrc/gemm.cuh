@@ -69,7 +69,8 @@ struct EpiTraits {
   // outputs staged per chunk (gated fwd: a, G, U; act fwd: a, P; dgated: dG,
   // dU, a; dact: dP, a; plain: D) and bytes of one staged 32 x 32 box
   static constexpr int NOUT = (EPI == EPI_GATED_FWD || EPI == EPI_DGATED) ? 3
-                              : (EPI == EPI_ACT_FWD || EPI == EPI_DACT)   ? 2
+                              : (EPI == EPI_ACT_FWD || EPI == EPI_DACT ||
+                                 EPI == EPI_DACT_RECOMP)                  ? 2
                                                                           : 1;
   static constexpr int OUT_BYTES = (EPI == EPI_ACCUM_F32) ? 4096 : 2048;
   static constexpr bool DACT = (EPI == EPI_DGATED || EPI == EPI_DACT);
@@ -99,6 +100,7 @@ struct EpiWarp {
   int lane;
   int row0;      // first of the warp's 32 rows
   bool rows_ok;  // any of the 32 rows inside the output
+  uint32_t box;  // EPI_DACT_RECOMP: which of the two boxes the next chunk fills
 };
 
 // Stage this lane's 32 bf16 (16 packed words) into a 64B-swizzled 32x32 box.
@@ -321,6 +323,77 @@ __device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, const E
   }
 }
 
+// Fused recompute + derivative (non-gated), in two phases per tile.  Every
+// chunk is one 32 x 32 bf16 box; the two staging boxes alternate across
+// chunks, phases and tiles (e.box), so a box is refilled once every store
+// group but the newest has read its box.
+//
+// Phase 1, accumulator p = x W1^T: the postact a = s*act(p) goes out
+// through map 1 (if requested); s*act'(p) of the thread's 128 columns stays
+// in registers as packed bf16 pairs (dd; 128 fp32 values would not fit the
+// 168 registers a thread of this kernel gets), the same rounding the
+// unfused path takes when it stores P in bf16, and the accumulator is
+// handed back to the MMAs, which compute the next p while phase 2 runs.
+template <int ACT>
+__device__ __forceinline__ void epi_recomp_p(const Params& p, const Prob& P, EpiWarp& e,
+                                             uint32_t tb, int col0, int cb, uint32_t (&dd)[64]) {
+  const float s = p.scale;
+  const bool want_a = P.mapO[1] >= 0;
+#pragma unroll
+  for (int ci = 0; ci < 4; ++ci) {
+    const int c = cb + 32 * ci;
+    const int col = col0 + c;
+    if (col >= P.N) break;  // warp-uniform
+    uint32_t z[32];
+    __syncwarp();
+    tmem_ld32(tb + c, z);
+    tmem_wait_ld();
+    uint32_t pa[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float a0, a1, d0, d1;
+      act_and_grad<ACT>(__uint_as_float(z[2 * j]), a0, d0);
+      act_and_grad<ACT>(__uint_as_float(z[2 * j + 1]), a1, d1);
+      dd[16 * ci + j] = pack_bf16x2(s * d0, s * d1);
+      pa[j] = pack_bf16x2(s * a0, s * a1);
+    }
+    if (want_a) {
+      const uint32_t buf = e.stg + e.box * 2048u;
+      staging_wait_read_but_one(e);
+      stage_bf16(buf, e.lane, pa);
+      store_box(p, P, e, 1, buf, col);
+      e.box ^= 1u;
+    }
+  }
+}
+
+// Phase 2, accumulator dh = dout Wd: dP = dh * s*act'(p) through map 0.
+__device__ __forceinline__ void epi_recomp_dh(const Params& p, const Prob& P, EpiWarp& e,
+                                              uint32_t tb, int col0, int cb,
+                                              const uint32_t (&dd)[64]) {
+#pragma unroll
+  for (int ci = 0; ci < 4; ++ci) {
+    const int c = cb + 32 * ci;
+    const int col = col0 + c;
+    if (col >= P.N) break;
+    uint32_t d[32];
+    __syncwarp();
+    tmem_ld32(tb + c, d);
+    tmem_wait_ld();
+    uint32_t q[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float2 g = unpack_bf16x2(dd[16 * ci + j]);
+      q[j] = pack_bf16x2(__uint_as_float(d[2 * j]) * g.x, __uint_as_float(d[2 * j + 1]) * g.y);
+    }
+    const uint32_t buf = e.stg + e.box * 2048u;
+    staging_wait_read_but_one(e);
+    stage_bf16(buf, e.lane, q);
+    store_box(p, P, e, 0, buf, col);
+    e.box ^= 1u;
+  }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epi_plain(const Params& p, const Prob& P, const EpiWarp& e,
                                           uint32_t tb, int col0, int cb, int ce) {
@@ -376,6 +449,7 @@ struct Cfg {
 //   B gated:   CG=1 the gate and the up rows (two {64, 128} boxes);
 //              CG=2 the leader stages the gate rows, the peer the up rows.
 //   B K-major: one box {64, 256 / CG};      B MN-major: 4 / CG boxes {64 n, 64 k}.
+//   EPI_DACT_RECOMP: segment 0 B K-major (W1), segment 1 B MN-major (Wd).
 template <int EPI, bool A_MN, bool B_MN, int CG>
 __device__ __forceinline__ void load_stage(const Params& p, const Prob& P, const Work& w, int seg,
                                            int kc, uint32_t sA, uint32_t sB, uint32_t full,
@@ -402,7 +476,9 @@ __device__ __forceinline__ void load_stage(const Params& p, const Prob& P, const
   } else {
     const CUtensorMap* mB = &p.maps[seg == 0 ? P.mapB0 : P.mapB1];
     const int n0 = w.tn * MMA_N + static_cast<int>(rank) * (MMA_N / CG);
-    if constexpr (!B_MN) {
+    // the fused recompute reads W1 (K-major) in segment 0, Wd (MN-major) in 1
+    const bool b_mn = EPI == EPI_DACT_RECOMP ? seg == 1 : B_MN;
+    if (!b_mn) {
       ld(sB, mB, kc, n0);
     } else {
 #pragma unroll
@@ -419,6 +495,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
   constexpr bool PAIR = CG == 2;
   constexpr int TILE_N = EpiTraits<EPI>::TILE_N;
   constexpr uint32_t IDESC = idesc_bf16(C::TILE_M, MMA_N, A_MN, B_MN);
+  constexpr uint32_t IDESC_BMN = idesc_bf16(C::TILE_M, MMA_N, A_MN, true);
 
   // 1024-byte aligned stage ring (the 128-byte swizzle repeats every 1 KB)
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -596,23 +673,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
         if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
         if (unit < 0) break;
         const Work w = decode_unit(p, unit);
+        // the fused recompute's second K segment goes to the other accumulator
+        const int kswitch = EPI == EPI_DACT_RECOMP ? p.prob[w.prob].kb0 : -1;
         if (!mbar_wait<PAIR>(bar_s(TEMPTY + acc), aphase ^ 1u, lim, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d = tmem + acc * MMA_N;
+        uint32_t d = tmem + acc * MMA_N;
+        int kfirst = w.kb_begin;
+        bool seg1 = false;
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (EPI == EPI_DACT_RECOMP && kb == kswitch) {
+            if constexpr (PAIR) tc_commit_pair(bar_s(TFULL + acc), 3);
+            else tc_commit(bar_s(TFULL + acc));
+            acc ^= 1;
+            if (acc == 0) aphase ^= 1u;
+            if (!mbar_wait<PAIR>(bar_s(TEMPTY + acc), aphase ^ 1u, lim, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d = tmem + acc * MMA_N;
+            kfirst = kb;
+            seg1 = true;
+          }
           if (!mbar_wait<PAIR>(bar_s(FULL + stage), phase, lim, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sA = base_s + stage * C::STAGE;
           const uint32_t sB = sA + C::A_BYTES;
+          const bool b_mn = B_MN || seg1;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = A_MN ? sdesc_sw128(sA + k * 2048, 8192, 1024)
                                      : sdesc_sw128(sA + k * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(sB + k * 2048, 8192, 1024)
+            const uint64_t bd = b_mn ? sdesc_sw128(sB + k * 2048, 8192, 1024)
                                      : sdesc_sw128(sB + k * 32, 16, 1024);
-            const uint32_t accum = (kb > w.kb_begin || k > 0) ? 1u : 0u;
-            if constexpr (PAIR) tc_mma_bf16_pair(d, ad, bd, IDESC, accum);
-            else tc_mma_bf16(d, ad, bd, IDESC, accum);
+            const uint32_t idesc = b_mn ? IDESC_BMN : IDESC;
+            const uint32_t accum = (kb > kfirst || k > 0) ? 1u : 0u;
+            if constexpr (PAIR) tc_mma_bf16_pair(d, ad, bd, idesc, accum);
+            else tc_mma_bf16(d, ad, bd, idesc, accum);
           }
           any = true;
           if constexpr (PAIR) tc_commit_pair(bar_s(EMPTY + stage), 3);
@@ -643,6 +740,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
     EpiWarp e;
     e.stg = stg_s + static_cast<uint32_t>(warp - 2) * EpiTraits<EPI>::STG_WARP;
     e.lane = lane;
+    e.box = 0;
     int slot = 0;
     uint32_t sphase = 0;
     int acc = 0;
@@ -666,6 +764,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       e.rows_ok = e.row0 < P.M;
       const int col0 = w.tn * TILE_N;
       uint4 pg[4], pu[4];
+      uint32_t dd[EPI == EPI_DACT_RECOMP ? 64 : 1];  // s*act'(p) between the two phases
+      (void)dd;
+      if constexpr (EPI == EPI_DACT_RECOMP) {
+        // phase 1 on the recomputed preact, then its accumulator goes back to the MMAs
+        if (!mbar_wait<PAIR>(bar_s(TFULL + acc), aphase, lim, abort_flag)) {
+          record_timeout(p, abort_flag);
+          break;
+        }
+        tc_fence_after();
+        if (e.rows_ok)
+          epi_recomp_p<ACT>(p, P, e, tmem + acc * MMA_N + (static_cast<uint32_t>(q * 32) << 16),
+                            col0, cb, dd);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(bar_s(TEMPTY + acc));
+          else mbar_arrive_cluster(lead(bar_s(TEMPTY + acc)));
+        }
+        acc ^= 1;
+        if (acc == 0) aphase ^= 1u;
+      }
       if constexpr (EpiTraits<EPI>::DACT) {
         // the saved preacts do not depend on the MMAs: fetch the first chunk now
         if (e.rows_ok) dact_load<EPI == EPI_DGATED>(P, e.row0 + lane, col0 + cb, pg, pu);
@@ -685,6 +804,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
           epi_dact<ACT, true>(p, P, e, tb, col0, cb, ce, pg, pu);
         } else if constexpr (EPI == EPI_DACT) {
           epi_dact<ACT, false>(p, P, e, tb, col0, cb, ce, pg, pu);
+        } else if constexpr (EPI == EPI_DACT_RECOMP) {
+          epi_recomp_dh(p, P, e, tb, col0, cb, dd);
         } else {
           epi_plain<EPI>(p, P, e, tb, col0, cb, ce);
         }

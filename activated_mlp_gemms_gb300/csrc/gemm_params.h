@@ -26,7 +26,11 @@ enum Epi : int {
   EPI_DGATED = 2,      // acc = dout*Wd: dG = s*acc*u*act'(g), dU = s*acc*act(g), a = s*act(g)*u
   EPI_DACT = 3,        // acc = dout*Wd: dP = s*acc*act'(p), a = s*act(p)
   EPI_STORE_BF16 = 4,  // D = bf16(acc)
-  EPI_ACCUM_F32 = 5    // D += acc (fp32, atomic add; split-K safe)
+  EPI_ACCUM_F32 = 5,   // D += acc (fp32, atomic add; split-K safe)
+  // non-gated backward with the preact recomputed in the same tile:
+  // segment 0 acc = p = x W1^T (accumulator 0), segment 1 acc = dh = dout Wd
+  // (accumulator 1): a = s*act(p), dP = s*dh*act'(p)
+  EPI_DACT_RECOMP = 6
 };
 
 // The function applied to the gate (gated MLPs) or to the preact (non-gated).
@@ -40,7 +44,8 @@ struct Prob {
   int ksplit, kper;       // split-K factor, k-blocks per split
   int unit_begin, units;  // this problem's slice of the global work-unit range
   int mapA0, mapB0;       // tensor maps of segment 0
-  int mapA1, mapB1;       // segment 1 (EPI_GATED_FWD: mapB1 = the up weight)
+  int mapA1, mapB1;       // segment 1 (EPI_GATED_FWD: mapB1 = the up weight;
+                          // EPI_DACT_RECOMP: B is K-major in segment 0, MN-major in 1)
   int ld;                 // row pitch (elements) of the epilogue's outputs and inputs
   int mapO[3];            // tensor maps of the epilogue's outputs (-1: output not written)
   void* out0;

@@ -14,6 +14,9 @@
 //        dWd = dout^T a  (K = M), bf16 store or fp32 in-place accumulation
 //   mlp_bwd_recompute
 //     0. gate/up GEMM storing only G, U into the workspace, then as mlp_bwd.
+//     Non-gated with dx/dWg requested: stages 0 and 1 are one kernel whose
+//     tiles accumulate p = x W1^T and dh = dout Wd in the two accumulators;
+//     its epilogue writes the postact a and dP (p never reaches memory).
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -474,6 +477,29 @@ int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* W
   return run_nongated<EPI_ACT_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
 }
 
+// Non-gated recompute, stages 0 + 1 fused: per output tile, segment 0
+// accumulates p = x W1^T (K = H) and segment 1 dh = dout Wd (K = H) into the
+// other accumulator; the epilogue writes a = s*act(p) (if a_out) and
+// dP = s*dh*act'(p).
+int launch_dact_recomp(const mlp_problem_t* p, Call& c, const void* x, const void* W1,
+                       const void* dout, const void* Wd, void* dP, void* a_out) {
+  Gemm g(*p, c.counter(), c.status, pick_cg(p->M));
+  const int mA0 = g.kmajor_a(x, p->M, p->H);
+  const int mB0 = g.kmajor(W1, p->I, p->H, g.b_rows());
+  const int mA1 = g.kmajor_a(dout, p->M, p->H);
+  const int mB1 = g.mnmajor(Wd, p->H, p->I);  // Wd [H,I]: B(n=i, k=h) is N-contiguous
+  const int oP = g.output(dP, p->M, p->I);
+  const int oA = g.output(a_out, p->M, p->I);
+  Prob& P = g.add(p->M, p->I, p->H, p->H, MMA_N);
+  P.mapA0 = mA0;
+  P.mapB0 = mB0;
+  P.mapA1 = mA1;
+  P.mapB1 = mB1;
+  P.mapO[0] = oP;
+  P.mapO[1] = oA;
+  return run_nongated<EPI_DACT_RECOMP, false, false>(g, c, MLP_KERNEL_DACT_RECOMPUTE);
+}
+
 // fp32 [n] -> bf16 [n] (the split-K partial-sum region to the output).
 int convert_out(Call& c, const float* part, void* out, long long n) {
   const bool pdl = c.pdl();
@@ -561,16 +587,22 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
   if (dx_split > 1)
     MLP_TRY(cuda_err(cudaMemsetAsync(part, 0, (size_t)p->M * p->H * 4, c.stream)));
   void* a = base;  // postact (input of dWd)
+  // non-gated recompute: the preact and its derivative in one kernel
+  const bool fused_recomp = recompute && !gated(p) && need_dact;
   if (recompute) {
     G = base + inter_bytes(p);
     U = gated(p) ? base + 2 * inter_bytes(p) : nullptr;
     // stage 0: recompute the preacts (quack MLPRecomputeFunc: preact = x W1^T);
     // the postact needed by dWd comes straight from the fp32 accumulators
-    MLP_TRY(launch_fwd_act(p, c, x, Wg, Wu, dWd ? a : nullptr, G, U));
+    if (fused_recomp) {
+      MLP_TRY(launch_dact_recomp(p, c, x, Wg, dout, Wd, G, dWd ? a : nullptr));
+    } else {
+      MLP_TRY(launch_fwd_act(p, c, x, Wg, Wu, dWd ? a : nullptr, G, U));
+    }
   }
   const int M = p->M, H = p->H, I = p->I;
 
-  if (need_dact) {
+  if (need_dact && !fused_recomp) {
     // stage 1: dh = dout Wd (K = H); epilogue writes dG, dU over G, U (and the
     // postact a when the saved preacts are the only source of it)
     Gemm g(*p, c.counter(), c.status, pick_cg(M));
@@ -784,6 +816,7 @@ const char* mlp_kernel_name(int tag) {
     case MLP_KERNEL_WGRAD: return "wgrad";
     case MLP_KERNEL_POSTACT: return "postact";
     case MLP_KERNEL_CONVERT: return "convert";
+    case MLP_KERNEL_DACT_RECOMPUTE: return "dact_recompute";
     default: return "unknown";
   }
 }

@@ -88,6 +88,7 @@ def kernel_flops(w):
         "dgated": 2 * mhi,
         "dx": (4 if g else 2) * mhi,
         "wgrad": (6 if g else 4) * mhi,
+        "dact_recompute": 4 * mhi,  # non-gated recompute: x W1^T and dout Wd
     }
 
 

@@ -167,7 +167,11 @@ int mlp_bwd(const mlp_problem_t* p, const void* dout, const void* x, const void*
 
 /* Backward that saved only x (quack mlp.py MLPRecomputeFunc): recomputes
  * the preacts x Wg^T, x Wu^T into the workspace, then runs mlp_bwd's
- * stages.  Arguments as in mlp_bwd without G and U. */
+ * stages.  Arguments as in mlp_bwd without G and U.  For the non-gated
+ * activations, when dx, dWg or dWu is requested, the preact and dout Wd
+ * are computed in the same output tile (two accumulators) and the epilogue
+ * writes the postact and dP straight from them: the preact never reaches
+ * memory. */
 int mlp_bwd_recompute(const mlp_problem_t* p, const void* dout, const void* x,
                       const void* Wg, const void* Wu, const void* Wd, void* dx,
                       void* dWg, void* dWu, void* dWd, int fuse_grad_accum,
@@ -243,7 +247,9 @@ typedef enum {
   MLP_KERNEL_DX = 3,       /* dx GEMM */
   MLP_KERNEL_WGRAD = 4,    /* grouped weight-gradient GEMMs */
   MLP_KERNEL_POSTACT = 5,  /* elementwise postact rebuild (dWd-only backward) */
-  MLP_KERNEL_CONVERT = 6   /* fp32 -> bf16 of a split-K output (decode-sized M) */
+  MLP_KERNEL_CONVERT = 6,  /* fp32 -> bf16 of a split-K output (decode-sized M) */
+  MLP_KERNEL_DACT_RECOMPUTE = 7 /* non-gated recompute: x W1^T and dout Wd in one tile,
+                                   epilogue postact and dP */
 } mlp_kernel_t;
 
 /* on != 0 starts recording, 0 stops (records already taken are kept). */

@@ -118,6 +118,7 @@ def test_backward_validation(L):
 def test_kernel_names_and_empty_trace(L):
     assert m.mlp_kernel_name(2) == "dgated"
     assert m.mlp_kernel_name(6) == "convert"
+    assert m.mlp_kernel_name(7) == "dact_recompute"
     assert m.mlp_kernel_name(99) == "unknown"
     assert m.mlp_trace_read() == []  # nothing recorded: no CUDA call is made
 

@@ -90,21 +90,24 @@ def test_infer_equals_train_forward_bitwise(act):
     assert torch.equal(o1, o2)
 
 
-@pytest.mark.parametrize("act", ["swiglu", "relu_sq"])
+@pytest.mark.parametrize("act", ["swiglu", "relu_sq", "gelu_tanh_approx"])
 def test_saved_equals_recompute(act):
-    # Both paths read bf16 preacts produced by the same GEMM tiles, so out,
-    # dx, dWg and dWu agree exactly.  dWd differs by rounding only: the
+    # Gated: both paths read bf16 preacts produced by the same GEMM tiles, so
+    # out, dx, dWg and dWu agree exactly.  dWd differs by rounding only: the
     # recompute path takes the postact from the fp32 accumulators, the saved
-    # path rebuilds it from the bf16 preacts.
+    # path rebuilds it from the bf16 preacts.  Non-gated: the recompute path
+    # takes the derivative from the fp32 preact too (rounded to bf16 where
+    # the saved path rounds the preact), so only out is bitwise equal.
     M, H, I = 300, 264, 392
     tc = dev_tensors(make_inputs(M, H, I, act, seed=3))
     a, _, _ = run_gpu(tc, M, H, I, act, 1.0, 1.0, mode="saved")
     b, _, _ = run_gpu(tc, M, H, I, act, 1.0, 1.0, mode="recompute")
+    exact = {"out", "dx", "dWg", "dWu"} if act in m.GATED_ACTS else {"out"}
     for k in a:
-        if k == "dWd":
-            assert rel_err(to_f64(a[k]), to_f64(b[k])) < TOL_BF16, k
-        else:
+        if k in exact:
             assert torch.equal(a[k], b[k]), k
+        else:
+            assert rel_err(to_f64(a[k]), to_f64(b[k])) < TOL_BF16, k
 
 
 @pytest.mark.parametrize("act", ["swiglu", "relu_sq"])
@@ -123,17 +126,42 @@ def test_single_cta_and_pair_tiles_agree(act):
         assert torch.equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("act", ["swiglu", "relu_sq"])
 @pytest.mark.parametrize("mode", ["saved", "recompute"])
 @pytest.mark.parametrize("want", [("dWd",), ("dx",), ("dWg",), ("dx", "dWd")])
-def test_partial_gradients(mode, want):
+def test_partial_gradients(act, mode, want):
     # Unrequested gradients are skipped (NULL outputs); requested ones match.
-    M, H, I, act = 200, 136, 264, "swiglu"
+    M, H, I = 200, 136, 264
     t = make_inputs(M, H, I, act, seed=4)
     got, bad, _ = run_gpu(dev_tensors(t), M, H, I, act, 1.125, 2.0, mode=mode, want=want)
     assert not bad
     ref = oracle_full(t, act, 1.125, 2.0)
     errs = compare_full(got, ref, fuse=False)
     assert set(errs) == {"out", *want}
+
+
+@pytest.mark.parametrize("act", ["relu_sq", "gelu_tanh_approx", "relu"])
+@pytest.mark.parametrize("M,H,I", [(64, 128, 352), (300, 200, 392), (1000, 768, 3072)])
+def test_nongated_recompute_is_one_fused_kernel(act, M, H, I):
+    # The non-gated recompute backward computes the preact and dout Wd in one
+    # kernel (no separate recompute GEMM) and matches the oracle.
+    t = make_inputs(M, H, I, act, seed=21, dW_prev=True)
+    tc = {k: v for k, v in t.items() if not k.endswith("_prev")}
+    prev = {k: v for k, v in t.items() if k.endswith("_prev")}
+    m.mlp_trace_read()
+    m.mlp_trace_enable(True)
+    try:
+        got, bad, _ = run_gpu(dev_tensors(tc), M, H, I, act, 0.75, 1.5, mode="recompute",
+                              fuse=True, dW_prev=prev)
+    finally:
+        m.mlp_trace_enable(False)
+    names = [n for n, _ in m.mlp_trace_read()]
+    # the forward's gate/up GEMM is the only one: the backward recomputes
+    # the preact inside the fused kernel
+    assert names.count("gate_up_act") == 1 and names.count("dact_recompute") == 1, names
+    assert "dgated" not in names, names
+    assert not bad
+    compare_full(got, oracle_full(tc, act, 0.75, 1.5, dW_prev=prev), fuse=True, M=M)
 
 
 def test_split_m_accumulation_matches_one_call():
