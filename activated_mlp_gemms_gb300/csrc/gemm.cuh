@@ -121,6 +121,28 @@ __device__ __forceinline__ void stage_f32(uint32_t buf, int r, const uint32_t (&
     st_shared_v4(rb + ((j ^ x) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
 }
 
+// What the epilogue needs of a work unit's problem, read from the launch
+// parameters once per unit and kept in registers (a per-chunk read would be
+// a generic load re-issued after every store's memory clobber).
+struct EpiUnit {
+  const CUtensorMap* out[3];  // output maps (nullptr: output not written)
+  int M, N, ld;
+  const void* in0;            // saved preacts (derivative epilogues)
+  const void* in1;
+};
+
+__device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P) {
+  EpiUnit U;
+#pragma unroll
+  for (int o = 0; o < 3; ++o) U.out[o] = P.mapO[o] >= 0 ? &p.maps[P.mapO[o]] : nullptr;
+  U.M = P.M;
+  U.N = P.N;
+  U.ld = P.ld;
+  U.in0 = P.in0;
+  U.in1 = P.in1;
+  return U;
+}
+
 // The staging buffers may be overwritten once the previous chunk's stores
 // have read them.
 __device__ __forceinline__ void staging_acquire(const EpiWarp& e) {
@@ -130,15 +152,15 @@ __device__ __forceinline__ void staging_acquire(const EpiWarp& e) {
 
 // Store the staged boxes of outputs whose map exists at (col, row0).
 template <int NOUT, int OUT_BYTES, bool REDUCE>
-__device__ __forceinline__ void flush_chunk(const Params& p, const Prob& P, const EpiWarp& e,
+__device__ __forceinline__ void flush_chunk(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                             int col) {
   fence_proxy_async_smem();
   __syncwarp();
   if (e.lane == 0) {
 #pragma unroll
     for (int o = 0; o < NOUT; ++o) {
-      if (P.mapO[o] >= 0) {
-        const CUtensorMap* m = &p.maps[P.mapO[o]];
+      if (P.out[o]) {
+        const CUtensorMap* m = P.out[o];
         if constexpr (REDUCE) tma_reduce_add_2d(m, e.stg + o * OUT_BYTES, col, e.row0);
         else tma_store_2d(m, e.stg + o * OUT_BYTES, col, e.row0);
       }
@@ -148,12 +170,12 @@ __device__ __forceinline__ void flush_chunk(const Params& p, const Prob& P, cons
 }
 
 // Store staged box `buf` of output o (if its map exists) as a bulk group of its own.
-__device__ __forceinline__ void store_box(const Params& p, const Prob& P, const EpiWarp& e, int o,
+__device__ __forceinline__ void store_box(const Params& p, const EpiUnit& P, const EpiWarp& e, int o,
                                           uint32_t buf, int col) {
   fence_proxy_async_smem();
   __syncwarp();
   if (e.lane == 0) {
-    if (P.mapO[o] >= 0) tma_store_2d(&p.maps[P.mapO[o]], buf, col, e.row0);
+    if (P.out[o]) tma_store_2d(P.out[o], buf, col, e.row0);
     bulk_commit();
   }
 }
@@ -166,7 +188,7 @@ __device__ __forceinline__ void staging_wait_read_but_one(const EpiWarp& e) {
 }
 
 template <int ACT>
-__device__ __forceinline__ void epi_gated_fwd(const Params& p, const Prob& P, const EpiWarp& e,
+__device__ __forceinline__ void epi_gated_fwd(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                               uint32_t tb, int col0, int cb, int ce) {
   const float s = p.scale;
 #pragma unroll 1
@@ -190,10 +212,10 @@ __device__ __forceinline__ void epi_gated_fwd(const Params& p, const Prob& P, co
     // a and G through the two boxes, then U through the first again
     staging_acquire(e);
     stage_bf16(e.stg, e.lane, pa);
-    if (P.mapO[1] >= 0) stage_bf16(e.stg + 2048, e.lane, pg);
+    if (P.out[1]) stage_bf16(e.stg + 2048, e.lane, pg);
     store_box(p, P, e, 0, e.stg, col);
     store_box(p, P, e, 1, e.stg + 2048, col);
-    if (P.mapO[2] >= 0) {
+    if (P.out[2]) {
       staging_wait_read_but_one(e);
       stage_bf16(e.stg, e.lane, pu);
       store_box(p, P, e, 2, e.stg, col);
@@ -202,7 +224,7 @@ __device__ __forceinline__ void epi_gated_fwd(const Params& p, const Prob& P, co
 }
 
 template <int ACT>
-__device__ __forceinline__ void epi_act_fwd(const Params& p, const Prob& P, const EpiWarp& e,
+__device__ __forceinline__ void epi_act_fwd(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                             uint32_t tb, int col0, int cb, int ce) {
   const float s = p.scale;
 #pragma unroll 1
@@ -222,14 +244,14 @@ __device__ __forceinline__ void epi_act_fwd(const Params& p, const Prob& P, cons
     }
     staging_acquire(e);
     stage_bf16(e.stg, e.lane, pa);
-    if (P.mapO[1] >= 0) stage_bf16(e.stg + 2048, e.lane, pp);
+    if (P.out[1]) stage_bf16(e.stg + 2048, e.lane, pp);
     flush_chunk<2, 2048, false>(p, P, e, col);
   }
 }
 
 // Loads this thread's 32 saved preacts (G and, if gated, U) of chunk `col`.
 template <bool GATED>
-__device__ __forceinline__ void dact_load(const Prob& P, int row, int col, uint4 (&g)[4],
+__device__ __forceinline__ void dact_load(const EpiUnit& P, int row, int col, uint4 (&g)[4],
                                           uint4 (&u)[4]) {
   const __nv_bfloat16* g_in = static_cast<const __nv_bfloat16*>(P.in0);
   const __nv_bfloat16* u_in = static_cast<const __nv_bfloat16*>(P.in1);
@@ -251,7 +273,7 @@ __device__ __forceinline__ void dact_load(const Prob& P, int row, int col, uint4
 // load) before the TMA store of its chunk is issued, and chunks do not
 // overlap.
 template <int ACT, bool GATED>
-__device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, const EpiWarp& e,
+__device__ __forceinline__ void epi_dact(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                          uint32_t tb, int col0, int cb, int ce, uint4 (&pg)[4],
                                          uint4 (&pu)[4]) {
   const float s = p.scale;
@@ -271,7 +293,7 @@ __device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, const E
     // the second, one 8-column group at a time; a gated postact waits in
     // registers for the first box to be read, then goes out through it
     staging_acquire(e);
-    const bool want_a = P.mapO[NOUT - 1] >= 0;
+    const bool want_a = P.out[NOUT - 1] != nullptr;
     const uint32_t rb = static_cast<uint32_t>(e.lane) * 64u;
     const uint32_t x = (static_cast<uint32_t>(e.lane) >> 1) & 3u;
     uint32_t pa[16];
@@ -335,10 +357,10 @@ __device__ __forceinline__ void epi_dact(const Params& p, const Prob& P, const E
 // unfused path takes when it stores P in bf16, and the accumulator is
 // handed back to the MMAs, which compute the next p while phase 2 runs.
 template <int ACT>
-__device__ __forceinline__ void epi_recomp_p(const Params& p, const Prob& P, EpiWarp& e,
+__device__ __forceinline__ void epi_recomp_p(const Params& p, const EpiUnit& P, EpiWarp& e,
                                              uint32_t tb, int col0, int cb, uint32_t (&dd)[64]) {
   const float s = p.scale;
-  const bool want_a = P.mapO[1] >= 0;
+  const bool want_a = P.out[1] != nullptr;
 #pragma unroll
   for (int ci = 0; ci < 4; ++ci) {
     const int c = cb + 32 * ci;
@@ -368,7 +390,7 @@ __device__ __forceinline__ void epi_recomp_p(const Params& p, const Prob& P, Epi
 }
 
 // Phase 2, accumulator dh = dout Wd: dP = dh * s*act'(p) through map 0.
-__device__ __forceinline__ void epi_recomp_dh(const Params& p, const Prob& P, EpiWarp& e,
+__device__ __forceinline__ void epi_recomp_dh(const Params& p, const EpiUnit& P, EpiWarp& e,
                                               uint32_t tb, int col0, int cb,
                                               const uint32_t (&dd)[64]) {
 #pragma unroll
@@ -395,7 +417,7 @@ __device__ __forceinline__ void epi_recomp_dh(const Params& p, const Prob& P, Ep
 }
 
 template <int EPI>
-__device__ __forceinline__ void epi_plain(const Params& p, const Prob& P, const EpiWarp& e,
+__device__ __forceinline__ void epi_plain(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                           uint32_t tb, int col0, int cb, int ce) {
 #pragma unroll 1
   for (int c = cb; c < ce; c += 32) {
@@ -443,6 +465,41 @@ struct Cfg {
   static_assert(SMEM <= MAX_SMEM, "shared memory over the limit");
 };
 
+// What the producer needs of a work unit, read from the launch parameters
+// once per unit and then kept in registers: the TMA issue loop must not go
+// back to parameter memory (a generic load, re-issued after every copy's
+// memory clobber) for every k-block.
+struct UnitLoads {
+  const CUtensorMap* a0;  // A operand of segment 0 / 1
+  const CUtensorMap* a1;
+  const CUtensorMap* b0;  // B operand of segment 0 / 1 (gated: this CTA's gate or up rows)
+  const CUtensorMap* b1;
+  int m0;                 // this CTA's first A row (K-major) / column (MN-major)
+  int n0;                 // this CTA's first B row
+  int kb0;                // k-blocks of segment 0
+};
+
+template <int EPI, int CG>
+__device__ __forceinline__ UnitLoads unit_loads(const Params& p, const Prob& P, const Work& w,
+                                                uint32_t rank) {
+  UnitLoads L;
+  L.a0 = &p.maps[P.mapA0];
+  L.a1 = &p.maps[P.mapA1];
+  L.m0 = w.tm * (BM * CG) + static_cast<int>(rank) * BM;
+  L.kb0 = P.kb0;
+  if constexpr (EPI == EPI_GATED_FWD) {
+    // CG=1: both weights' rows; CG=2: the leader stages the gate rows, the peer the up rows
+    L.b0 = &p.maps[(CG == 2 && rank != 0) ? P.mapB1 : P.mapB0];
+    L.b1 = &p.maps[P.mapB1];
+    L.n0 = w.tn * 128;
+  } else {
+    L.b0 = &p.maps[P.mapB0];
+    L.b1 = &p.maps[P.mapB1];
+    L.n0 = w.tn * MMA_N + static_cast<int>(rank) * (MMA_N / CG);
+  }
+  return L;
+}
+
 // Issues the TMA boxes of one k-block into this CTA's stage (A at sA, B at
 // sB), completing on barrier `full` (for a pair: the leader's barrier).
 //   A K-major: one box {64 k, 128 rows};  A MN-major: two boxes {64 m, 64 k}.
@@ -451,38 +508,31 @@ struct Cfg {
 //   B K-major: one box {64, 256 / CG};      B MN-major: 4 / CG boxes {64 n, 64 k}.
 //   EPI_DACT_RECOMP: segment 0 B K-major (W1), segment 1 B MN-major (Wd).
 template <int EPI, bool A_MN, bool B_MN, int CG>
-__device__ __forceinline__ void load_stage(const Params& p, const Prob& P, const Work& w, int seg,
-                                           int kc, uint32_t sA, uint32_t sB, uint32_t full,
-                                           uint32_t rank, uint64_t pol) {
+__device__ __forceinline__ void load_stage(const UnitLoads& L, int seg, int kc, uint32_t sA,
+                                           uint32_t sB, uint32_t full, uint64_t pol) {
   auto ld = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
     if constexpr (CG == 2) tma_load_2d_pair(dst, m, c0, c1, full, pol);
     else tma_load_2d(dst, m, c0, c1, full, pol);
   };
-  const CUtensorMap* mA = &p.maps[seg == 0 ? P.mapA0 : P.mapA1];
-  const int m0 = w.tm * (BM * CG) + static_cast<int>(rank) * BM;
+  const CUtensorMap* mA = seg == 0 ? L.a0 : L.a1;
   if constexpr (!A_MN) {
-    ld(sA, mA, kc, m0);
+    ld(sA, mA, kc, L.m0);
   } else {
-    ld(sA, mA, m0, kc);
-    ld(sA + 8192, mA, m0 + 64, kc);
+    ld(sA, mA, L.m0, kc);
+    ld(sA + 8192, mA, L.m0 + 64, kc);
   }
   if constexpr (EPI == EPI_GATED_FWD) {
-    if constexpr (CG == 1) {
-      ld(sB, &p.maps[P.mapB0], kc, w.tn * 128);
-      ld(sB + 16384, &p.maps[P.mapB1], kc, w.tn * 128);
-    } else {
-      ld(sB, &p.maps[rank == 0 ? P.mapB0 : P.mapB1], kc, w.tn * 128);
-    }
+    ld(sB, L.b0, kc, L.n0);
+    if constexpr (CG == 1) ld(sB + 16384, L.b1, kc, L.n0);
   } else {
-    const CUtensorMap* mB = &p.maps[seg == 0 ? P.mapB0 : P.mapB1];
-    const int n0 = w.tn * MMA_N + static_cast<int>(rank) * (MMA_N / CG);
+    const CUtensorMap* mB = seg == 0 ? L.b0 : L.b1;
     // the fused recompute reads W1 (K-major) in segment 0, Wd (MN-major) in 1
     const bool b_mn = EPI == EPI_DACT_RECOMP ? seg == 1 : B_MN;
     if (!b_mn) {
-      ld(sB, mB, kc, n0);
+      ld(sB, mB, kc, L.n0);
     } else {
 #pragma unroll
-      for (int j = 0; j < 4 / CG; ++j) ld(sB + j * 8192, mB, n0 + j * 64, kc);
+      for (int j = 0; j < 4 / CG; ++j) ld(sB + j * 8192, mB, L.n0 + j * 64, kc);
     }
   }
 }
@@ -565,6 +615,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_normal();
+      const uint32_t tx_bytes = CG * (p.a_tx_bytes + C::B_BYTES);
       int stage = 0;
       uint32_t phase = 0;
       int slot = 0;
@@ -593,7 +644,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
           if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
           if (done) break;
           const Work w = decode_unit(p, unit);
-          const Prob& P = p.prob[w.prob];
+          const UnitLoads L = unit_loads<EPI, CG>(p, p.prob[w.prob], w, rank);
           for (int kb = w.kb_begin; kb < w.kb_end && ok; ++kb) {
             if (!mbar_wait<PAIR>(bar_s(EMPTY + stage), phase ^ 1u, lim, abort_flag)) {
               ok = false;
@@ -602,11 +653,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
             const uint32_t full = bar_s(FULL + stage);
             // the leader's full barrier expects the bytes of both CTAs of a pair
             // (the A boxes of an output with few rows cover only those rows)
-            mbar_expect_tx(full, CG * (p.a_tx_bytes + C::B_BYTES));
-            const int seg = kb < P.kb0 ? 0 : 1;
-            const int kc = (seg == 0 ? kb : kb - P.kb0) * BK;
+            mbar_expect_tx(full, tx_bytes);
+            const int seg = kb < L.kb0 ? 0 : 1;
+            const int kc = (seg == 0 ? kb : kb - L.kb0) * BK;
             const uint32_t sA = base_s + stage * C::STAGE;
-            load_stage<EPI, A_MN, B_MN, CG>(p, P, w, seg, kc, sA, sA + C::A_BYTES, full, rank, pol);
+            load_stage<EPI, A_MN, B_MN, CG>(L, seg, kc, sA, sA + C::A_BYTES, full, pol);
             ++issued;
             if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
           }
@@ -622,18 +673,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
           if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
           if (v < 0) break;
           const Work w = decode_unit(p, v);
-          const Prob& P = p.prob[w.prob];
+          const UnitLoads L = unit_loads<EPI, CG>(p, p.prob[w.prob], w, rank);
           const uint32_t full_lead = lead(bar_s(FULL));
           for (int kb = w.kb_begin; kb < w.kb_end && ok; ++kb) {
             if (!mbar_wait<PAIR>(bar_s(EMPTY + stage), phase ^ 1u, lim, abort_flag)) {
               ok = false;
               break;
             }
-            const int seg = kb < P.kb0 ? 0 : 1;
-            const int kc = (seg == 0 ? kb : kb - P.kb0) * BK;
+            const int seg = kb < L.kb0 ? 0 : 1;
+            const int kc = (seg == 0 ? kb : kb - L.kb0) * BK;
             const uint32_t sA = base_s + stage * C::STAGE;
-            load_stage<EPI, A_MN, B_MN, CG>(p, P, w, seg, kc, sA, sA + C::A_BYTES,
-                                            full_lead + 8u * stage, rank, pol);
+            load_stage<EPI, A_MN, B_MN, CG>(L, seg, kc, sA, sA + C::A_BYTES,
+                                            full_lead + 8u * stage, pol);
             ++issued;
             if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
           }
@@ -759,7 +810,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
       if (unit < 0) break;
       const Work w = decode_unit(p, unit);
-      const Prob& P = p.prob[w.prob];
+      const EpiUnit P = epi_unit(p, p.prob[w.prob]);
       e.row0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
       e.rows_ok = e.row0 < P.M;
       const int col0 = w.tn * TILE_N;
