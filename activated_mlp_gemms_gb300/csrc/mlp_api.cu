@@ -11,7 +11,8 @@
 //     1. dgated GEMM  dout Wd  (K = H), epilogue dG, dU over G, U and the postact a
 //     2. dx GEMM      [dG|dU] [Wg;Wu]  (K = 2I, one accumulator)
 //     3. one grouped launch of the weight gradients dWg = dG^T x, dWu = dU^T x,
-//        dWd = dout^T a  (K = M), bf16 store or fp32 in-place accumulation
+//        dWd = dout^T a  (K = M), bf16 store or fp32 in-place accumulation,
+//        on a second stream beside stage 2 when both are requested
 //   mlp_bwd_recompute
 //     0. gate/up GEMM storing only G, U into the workspace, then as mlp_bwd.
 //     Non-gated with dx/dWg requested: stages 0 and 1 are one kernel whose
@@ -253,6 +254,39 @@ struct Call {
 
 int cuda_err(cudaError_t e) { return e == cudaSuccess ? MLP_OK : MLP_ERR_CUDA; }
 
+// A second stream per device for GEMMs that may run beside the caller's
+// (the weight gradients beside dx), with the events of the fork and the
+// join.  `mu` is held from the fork to the join so that concurrent calls do
+// not interleave their records and waits.
+struct Side {
+  std::mutex mu;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ok = false;
+};
+Side g_side[64];
+std::mutex g_side_mu;
+
+// The current device's side stream, created on first use; nullptr when it
+// cannot be had (no device, creation failed, or first asked for while
+// `caller` is being captured into a graph).
+Side* side_stream(cudaStream_t caller) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  Side& sd = g_side[dev];
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  if (sd.ok) return &sd;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return nullptr;
+  if (cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+  if (cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess)
+    return nullptr;
+  sd.ok = true;
+  return &sd;
+}
+
 // ------------------------------------------------------------ tracing
 // When enabled, every kernel launch is bracketed by a pair of CUDA events on
 // its stream; mlp_trace_read returns (kernel tag, milliseconds) per launch.
@@ -262,6 +296,7 @@ struct TraceRec {
 };
 std::mutex g_trace_mu;
 bool g_trace_on = false;
+std::atomic<bool> g_trace_flag{false};  // g_trace_on, readable without the lock
 std::vector<TraceRec> g_trace;
 std::vector<cudaEvent_t> g_event_pool;
 
@@ -638,6 +673,21 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
   void* dG = G;
   void* dU = U;
 
+  // Stages 2 and 3 read only what stage 1 wrote (and the inputs).  With both
+  // requested, the weight gradients go to the side stream, forked after
+  // stage 1 and joined before the call returns: dx, enqueued first and
+  // launched early through PDL, takes the SMs, and the weight-gradient CTAs
+  // take those that dx's last, partial wave of tiles leaves idle.
+  // (With tracing on, kernels run one after another so that each traced
+  // duration is the kernel's own.)
+  const bool want_w = dWg || dWu || dWd;
+  Side* side = (dx && want_w && !g_trace_flag.load()) ? side_stream(c.stream) : nullptr;
+  std::unique_lock<std::mutex> side_lk;
+  if (side) {
+    side_lk = std::unique_lock<std::mutex>(side->mu);
+    MLP_TRY(cuda_err(cudaEventRecord(side->fork, c.stream)));
+  }
+
   if (dx) {
     // stage 2: dx = [dG|dU] [Wg;Wu], one accumulator over K = 2I (non-gated: K = I)
     Gemm g(*p, c.counter(), c.status, pick_cg(M));
@@ -663,9 +713,15 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     }
   }
 
-  if (dWg || dWu || dWd) {
+  if (want_w) {
     // stage 3: weight gradients in one grouped launch, reduced over the M tokens:
     //   dWg = dG^T x, dWu = dU^T x  ([I,H])   dWd = dout^T a  ([H,I])
+    Call cw = c;  // same control block; the side stream when forked
+    if (side) {
+      cw.stream = side->stream;
+      cw.launches = 0;  // its first kernel follows an event wait, not a kernel
+      MLP_TRY(cuda_err(cudaStreamWaitEvent(side->stream, side->fork, 0)));
+    }
     Gemm g(*p, c.counter(), c.status, pick_cg(H < I ? H : I));
     struct W { const void* A; int rows; const void* B; int cols; void* out; };
     W list[3];
@@ -696,9 +752,13 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
       P.mapO[0] = oW;
     }
     if (fuse) {
-      MLP_TRY((run<EPI_ACCUM_F32, true, true>(g, c, MLP_KERNEL_WGRAD)));
+      MLP_TRY((run<EPI_ACCUM_F32, true, true>(g, cw, MLP_KERNEL_WGRAD)));
     } else {
-      MLP_TRY((run<EPI_STORE_BF16, true, true>(g, c, MLP_KERNEL_WGRAD)));
+      MLP_TRY((run<EPI_STORE_BF16, true, true>(g, cw, MLP_KERNEL_WGRAD)));
+    }
+    if (side) {
+      MLP_TRY(cuda_err(cudaEventRecord(side->join, side->stream)));
+      MLP_TRY(cuda_err(cudaStreamWaitEvent(c.stream, side->join, 0)));
     }
   }
   return MLP_OK;
@@ -783,6 +843,7 @@ int mlp_debug_set_flags(int flags) {
 int mlp_trace_enable(int on) {
   std::lock_guard<std::mutex> lk(g_trace_mu);
   g_trace_on = on != 0;
+  g_trace_flag.store(g_trace_on);
   return MLP_OK;
 }
 

@@ -159,7 +159,15 @@ int mlp_fwd_infer(const mlp_problem_t* p, const void* x, const void* Wg, const v
  *                     = 1: fp32, dW += gradient in place (quack
  *                     _compute_weight_grad with fuse_grad_accum).
  * When only dWd is requested, the postact is rebuilt from G/U without the
- * activation derivative (quack MLPRecomputeFunc.backward, "only dW2 needed"). */
+ * activation derivative (quack MLPRecomputeFunc.backward, "only dW2 needed").
+ * Streams: when dx and a weight gradient are both requested, the weight
+ * gradients run on a second stream the library keeps per device, forked
+ * from `stream` after the dgated GEMM and joined back into it before the
+ * call returns (event record / wait, so the call stays capturable into a
+ * CUDA graph once one direct backward call on the device has created that
+ * stream).  Work enqueued on `stream` after the call sees every output.
+ * Calls from several host threads or streams on one device are safe; a
+ * capture and eager calls on one device should not overlap in time. */
 int mlp_bwd(const mlp_problem_t* p, const void* dout, const void* x, const void* Wg,
             const void* Wu, const void* Wd, void* G, void* U, void* dx,
             void* dWg, void* dWu, void* dWd, int fuse_grad_accum,
@@ -239,7 +247,9 @@ int mlp_debug_set_flags(int flags);
  * With tracing on, every kernel launch of the calls above is bracketed by
  * a pair of CUDA events recorded on the call's stream (this may keep
  * consecutive kernels from overlapping through programmatic dependent
- * launch).  Kernel tags: */
+ * launch), and the backward runs its weight-gradient GEMMs after dx on the
+ * call's stream instead of beside it on the library's second stream, so
+ * that each traced duration is one kernel's own.  Kernel tags: */
 typedef enum {
   MLP_KERNEL_GATE_UP = 0,  /* gate/up (or fc1) GEMM with the activation epilogue */
   MLP_KERNEL_DOWN = 1,     /* down projection GEMM */
