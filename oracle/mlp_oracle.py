@@ -229,6 +229,52 @@ def sampled_inter_units(cols, dout, x, Wg, Wu, Wd, act="swiglu", gate_mult=1.0,
     return res
 
 
+# ---------------------------------------------------------------------------
+# The MLP block with its neighbours (modded-nanogpt track_1_short/model/gpt.py,
+# the "process mlp" step of the layer loop): the input is RMS-normalised,
+# ``mlp_in = norm(x)``, and the output joins the residual stream through
+# ``x = scale_add(resid_lambdas_mlp[i], x, post_lambdas_mlp[i], mlp_out)``.
+# Readings (the pages show the calls, not the bodies): ``norm`` is an RMS
+# norm over the last axis with no learned weight, x / sqrt(mean(x^2) + eps);
+# ``scale_add(a, x, b, y)`` is a*x + b*y, as the page's other branch
+# ``scale(resid_lambdas_mlp[i], x) + mlp_out`` (post-lambda folded) shows.
+# ---------------------------------------------------------------------------
+
+def rms_norm(x, eps):
+    """``norm(x)`` of the block: ``x / r`` with ``r = sqrt(mean(x^2) + eps)``
+    over the last axis (one value per token).  Returns ``(n, r)``."""
+    r = np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return x / r, r
+
+
+def block_forward(x, Wg, Wu, Wd, act="relu_sq", gate_mult=1.0, down_mult=1.0,
+                  resid_lambda=1.0, post_lambda=1.0, eps=2.0 ** -7):
+    """``y = resid_lambda * x + post_lambda * MLP(norm(x))``.
+
+    Returns ``y``, the normalised input ``n``, ``rstd = 1 / r`` (per token,
+    shape ``[M]``) and the MLP output ``mlp_out``."""
+    n, r = rms_norm(x, eps)
+    fw = mlp_forward(n, Wg, Wu, Wd, act, gate_mult, down_mult)
+    y = resid_lambda * x + post_lambda * fw["out"]
+    return {"y": y, "n": n, "rstd": 1.0 / r[:, 0], "mlp_out": fw["out"]}
+
+
+def block_backward(dy, x, Wg, Wu, Wd, act="relu_sq", gate_mult=1.0, down_mult=1.0,
+                   resid_lambda=1.0, post_lambda=1.0, eps=2.0 ** -7, dW_prev=None):
+    """Backward pass of ``block_forward`` for the upstream gradient ``dy``.
+
+    The MLP sees ``n = norm(x)`` and the gradient ``post_lambda * dy``; its
+    input gradient ``dn`` goes back through the RMS norm by the derivative
+    of ``n = x / r``, ``dx = (dn - n * mean(dn * n)) / r`` (per token), and
+    the residual branch adds ``resid_lambda * dy``."""
+    n, r = rms_norm(x, eps)
+    bw = mlp_backward(post_lambda * dy, n, Wg, Wu, Wd, act, gate_mult, down_mult,
+                      dW_prev=dW_prev)
+    dn = bw["dx"]
+    dx = resid_lambda * dy + (dn - n * np.mean(dn * n, axis=-1, keepdims=True)) / r
+    return {"dx": dx, "dWg": bw["dWg"], "dWu": bw["dWu"], "dWd": bw["dWd"]}
+
+
 def rel_err(got, ref):
     """The parity metric: max|got - ref| / max|ref| (0 if both are zero)."""
     got = np.asarray(got, dtype=np.float64)
