@@ -23,6 +23,7 @@ __all__ = [
     "mlp_bwd", "mlp_bwd_recompute", "mlp_status_string", "mlp_device_status", "mlp_version",
     "MODE_FWD", "MODE_INFER", "MODE_BWD", "MODE_BWD_RECOMPUTE", "mlp_trace_enable",
     "mlp_trace_read", "mlp_kernel_name", "mlp_set_tile_policy", "mlp_fwd_infer_noalloc",
+    "Block", "block", "mlp_block_fwd", "mlp_block_bwd",
     "NOALLOC_SCRATCH_BYTES", "mlp_set_wait_timeout_ms", "mlp_debug_set_flags", "DEBUG_NO_WORK",
 ]
 
@@ -50,6 +51,12 @@ class Problem(ctypes.Structure):
                 ("down_mult", ctypes.c_float)]
 
 
+class Block(ctypes.Structure):
+    """mlp_block_t: y = resid_lambda * x + post_lambda * MLP(x / sqrt(mean x^2 + eps))"""
+    _fields_ = [("resid_lambda", ctypes.c_float), ("post_lambda", ctypes.c_float),
+                ("eps", ctypes.c_float)]
+
+
 _LIB = None
 _VP = ctypes.c_void_p
 
@@ -74,6 +81,11 @@ def lib():
     L.mlp_bwd.restype = ctypes.c_int
     L.mlp_bwd_recompute.argtypes = [P] + [_VP] * 9 + [ctypes.c_int, _VP, ctypes.c_size_t, _VP]
     L.mlp_bwd_recompute.restype = ctypes.c_int
+    B = ctypes.POINTER(Block)
+    L.mlp_block_fwd.argtypes = [P, B] + [_VP] * 8 + [_VP, ctypes.c_size_t, _VP]
+    L.mlp_block_fwd.restype = ctypes.c_int
+    L.mlp_block_bwd.argtypes = [P, B] + [_VP] * 12 + [ctypes.c_int, _VP, ctypes.c_size_t, _VP]
+    L.mlp_block_bwd.restype = ctypes.c_int
     L.mlp_status_string.argtypes = [ctypes.c_int]
     L.mlp_status_string.restype = ctypes.c_char_p
     L.mlp_device_status.argtypes = [_VP, _VP]
@@ -103,6 +115,10 @@ def problem(M, H, I, act="swiglu", gate_mult=1.0, down_mult=1.0) -> Problem:
     if act not in ACTS:
         raise ValueError(f"unknown activation {act!r}; one of {list(ACTS)}")
     return Problem(int(M), int(H), int(I), ACTS[act], float(gate_mult), float(down_mult))
+
+
+def block(resid_lambda=1.0, post_lambda=1.0, eps=2.0 ** -7) -> Block:
+    return Block(float(resid_lambda), float(post_lambda), float(eps))
 
 
 def _ptr(t, dtype=torch.bfloat16, name="tensor"):
@@ -210,6 +226,38 @@ def mlp_bwd_recompute(prob: Problem, dout, x, Wg, Wu, Wd, dx=None, dWg=None, dWu
                                  _ptr(dWd, wd, "dWd"), int(bool(fuse_grad_accum)),
                                  ws.data_ptr(), ws.numel(), _stream(stream))
     _check(rc, "mlp_bwd_recompute")
+    return ws
+
+
+def mlp_block_fwd(prob: Problem, blk: Block, x, Wg, Wu, Wd, y, G_save=None, U_save=None,
+                  rstd=None, ws=None, stream=None):
+    """The MLP block: y = resid_lambda x + post_lambda MLP(RMSNorm(x)).  Returns
+    (rstd, ws): the fp32 per-token 1/r the backward takes, and the workspace."""
+    ws = _ws(ws, prob, MODE_FWD, x.device)
+    if rstd is None:
+        rstd = torch.empty(prob.M, dtype=torch.float32, device=x.device)
+    rc = lib().mlp_block_fwd(ctypes.byref(prob), ctypes.byref(blk), _ptr(x, name="x"),
+                             _ptr(Wg, name="Wg"), _ptr(Wu, name="Wu"), _ptr(Wd, name="Wd"),
+                             _ptr(y, name="y"), _ptr(G_save, name="G_save"),
+                             _ptr(U_save, name="U_save"), _ptr(rstd, torch.float32, "rstd"),
+                             ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(rc, "mlp_block_fwd")
+    return rstd, ws
+
+
+def mlp_block_bwd(prob: Problem, blk: Block, dy, x, Wg, Wu, Wd, G, U, rstd, dx=None, dWg=None,
+                  dWu=None, dWd=None, fuse_grad_accum=False, ws=None, stream=None):
+    """Backward of mlp_block_fwd from its saved G, U (overwritten) and rstd."""
+    ws = _ws(ws, prob, MODE_BWD, x.device)
+    wd = _wdt(fuse_grad_accum)
+    rc = lib().mlp_block_bwd(ctypes.byref(prob), ctypes.byref(blk), _ptr(dy, name="dy"),
+                             _ptr(x, name="x"), _ptr(Wg, name="Wg"), _ptr(Wu, name="Wu"),
+                             _ptr(Wd, name="Wd"), _ptr(G, name="G"), _ptr(U, name="U"),
+                             _ptr(rstd, torch.float32, "rstd"), _ptr(dx, name="dx"),
+                             _ptr(dWg, wd, "dWg"), _ptr(dWu, wd, "dWu"), _ptr(dWd, wd, "dWd"),
+                             int(bool(fuse_grad_accum)), ws.data_ptr(), ws.numel(),
+                             _stream(stream))
+    _check(rc, "mlp_block_bwd")
     return ws
 
 

@@ -101,6 +101,7 @@ struct EpiWarp {
   int row0;      // first of the warp's 32 rows
   bool rows_ok;  // any of the 32 rows inside the output
   uint32_t box;  // EPI_DACT_RECOMP: which of the two boxes the next chunk fills
+  float rs;      // this lane's row scale (the block's RMS norm; 1 without it)
 };
 
 // Stage this lane's 32 bf16 (16 packed words) into a 64B-swizzled 32x32 box.
@@ -127,8 +128,10 @@ __device__ __forceinline__ void stage_f32(uint32_t buf, int r, const uint32_t (&
 struct EpiUnit {
   const CUtensorMap* out[3];  // output maps (nullptr: output not written)
   int M, N, ld;
-  const void* in0;            // saved preacts (derivative epilogues)
+  const void* in0;            // saved preacts (derivative epilogues); the residual (plain store)
   const void* in1;
+  const float* rstd;          // per-row scale (nullptr: none)
+  float alpha;                // residual scale
 };
 
 __device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P) {
@@ -140,6 +143,8 @@ __device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P) {
   U.ld = P.ld;
   U.in0 = P.in0;
   U.in1 = P.in1;
+  U.rstd = P.rstd;
+  U.alpha = P.alpha;
   return U;
 }
 
@@ -203,8 +208,9 @@ __device__ __forceinline__ void epi_gated_fwd(const Params& p, const EpiUnit& P,
     uint32_t pa[16], pg[16], pu[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
-      const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+      // the block's RMS norm of the input row, applied to the preacts
+      const float g0 = e.rs * __uint_as_float(g[2 * j]), g1 = e.rs * __uint_as_float(g[2 * j + 1]);
+      const float u0 = e.rs * __uint_as_float(u[2 * j]), u1 = e.rs * __uint_as_float(u[2 * j + 1]);
       pa[j] = pack_bf16x2(s * act_f<ACT>(g0) * u0, s * act_f<ACT>(g1) * u1);
       pg[j] = pack_bf16x2(g0, g1);
       pu[j] = pack_bf16x2(u0, u1);
@@ -238,7 +244,7 @@ __device__ __forceinline__ void epi_act_fwd(const Params& p, const EpiUnit& P, c
     uint32_t pa[16], pp[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const float z0 = __uint_as_float(z[2 * j]), z1 = __uint_as_float(z[2 * j + 1]);
+      const float z0 = e.rs * __uint_as_float(z[2 * j]), z1 = e.rs * __uint_as_float(z[2 * j + 1]);
       pa[j] = pack_bf16x2(s * act_f<ACT>(z0), s * act_f<ACT>(z1));
       pp[j] = pack_bf16x2(z0, z1);
     }
@@ -277,6 +283,7 @@ __device__ __forceinline__ void epi_dact(const Params& p, const EpiUnit& P, cons
                                          uint32_t tb, int col0, int cb, int ce, uint4 (&pg)[4],
                                          uint4 (&pu)[4]) {
   const float s = p.scale;
+  const float sr = s * e.rs;
   const int row = e.row0 + e.lane;
   constexpr int NOUT = GATED ? 3 : 2;
 #pragma unroll 1
@@ -305,8 +312,10 @@ __device__ __forceinline__ void epi_dact(const Params& p, const EpiUnit& P, cons
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float2 gg = unpack_bf16x2(gw[j]);
-        const float dh0 = s * __uint_as_float(d[8 * v + 2 * j]);
-        const float dh1 = s * __uint_as_float(d[8 * v + 2 * j + 1]);
+        // (times the row scale of the block's RMS norm: the weight and input
+        // gradients then come out in terms of the un-normalised input)
+        const float dh0 = sr * __uint_as_float(d[8 * v + 2 * j]);
+        const float dh1 = sr * __uint_as_float(d[8 * v + 2 * j + 1]);
         float a0, da0, a1, da1;
         act_and_grad<ACT>(gg.x, a0, da0);
         act_and_grad<ACT>(gg.y, a1, da1);
@@ -430,9 +439,28 @@ __device__ __forceinline__ void epi_plain(const Params& p, const EpiUnit& P, con
     staging_acquire(e);
     if constexpr (EPI == EPI_STORE_BF16) {
       uint32_t q[16];
+      if (P.in0) {
+        // the block's residual add: D = alpha * residual + acc
+        const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(P.in0);
+        const int row = e.row0 + e.lane;
+        const size_t off = static_cast<size_t>(row) * P.ld + col;
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        q[j] = pack_bf16x2(__uint_as_float(d[2 * j]), __uint_as_float(d[2 * j + 1]));
+        for (int v = 0; v < 4; ++v) {
+          const uint4 r = (row < P.M && col + 8 * v < P.N) ? ld_global_v4(res + off + 8 * v)
+                                                          : make_uint4(0, 0, 0, 0);
+          const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = unpack_bf16x2(rw[j]);
+            q[4 * v + j] = pack_bf16x2(P.alpha * f.x + __uint_as_float(d[8 * v + 2 * j]),
+                                       P.alpha * f.y + __uint_as_float(d[8 * v + 2 * j + 1]));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          q[j] = pack_bf16x2(__uint_as_float(d[2 * j]), __uint_as_float(d[2 * j + 1]));
+      }
       stage_bf16(e.stg, e.lane, q);
       flush_chunk<1, 2048, false>(p, P, e, col);
     } else {
@@ -813,6 +841,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       const EpiUnit P = epi_unit(p, p.prob[w.prob]);
       e.row0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
       e.rows_ok = e.row0 < P.M;
+      e.rs = (P.rstd && e.row0 + lane < P.M) ? P.rstd[e.row0 + lane] : 1.f;
       const int col0 = w.tn * TILE_N;
       uint4 pg[4], pu[4];
       uint32_t dd[EPI == EPI_DACT_RECOMP ? 64 : 1];  // s*act'(p) between the two phases

@@ -53,6 +53,11 @@ struct Prob {
   void* out2;
   const void* in0;
   const void* in1;
+  // the MLP block's neighbours (0 / nullptr: none):
+  const float* rstd;      // per output row: gate/up accumulators (activation forward) and
+                          // dG, dU / dP (derivative epilogues) are multiplied by rstd[row]
+  float alpha;            // EPI_STORE_BF16 with in0 = residual [M, ld]: D = alpha*in0 + acc
+  int pad_b;
 };
 
 struct Params {  // 64-byte aligned through CUtensorMap
@@ -87,8 +92,17 @@ int max_groups();
 cudaError_t launch_postact(const void* G, const void* U, void* a, long long n, int act,
                            float scale, cudaStream_t stream, bool pdl);
 
-// fp32 -> bf16 (round to nearest even), n elements (a multiple of 8).
+// fp32 -> bf16 (round to nearest even), n elements (a multiple of 8); with
+// `resid` (bf16, n elements) the result is src + alpha * resid.
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, long long n, cudaStream_t stream,
-                               bool pdl);
+                               bool pdl, const void* resid = nullptr, float alpha = 0.f);
+
+// Per-token RMS-norm scale rstd[m] = 1 / sqrt(mean_h x^2 + eps), x bf16 [M, H].
+cudaError_t launch_rstd(const void* x, float* rstd, int M, int H, float eps, cudaStream_t stream,
+                        bool pdl);
+
+// In place over dx (holding D = dn * rstd): dx = alpha dy + D - (rstd^2 / H) (sum_h D x) x.
+cudaError_t launch_rmsnorm_bwd(void* dx, const void* x, const void* dy, const float* rstd, int M,
+                               int H, float alpha, cudaStream_t stream, bool pdl);
 
 }  // namespace mlpk

@@ -73,25 +73,38 @@ cudaError_t launch_postact(const void* G, const void* U, void* a, long long n, i
 }
 
 // fp32 -> bf16 over n elements, 8 per thread per step (two 16-byte loads,
-// one 16-byte store); the split-K partial sums of a decode-sized output.
+// one 16-byte store); the split-K partial sums of a decode-sized output,
+// plus alpha * resid when a residual is given.
 __global__ void __launch_bounds__(256) k_f32_to_bf16(const float* __restrict__ src,
-                                                     __nv_bfloat16* __restrict__ dst, long long n8) {
+                                                     __nv_bfloat16* __restrict__ dst, long long n8,
+                                                     const __nv_bfloat16* __restrict__ resid,
+                                                     float alpha) {
   pdl_wait();
   pdl_launch_dependents();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
        i += (long long)gridDim.x * blockDim.x) {
     const uint4 a = ld_global_v4(src + 8 * i);
     const uint4 b = ld_global_v4(src + 8 * i + 4);
-    st_global_v4(dst + 8 * i,
-                 make_uint4(pack_bf16x2(__uint_as_float(a.x), __uint_as_float(a.y)),
-                            pack_bf16x2(__uint_as_float(a.z), __uint_as_float(a.w)),
-                            pack_bf16x2(__uint_as_float(b.x), __uint_as_float(b.y)),
-                            pack_bf16x2(__uint_as_float(b.z), __uint_as_float(b.w))));
+    float v[8] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
+                  __uint_as_float(a.w), __uint_as_float(b.x), __uint_as_float(b.y),
+                  __uint_as_float(b.z), __uint_as_float(b.w)};
+    if (resid) {
+      const uint4 r = ld_global_v4(resid + 8 * i);
+      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = unpack_bf16x2(rw[j]);
+        v[2 * j] += alpha * f.x;
+        v[2 * j + 1] += alpha * f.y;
+      }
+    }
+    st_global_v4(dst + 8 * i, make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                         pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7])));
   }
 }
 
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, long long n, cudaStream_t stream,
-                               bool pdl) {
+                               bool pdl, const void* resid, float alpha) {
   const long long n8 = n / 8;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -108,7 +121,8 @@ cudaError_t launch_f32_to_bf16(const float* src, void* dst, long long n, cudaStr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_f32_to_bf16, src, static_cast<__nv_bfloat16*>(dst), n8);
+  return cudaLaunchKernelEx(&cfg, k_f32_to_bf16, src, static_cast<__nv_bfloat16*>(dst), n8,
+                            static_cast<const __nv_bfloat16*>(resid), alpha);
 }
 
 }  // namespace mlpk

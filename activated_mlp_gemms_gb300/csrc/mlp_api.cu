@@ -466,6 +466,14 @@ int check_weights(const mlp_problem_t* p, const void* Wg, const void* Wu, const 
   return MLP_OK;
 }
 
+int check_block(const mlp_block_t* b) {
+  if (!b) return MLP_ERR_INVALID_ARG;
+  if (!std::isfinite(b->resid_lambda) || !std::isfinite(b->post_lambda) ||
+      !std::isfinite(b->eps) || b->eps < 0.f)
+    return MLP_ERR_INVALID_ARG;
+  return MLP_OK;
+}
+
 int check_ws(const mlp_problem_t* p, int mode, const void* ws, size_t ws_bytes) {
   if (!ws) return MLP_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return MLP_ERR_ALIGNMENT;
@@ -480,10 +488,20 @@ int begin_call(Call& c, void* ws, void* stream) {
   return cuda_err(cudaMemsetAsync(ws, 0, CTRL_BYTES, c.stream));
 }
 
+// The MLP block's neighbours (mlp_block_fwd / mlp_block_bwd); nullptr for
+// the plain MLP.
+struct Block {
+  float alpha;        // the residual stream's scale (resid_lambda)
+  float eps;          // the RMS norm's epsilon
+  float* rstd_out;    // forward: where the per-token scale 1/r goes
+  const float* rstd;  // the per-token scale the GEMM epilogues apply
+};
+
 // gate/up (or fc1) GEMM with the activation epilogue.
 //   a_out: postact (may be null), G_out/U_out: preact stores (may be null)
+//   rstd: per-row scale of the accumulators (the block's RMS norm; may be null)
 int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* Wg, const void* Wu,
-                   void* a_out, void* G_out, void* U_out) {
+                   void* a_out, void* G_out, void* U_out, const float* rstd = nullptr) {
   Gemm g(*p, c.counter(), c.status, pick_cg(p->M));
   const int mA = g.kmajor_a(x, p->M, p->H);
   if (gated(p)) {
@@ -499,6 +517,7 @@ int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* W
     P.mapO[0] = oA;
     P.mapO[1] = oG;
     P.mapO[2] = oU;
+    P.rstd = rstd;
     return run_gated<EPI_GATED_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
   }
   const int mW = g.kmajor(Wg, p->I, p->H, g.b_rows());
@@ -509,6 +528,7 @@ int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* W
   P.mapB0 = mW;
   P.mapO[0] = oA;
   P.mapO[1] = oP;
+  P.rstd = rstd;
   return run_nongated<EPI_ACT_FWD, false, false>(g, c, MLP_KERNEL_GATE_UP);
 }
 
@@ -535,16 +555,19 @@ int launch_dact_recomp(const mlp_problem_t* p, Call& c, const void* x, const voi
   return run_nongated<EPI_DACT_RECOMP, false, false>(g, c, MLP_KERNEL_DACT_RECOMPUTE);
 }
 
-// fp32 [n] -> bf16 [n] (the split-K partial-sum region to the output).
-int convert_out(Call& c, const float* part, void* out, long long n) {
+// fp32 [n] -> bf16 [n] (the split-K partial-sum region to the output), plus
+// alpha * resid when the block's residual is given.
+int convert_out(Call& c, const float* part, void* out, long long n, const void* resid = nullptr,
+                float alpha = 0.f) {
   const bool pdl = c.pdl();
   return traced(MLP_KERNEL_CONVERT, c.stream,
-                [&] { return launch_f32_to_bf16(part, out, n, c.stream, pdl); });
+                [&] { return launch_f32_to_bf16(part, out, n, c.stream, pdl, resid, alpha); });
 }
 
-// out = a Wd^T; with split > 1 through the zeroed fp32 region `part`.
+// out = a Wd^T (+ alpha * resid for the block); with split > 1 through the
+// zeroed fp32 region `part`.
 int launch_down(const mlp_problem_t* p, Call& c, const void* a, const void* Wd, void* out,
-                float* part, int split) {
+                float* part, int split, const void* resid = nullptr, float alpha = 0.f) {
   Gemm g(*p, c.counter(), c.status, pick_cg(p->M));
   const int mA = g.kmajor_a(a, p->M, p->I);
   const int mB = g.kmajor(Wd, p->H, p->I, g.b_rows());
@@ -555,19 +578,21 @@ int launch_down(const mlp_problem_t* p, Call& c, const void* a, const void* Wd, 
     P.mapB0 = mB;
     P.mapO[0] = oP;
     MLP_TRY(run<EPI_ACCUM_F32, false, false>(g, c, MLP_KERNEL_DOWN));
-    return convert_out(c, part, out, (long long)p->M * p->H);
+    return convert_out(c, part, out, (long long)p->M * p->H, resid, alpha);
   }
   const int oO = g.output(out, p->M, p->H);
   Prob& P = g.add(p->M, p->H, p->I, 0, MMA_N);
   P.mapA0 = mA;
   P.mapB0 = mB;
   P.mapO[0] = oO;
+  P.in0 = resid;  // the epilogue reads the residual tile before storing over it
+  P.alpha = alpha;
   return run<EPI_STORE_BF16, false, false>(g, c, MLP_KERNEL_DOWN);
 }
 
 int forward(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu, const void* Wd,
             void* out, void* G_save, void* U_save, void* ws, size_t ws_bytes, void* stream,
-            int mode) {
+            int mode, const Block* blk = nullptr) {
   MLP_TRY(check_problem(p));
   MLP_TRY(need(x));
   MLP_TRY(check_weights(p, Wg, Wu, Wd));
@@ -583,13 +608,21 @@ int forward(const mlp_problem_t* p, const void* x, const void* Wg, const void* W
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + split_offset(p, mode));
   if (split > 1)
     MLP_TRY(cuda_err(cudaMemsetAsync(part, 0, (size_t)p->M * p->H * 4, c.stream)));
-  MLP_TRY(launch_fwd_act(p, c, x, Wg, Wu, a, G_save, U_save));
-  return launch_down(p, c, a, Wd, out, part, split);
+  if (blk) {
+    // the block's RMS norm: 1/r per token, applied in the gate/up epilogue
+    const bool pdl = c.pdl();
+    MLP_TRY(traced(MLP_KERNEL_RSTD, c.stream, [&] {
+      return launch_rstd(x, blk->rstd_out, p->M, p->H, blk->eps, c.stream, pdl);
+    }));
+  }
+  MLP_TRY(launch_fwd_act(p, c, x, Wg, Wu, a, G_save, U_save, blk ? blk->rstd : nullptr));
+  return launch_down(p, c, a, Wd, out, part, split, blk ? x : nullptr, blk ? blk->alpha : 0.f);
 }
 
 int backward(const mlp_problem_t* p, const void* dout, const void* x, const void* Wg,
              const void* Wu, const void* Wd, void* G, void* U, void* dx, void* dWg, void* dWu,
-             void* dWd, int fuse, void* ws, size_t ws_bytes, void* stream, bool recompute) {
+             void* dWd, int fuse, void* ws, size_t ws_bytes, void* stream, bool recompute,
+             const Block* blk = nullptr) {
   MLP_TRY(check_problem(p));
   if (fuse != 0 && fuse != 1) return MLP_ERR_INVALID_ARG;
   MLP_TRY(need(dout));
@@ -652,6 +685,7 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     P.mapB0 = mB;
     P.in0 = G;
     P.in1 = U;
+    P.rstd = blk ? blk->rstd : nullptr;  // dG, dU (dP) come out times 1/r
     // gated: dG, dU, a;  non-gated: dP, a
     P.mapO[0] = oG;
     if (gated(p)) {
@@ -710,6 +744,13 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
       MLP_TRY(convert_out(c, part, dx, (long long)M * H));
     } else {
       MLP_TRY((run<EPI_STORE_BF16, false, true>(g, c, MLP_KERNEL_DX)));
+    }
+    if (blk) {
+      // the block: dx holds D = dn / r; through the RMS norm and the residual
+      const bool pdl = c.pdl();
+      MLP_TRY(traced(MLP_KERNEL_RMSNORM_BWD, c.stream, [&] {
+        return launch_rmsnorm_bwd(dx, x, dout, blk->rstd, M, H, blk->alpha, c.stream, pdl);
+      }));
     }
   }
 
@@ -782,6 +823,35 @@ int mlp_fwd(const mlp_problem_t* p, const void* x, const void* Wg, const void* W
 int mlp_fwd_infer(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu,
                   const void* Wd, void* out, void* ws, size_t ws_bytes, void* stream) {
   return forward(p, x, Wg, Wu, Wd, out, nullptr, nullptr, ws, ws_bytes, stream, MLP_MODE_INFER);
+}
+
+int mlp_block_fwd(const mlp_problem_t* p, const mlp_block_t* b, const void* x, const void* Wg,
+                  const void* Wu, const void* Wd, void* y, void* G_save, void* U_save,
+                  float* rstd_save, void* ws, size_t ws_bytes, void* stream) {
+  MLP_TRY(check_problem(p));
+  MLP_TRY(check_block(b));
+  MLP_TRY(need(rstd_save));
+  mlp_problem_t q = *p;
+  q.down_mult *= b->post_lambda;  // post_lambda scales the MLP output
+  const Block blk{b->resid_lambda, b->eps, rstd_save, rstd_save};
+  return forward(&q, x, Wg, Wu, Wd, y, G_save, U_save, ws, ws_bytes, stream, MLP_MODE_FWD, &blk);
+}
+
+int mlp_block_bwd(const mlp_problem_t* p, const mlp_block_t* b, const void* dy, const void* x,
+                  const void* Wg, const void* Wu, const void* Wd, void* G, void* U,
+                  const float* rstd, void* dx, void* dWg, void* dWu, void* dWd,
+                  int fuse_grad_accum, void* ws, size_t ws_bytes, void* stream) {
+  MLP_TRY(check_problem(p));
+  MLP_TRY(check_block(b));
+  MLP_TRY(need(rstd));
+  // dx is written while the weight gradients (on the second stream) and
+  // the RMS-norm pass still read x and dy
+  if (dx && (dx == x || dx == dy)) return MLP_ERR_INVALID_ARG;
+  mlp_problem_t q = *p;
+  q.down_mult *= b->post_lambda;
+  const Block blk{b->resid_lambda, b->eps, nullptr, rstd};
+  return backward(&q, dy, x, Wg, Wu, Wd, G, U, dx, dWg, dWu, dWd, fuse_grad_accum, ws, ws_bytes,
+                  stream, false, &blk);
 }
 
 int mlp_bwd(const mlp_problem_t* p, const void* dout, const void* x, const void* Wg,
@@ -878,6 +948,8 @@ const char* mlp_kernel_name(int tag) {
     case MLP_KERNEL_POSTACT: return "postact";
     case MLP_KERNEL_CONVERT: return "convert";
     case MLP_KERNEL_DACT_RECOMPUTE: return "dact_recompute";
+    case MLP_KERNEL_RSTD: return "rstd";
+    case MLP_KERNEL_RMSNORM_BWD: return "rmsnorm_bwd";
     default: return "unknown";
   }
 }

@@ -185,6 +185,51 @@ int mlp_bwd_recompute(const mlp_problem_t* p, const void* dout, const void* x,
                       void* dWg, void* dWu, void* dWd, int fuse_grad_accum,
                       void* ws, size_t ws_bytes, void* stream);
 
+/* ---- The MLP block with its neighbours ----
+ * modded-nanogpt track_1_short/model/gpt.py, the layer loop's "process mlp":
+ * `mlp_in = norm(x)`, the MLP, then
+ * `x = scale_add(resid_lambdas_mlp[i], x, post_lambdas_mlp[i], mlp_out)`:
+ *   y = resid_lambda * x + post_lambda * MLP(x / r),
+ *   r = sqrt(mean_h x^2 + eps) per token (an RMS norm with no weight),
+ * MLP as in mlp_fwd (activation, gate_mult, down_mult of `p`).  The norm is
+ * fused into the gate/up GEMM (its epilogue scales the accumulator rows by
+ * 1/r, computed by a small per-token kernel first), the residual add into
+ * the down projection's epilogue.  Readings: the pages show the calls only;
+ * norm is the plain RMS norm above, scale_add(a, x, b, y) = a x + b y. */
+typedef struct {
+  float resid_lambda;  /* scale of the residual stream x */
+  float post_lambda;   /* scale of the MLP output (folded into down_mult) */
+  float eps;           /* the RMS norm's epsilon (>= 0; F.rms_norm's default for bf16
+                          inputs is 2^-7) */
+} mlp_block_t;
+
+/* Forward of the block.  Arguments as in mlp_fwd, plus
+ *   b          the block's scalars (finite, eps >= 0), else MLP_ERR_INVALID_ARG
+ *   y          bf16 [M,H] out; may be x itself (each element of x is read
+ *              before its tile of y is written)
+ *   G_save, U_save  the preacts of the normalised input, (x/r) Wg^T, (x/r) Wu^T
+ *   rstd_save  fp32 [M] out, 16-byte aligned: 1/r per token (input of the backward)
+ * Workspace: mlp_workspace_size(p, MLP_MODE_FWD). */
+int mlp_block_fwd(const mlp_problem_t* p, const mlp_block_t* b, const void* x, const void* Wg,
+                  const void* Wu, const void* Wd, void* y, void* G_save, void* U_save,
+                  float* rstd_save, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of the block from the saved preacts and rstd (as mlp_bwd):
+ *   dy    bf16 [M,H] in: gradient of y
+ *   dx    bf16 [M,H] out or NULL: resid_lambda dy plus the MLP's input
+ *         gradient taken back through the RMS norm,
+ *         dx = resid_lambda dy + (dn - n mean_h(dn n)) / r;  must not be x or dy
+ *   dWg, dWu, dWd: as in mlp_bwd (gradients w.r.t. the weights of the MLP
+ *         applied to x / r, with post_lambda dy as its output gradient)
+ * The dgated / dact epilogue scales dG, dU (dP) by 1/r, so that dx's GEMM
+ * and the weight gradients work on x itself; a per-token kernel then applies
+ * the norm's projection term and adds the residual's gradient.
+ * Workspace: mlp_workspace_size(p, MLP_MODE_BWD). */
+int mlp_block_bwd(const mlp_problem_t* p, const mlp_block_t* b, const void* dy, const void* x,
+                  const void* Wg, const void* Wu, const void* Wd, void* G, void* U,
+                  const float* rstd, void* dx, void* dWg, void* dWu, void* dWd,
+                  int fuse_grad_accum, void* ws, size_t ws_bytes, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mlp_status_string(int status);
 
@@ -258,8 +303,10 @@ typedef enum {
   MLP_KERNEL_WGRAD = 4,    /* grouped weight-gradient GEMMs */
   MLP_KERNEL_POSTACT = 5,  /* elementwise postact rebuild (dWd-only backward) */
   MLP_KERNEL_CONVERT = 6,  /* fp32 -> bf16 of a split-K output (decode-sized M) */
-  MLP_KERNEL_DACT_RECOMPUTE = 7 /* non-gated recompute: x W1^T and dout Wd in one tile,
-                                   epilogue postact and dP */
+  MLP_KERNEL_DACT_RECOMPUTE = 7, /* non-gated recompute: x W1^T and dout Wd in one tile,
+                                    epilogue postact and dP */
+  MLP_KERNEL_RSTD = 8,          /* the block's per-token RMS-norm scale */
+  MLP_KERNEL_RMSNORM_BWD = 9    /* the block's RMS-norm derivative and residual gradient */
 } mlp_kernel_t;
 
 /* on != 0 starts recording, 0 stops (records already taken are kept). */

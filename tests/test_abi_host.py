@@ -35,7 +35,7 @@ def test_header_declares_the_abi():
                             "mlp_version", "mlp_trace_enable", "mlp_trace_read",
                             "mlp_kernel_name", "mlp_set_tile_policy",
                             "mlp_fwd_infer_noalloc", "mlp_set_wait_timeout_ms",
-                            "mlp_debug_set_flags"])
+                            "mlp_debug_set_flags", "mlp_block_fwd", "mlp_block_bwd"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -115,10 +115,30 @@ def test_backward_validation(L):
                                None, 0, FAKE, 1 << 40, None) == -1
 
 
+def test_block_validation(L):
+    p = m.problem(64, 128, 352, "relu_sq")
+    b = m.block(1.1 ** 0.5, 0.8, 2.0 ** -7)
+    ws = 1 << 40
+    fwd = lambda prob, blk, rstd=FAKE: L.mlp_block_fwd(  # noqa: E731
+        ctypes.byref(prob), blk, FAKE, FAKE, None, FAKE, FAKE, None, None, rstd, FAKE, ws, None)
+    assert fwd(p, None) == -1                       # no block
+    assert fwd(p, ctypes.byref(b), rstd=None) == -1  # rstd required
+    assert fwd(p, ctypes.byref(b), rstd=FAKE + 4) == -2  # rstd 16-byte aligned
+    assert fwd(p, ctypes.byref(m.block(eps=-1.0))) == -1
+    assert fwd(p, ctypes.byref(m.block(post_lambda=float("inf")))) == -1
+    bwd = lambda dx: L.mlp_block_bwd(  # noqa: E731
+        ctypes.byref(p), ctypes.byref(b), FAKE + 256, FAKE, FAKE, None, FAKE, FAKE, None, FAKE,
+        dx, None, None, None, 0, FAKE, ws, None)
+    assert bwd(FAKE) == -1        # dx aliases x
+    assert bwd(FAKE + 256) == -1  # dx aliases dy
+
+
 def test_kernel_names_and_empty_trace(L):
     assert m.mlp_kernel_name(2) == "dgated"
     assert m.mlp_kernel_name(6) == "convert"
     assert m.mlp_kernel_name(7) == "dact_recompute"
+    assert m.mlp_kernel_name(8) == "rstd"
+    assert m.mlp_kernel_name(9) == "rmsnorm_bwd"
     assert m.mlp_kernel_name(99) == "unknown"
     assert m.mlp_trace_read() == []  # nothing recorded: no CUDA call is made
 

@@ -1,0 +1,113 @@
+"""GPU parity of the MLP block with its neighbours (mlp_block_fwd /
+mlp_block_bwd: RMS-normalised input, scaled residual add; modded-nanogpt
+gpt.py, "process mlp") against the fp64 oracle's block_forward /
+block_backward, through the C ABI, on seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import activated_mlp_gemms_gb300 as m
+from activated_mlp_gemms_gb300.workloads import make_inputs, to_f64
+from mlp_gpu_helpers import F32_TOL_MIN_TOKENS, TOL_BF16, TOL_F32, TOL_F32_SMALL
+from oracle import block_backward, block_forward, rel_err
+
+pytestmark = pytest.mark.gpu
+
+LAMBDAS = dict(resid_lambda=1.1 ** 0.5, post_lambda=0.8, eps=2.0 ** -7)
+
+
+@pytest.fixture
+def tile_policy(request):
+    m.mlp_set_tile_policy(request.param)
+    yield request.param
+    m.mlp_set_tile_policy(0)
+
+
+def _run(t, M, H, I, act, gm, dm, fuse, inplace=False):
+    d = {k: (v.cuda() if v is not None else None) for k, v in t.items()}
+    gated = act in m.GATED_ACTS
+    prob = m.problem(M, H, I, act, gm, dm)
+    blk = m.block(**LAMBDAS)
+    bf = torch.bfloat16
+    G = torch.empty(M, I, dtype=bf, device="cuda")
+    U = torch.empty(M, I, dtype=bf, device="cuda") if gated else None
+    x_in = d["x"].clone() if inplace else d["x"]
+    y = x_in if inplace else torch.full((M, H), float("nan"), dtype=bf, device="cuda")
+    rstd, _ = m.mlp_block_fwd(prob, blk, x_in, d["Wg"], d["Wu"], d["Wd"], y, G, U)
+    res = {"y": y.clone(), "rstd": rstd.clone()}
+    wdt = torch.float32 if fuse else bf
+    dx = torch.full((M, H), float("nan"), dtype=bf, device="cuda")
+    dW = {}
+    for k, shp in (("dWg", (I, H)), ("dWu", (I, H)), ("dWd", (H, I))):
+        if k == "dWu" and not gated:
+            dW[k] = None
+            continue
+        dW[k] = (d[k + "_prev"].clone() if fuse else torch.full(shp, float("nan"), dtype=bf,
+                                                                  device="cuda"))
+    ws = m.mlp_block_bwd(prob, blk, d["dout"], d["x"], d["Wg"], d["Wu"], d["Wd"], G, U, rstd,
+                         dx, dW["dWg"], dW["dWu"], dW["dWd"], fuse_grad_accum=fuse)
+    torch.cuda.synchronize()
+    assert m.mlp_device_status(ws) == 0
+    res.update({"dx": dx, **{k: v for k, v in dW.items() if v is not None}})
+    return res
+
+
+def _oracle(t, act, gm, dm, fuse):
+    a = {k: to_f64(v) if v is not None else None for k, v in t.items()}
+    fw = block_forward(a["x"], a["Wg"], a["Wu"], a["Wd"], act, gm, dm, **LAMBDAS)
+    prev = ({"dWg": a["dWg_prev"], "dWu": a.get("dWu_prev"), "dWd": a["dWd_prev"]}
+            if fuse else None)
+    bw = block_backward(a["dout"], a["x"], a["Wg"], a["Wu"], a["Wd"], act, gm, dm, **LAMBDAS,
+                        dW_prev=prev)
+    return {"y": fw["y"], "rstd": fw["rstd"], **bw}
+
+
+def _compare(got, ref, fuse, M):
+    errs = {}
+    for k, v in got.items():
+        if ref.get(k) is None:
+            continue
+        g = to_f64(v)
+        assert np.all(np.isfinite(g)), k
+        errs[k] = rel_err(g, ref[k])
+    for k, e in errs.items():
+        if k == "rstd":
+            tol = 1e-5  # fp32 sum of squares of bf16 inputs
+        elif fuse and k.startswith("dW"):
+            tol = TOL_F32 if M >= F32_TOL_MIN_TOKENS else TOL_F32_SMALL
+        else:
+            tol = TOL_BF16
+        assert e <= tol, f"{k}: rel err {e:.3e} > {tol} (all: {errs})"
+    return errs
+
+
+@pytest.mark.parametrize("tile_policy", [1, 2], indirect=True)
+@pytest.mark.parametrize("act,gm,dm", [("relu_sq", 1.0, 1.0), ("swiglu", 1.125, 2.0),
+                                       ("gelu_tanh_approx", 0.75, 1.5)])
+@pytest.mark.parametrize("M,H,I", [(64, 128, 352), (300, 200, 392), (520, 1032, 776)])
+@pytest.mark.parametrize("fuse", [False, True])
+def test_block_parity(act, gm, dm, M, H, I, fuse, tile_policy):
+    t = make_inputs(M, H, I, act, seed=41, dW_prev=fuse)
+    got = _run(t, M, H, I, act, gm, dm, fuse)
+    _compare(got, _oracle(t, act, gm, dm, fuse), fuse, M)
+
+
+@pytest.mark.parametrize("act", ["relu_sq", "swiglu"])
+@pytest.mark.parametrize("M", [16, 100])
+def test_block_decode_sized_split_k(act, M):
+    # few tokens: the down projection and dx split K; the residual add moves
+    # into the fp32 -> bf16 pass, the norm's projection into its own kernel
+    H, I = 512, 2048
+    t = make_inputs(M, H, I, act, seed=42)
+    got = _run(t, M, H, I, act, 1.0, 1.0, False)
+    _compare(got, _oracle(t, act, 1.0, 1.0, False), False, M)
+
+
+def test_block_output_over_its_input():
+    # y may be x itself: each residual element is read before its tile of y
+    # is stored
+    M, H, I, act = 300, 264, 392, "relu_sq"
+    t = make_inputs(M, H, I, act, seed=43)
+    got = _run(t, M, H, I, act, 1.0, 1.0, False, inplace=True)
+    ref = _oracle(t, act, 1.0, 1.0, False)
+    assert rel_err(to_f64(got["y"]), ref["y"]) <= TOL_BF16
