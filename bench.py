@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-trace", action="store_true")
+    ap.add_argument("--block", action="store_true",
+                    help="also time the MLP block with its fused RMS norm and residual add")
     ap.add_argument("--sweep-m", action="store_true",
                     help="also time the inference forward at decode-sized token counts")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -453,6 +455,7 @@ def run_ours(args, rank, world, local_rank):
         infer = {"ms": im, "tflops": flops_of(w, "infer") / (im * 1e-3) / 1e12}
 
     sweep = infer_m_sweep(m, w, g, dev, flush, peaks) if args.sweep_m else None
+    block = block_step(m, w, g, dev, flush, K) if args.block else None
 
     peak = float(peaks["bf16_tflops"])
     res = {
@@ -475,7 +478,7 @@ def run_ours(args, rank, world, local_rank):
                       "executed_flops_per_step": f_step, "kernels": kernels,
                       "kernels_timing": f"separate traced pass of {k_tr} L2-flushed steps, "
                                         "kernels serialised (no side stream, no PDL overlap)",
-                      "infer": infer, "infer_m_sweep": sweep},
+                      "infer": infer, "infer_m_sweep": sweep, "block": block},
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": (len(recs) // k_tr) * K if trace else None,
@@ -484,6 +487,58 @@ def run_ours(args, rank, world, local_rank):
         "wall_s_timed_region": wall,
     }
     return res, w
+
+
+def block_step(m, w, g, dev, flush, K):
+    """fwd + bwd of the MLP block with its neighbours (RMS-normalised input,
+    scaled residual add; saved preacts, bf16 weight gradients) against the
+    plain MLP's fwd + bwd on the same inputs, L2 flushed before each step."""
+    import torch
+    bf = torch.bfloat16
+    M, H, I = w.M, w.H, w.I
+    prob = m.problem(M, H, I, w.act, w.gate_mult, w.down_mult)
+    blk = m.block(1.1 ** 0.5, 0.8, 2.0 ** -7)
+    G = torch.empty(M, I, dtype=bf, device=dev)
+    U = torch.empty(M, I, dtype=bf, device=dev) if w.gated else None
+    y = torch.empty(M, H, dtype=bf, device=dev)
+    dx = torch.empty(M, H, dtype=bf, device=dev)
+    dWg = torch.empty(I, H, dtype=bf, device=dev)
+    dWu = torch.empty(I, H, dtype=bf, device=dev) if w.gated else None
+    dWd = torch.empty(H, I, dtype=bf, device=dev)
+    rstd = torch.empty(M, dtype=torch.float32, device=dev)
+    wsf = m.alloc_workspace(prob, m.MODE_FWD, dev)
+    wsb = m.alloc_workspace(prob, m.MODE_BWD, dev)
+
+    def plain():
+        m.mlp_fwd(prob, g["x"], g["Wg"], g["Wu"], g["Wd"], y, G, U, ws=wsf)
+        m.mlp_bwd(prob, g["dout"], g["x"], g["Wg"], g["Wu"], g["Wd"], G, U, dx, dWg, dWu, dWd,
+                  ws=wsb)
+
+    def blk_step():
+        m.mlp_block_fwd(prob, blk, g["x"], g["Wg"], g["Wu"], g["Wd"], y, G, U, rstd, ws=wsf)
+        m.mlp_block_bwd(prob, blk, g["dout"], g["x"], g["Wg"], g["Wu"], g["Wd"], G, U, rstd, dx,
+                        dWg, dWu, dWd, ws=wsb)
+
+    res = {}
+    for name, fn in (("plain_ms", plain), ("block_ms", blk_step)):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(max(5, min(K, 30))):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        res[name] = sorted(ts)[len(ts) // 2]
+    f = flops_of(w, "fwd") + flops_of(w, "bwd")
+    res["block_tflops"] = f / (res["block_ms"] * 1e-3) / 1e12
+    res["overhead"] = res["block_ms"] / res["plain_ms"] - 1.0
+    res["lambdas"] = {"resid_lambda": 1.1 ** 0.5, "post_lambda": 0.8, "eps": 2.0 ** -7}
+    return res
 
 
 def infer_m_sweep(m, w, g, dev, flush, peaks):
