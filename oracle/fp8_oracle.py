@@ -1,0 +1,71 @@
+"""Plain fp64 CPU oracle of the FP8 forward of the ReLU^2 MLP.
+
+TEST INFRASTRUCTURE ONLY: the same rules as ``oracle.mlp_oracle`` (only
+tests, ``__graft_entry__.smoke()`` and ``bench.py`` may use it; it shares no
+code with the library).
+
+What is computed, and where the pages define it
+-----------------------------------------------
+modded-nanogpt ``track_1_short/model/gpt.py`` trains its ReLU^2 MLP in FP8
+(the constants block above ``ReLUSqrdMLP`` and the ``_mlp_*`` buffers):
+e4m3 operands with dequant scales (a value is its code times the scale):
+* the input: static scale ``FP8_MLP_X_SCALE = 2^-4`` (its comment: post-norm
+  rows stay below 448 * 2^-4);
+* each weight matrix: ``amax / 448`` (``_quantize_mlp_weights_and_scales``,
+  the exact branch);
+* the GEMM dequant ``up_scales * x_scale`` (``_mlp_up_dequant``);
+* the ReLU^2 output: a delayed scale, the last step's amax times
+  ``FP8_POST_HEADROOM = 1.03`` over 448, with the kernels recording the new
+  amax by atomic max (``_mlp_post_scales``, ``_mlp_post_amax``,
+  ``_refresh_delayed_scale``);
+* the down projection dequantised by the post scale times the down weight's
+  scale.
+Readings where the page is silent (the kernels are not on it):
+* quantisation is q = e4m3(v * inv), inv = fp32(1 / scale) computed in fp32,
+  v * inv in fp32, then rounded to nearest even on the e4m3 grid with
+  saturation at +-448 (e4m3fn has no infinity);
+* the multipliers: ``gate_mult`` scales the ReLU^2 output before it is
+  quantised, ``down_mult`` the dequantised output (both 1 on the page).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0
+
+
+def e4m3(v):
+    """Round to the e4m3fn grid (1 sign, 4 exponent bits with bias 7, 3
+    mantissa bits; subnormals below 2^-6; no infinity), nearest even,
+    saturating at +-448."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))   # a = m 2^ex, m in [0.5, 1)
+    e = np.maximum(ex - 1, -6)                   # binade, clamped to the subnormal one
+    ulp = np.ldexp(1.0, e - 3)                   # 3 mantissa bits
+    r = np.round(a / ulp) * ulp                  # np.round: half to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.where(a > 0, np.sign(v) * r, 0.0 * v)
+
+
+def quantize(v, scale):
+    """Codes (as float64 values) of v with dequant scale `scale`: the fp32
+    product v * fp32(1/scale), rounded to e4m3."""
+    inv = np.float32(1.0) / np.float32(scale)
+    return e4m3((np.asarray(v, dtype=np.float32) * inv).astype(np.float64))
+
+
+def weight_scale(W):
+    """Exact weight scale amax / 448 (the page computes it in the weights' bf16)."""
+    return max(float(np.max(np.abs(W))), 1e-12) / E4M3_MAX
+
+
+def fp8_relu_sq_forward(x8, W1_8, W2_8, sx, s1, s2, s_post, gate_mult=1.0, down_mult=1.0):
+    """The forward on e4m3 codes: pre = (x8 W1_8^T) sx s1,
+    a = gate_mult relu(pre)^2, a8 = quantize(a, s_post),
+    out = down_mult (a8 W2_8^T) s_post s2.  Returns out, a, a8 and amax(a)."""
+    pre = (x8 @ W1_8.T) * (sx * s1)
+    a = gate_mult * np.maximum(pre, 0.0) ** 2
+    a8 = quantize(a, s_post)
+    out = down_mult * (a8 @ W2_8.T) * (s_post * s2)
+    return {"out": out, "a": a, "a8": a8, "amax_a": float(np.max(a)) if a.size else 0.0}
