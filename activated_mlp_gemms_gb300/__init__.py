@@ -23,7 +23,8 @@ __all__ = [
     "mlp_bwd", "mlp_bwd_recompute", "mlp_status_string", "mlp_device_status", "mlp_version",
     "MODE_FWD", "MODE_INFER", "MODE_BWD", "MODE_BWD_RECOMPUTE", "mlp_trace_enable",
     "mlp_trace_read", "mlp_kernel_name", "mlp_set_tile_policy", "mlp_fwd_infer_noalloc",
-    "Block", "block", "mlp_block_fwd", "mlp_block_bwd",
+    "Block", "block", "mlp_block_fwd", "mlp_block_bwd", "mlp_fp8_quantize", "mlp_fp8_fwd",
+    "MODE_FP8_FWD",
     "NOALLOC_SCRATCH_BYTES", "mlp_set_wait_timeout_ms", "mlp_debug_set_flags", "DEBUG_NO_WORK",
 ]
 
@@ -33,7 +34,7 @@ LIB_PATH = os.path.join(_HERE, "libmlp.so")
 ACTS = {"swiglu": 0, "relu_sq": 1, "gelu_tanh_approx": 2, "relu": 3, "reglu": 4, "geglu": 5,
         "glu": 6}
 GATED_ACTS = ("swiglu", "reglu", "geglu", "glu")
-MODE_FWD, MODE_INFER, MODE_BWD, MODE_BWD_RECOMPUTE = 0, 1, 2, 3
+MODE_FWD, MODE_INFER, MODE_BWD, MODE_BWD_RECOMPUTE, MODE_FP8_FWD = 0, 1, 2, 3, 4
 NOALLOC_SCRATCH_BYTES = 16 << 20  # MLP_NOALLOC_SCRATCH_BYTES
 DEBUG_NO_WORK = 1  # MLP_DEBUG_NO_WORK
 
@@ -81,6 +82,10 @@ def lib():
     L.mlp_bwd.restype = ctypes.c_int
     L.mlp_bwd_recompute.argtypes = [P] + [_VP] * 9 + [ctypes.c_int, _VP, ctypes.c_size_t, _VP]
     L.mlp_bwd_recompute.restype = ctypes.c_int
+    L.mlp_fp8_quantize.argtypes = [_VP, ctypes.c_longlong, _VP, _VP, _VP, _VP]
+    L.mlp_fp8_quantize.restype = ctypes.c_int
+    L.mlp_fp8_fwd.argtypes = [P] + [_VP] * 7 + [_VP, ctypes.c_size_t, _VP]
+    L.mlp_fp8_fwd.restype = ctypes.c_int
     B = ctypes.POINTER(Block)
     L.mlp_block_fwd.argtypes = [P, B] + [_VP] * 8 + [_VP, ctypes.c_size_t, _VP]
     L.mlp_block_fwd.restype = ctypes.c_int
@@ -258,6 +263,35 @@ def mlp_block_bwd(prob: Problem, blk: Block, dy, x, Wg, Wu, Wd, G, U, rstd, dx=N
                              int(bool(fuse_grad_accum)), ws.data_ptr(), ws.numel(),
                              _stream(stream))
     _check(rc, "mlp_block_bwd")
+    return ws
+
+
+def _u8(t, name):
+    if t is None:
+        return None
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()
+            and t.dtype in (torch.uint8, torch.float8_e4m3fn)):
+        raise ValueError(f"{name} must be a contiguous CUDA uint8 / float8_e4m3fn tensor")
+    return t.data_ptr()
+
+
+def mlp_fp8_quantize(src, scale, dst, amax=None, stream=None):
+    """dst (e4m3 codes) = e4m3(src * (1 / scale[0])); max|src| atomically into amax[0]."""
+    rc = lib().mlp_fp8_quantize(_ptr(src, name="src"), src.numel(),
+                                _ptr(scale, torch.float32, "scale"), _u8(dst, "dst"),
+                                _ptr(amax, torch.float32, "amax"), _stream(stream))
+    _check(rc, "mlp_fp8_quantize")
+
+
+def mlp_fp8_fwd(prob: Problem, x8, W1_8, W2_8, scales, out, a8_save=None, amax_a=None, ws=None,
+                stream=None):
+    """e4m3 forward of the ReLU^2 MLP; scales = fp32 [4] device tensor {sx, s1, s2, s_post}."""
+    ws = _ws(ws, prob, MODE_FP8_FWD, out.device)
+    rc = lib().mlp_fp8_fwd(ctypes.byref(prob), _u8(x8, "x8"), _u8(W1_8, "W1_8"), _u8(W2_8, "W2_8"),
+                           _ptr(scales, torch.float32, "scales"), _ptr(out, name="out"),
+                           _u8(a8_save, "a8_save"), _ptr(amax_a, torch.float32, "amax_a"),
+                           ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(rc, "mlp_fp8_fwd")
     return ws
 
 

@@ -72,7 +72,9 @@ struct EpiTraits {
                               : (EPI == EPI_ACT_FWD || EPI == EPI_DACT ||
                                  EPI == EPI_DACT_RECOMP)                  ? 2
                                                                           : 1;
-  static constexpr int OUT_BYTES = (EPI == EPI_ACCUM_F32) ? 4096 : 2048;
+  // bytes of a 32 x 32 output box: fp32 4096, bf16 2048, e4m3 1024
+  static constexpr int OUT_BYTES = (EPI == EPI_ACCUM_F32) ? 4096 : (EPI == EPI_ACT_FWD_F8) ? 1024
+                                                                                            : 2048;
   static constexpr bool DACT = (EPI == EPI_DGATED || EPI == EPI_DACT);
   // staged boxes per warp: at most two (a third output reuses the first box
   // once that box's store has read it), so the stage ring keeps 6 stages
@@ -132,6 +134,8 @@ struct EpiUnit {
   const void* in1;
   const float* rstd;          // per-row scale (nullptr: none)
   float alpha;                // residual scale
+  const float* scl;           // e4m3 dequant scales {sx, s1, s2, s_post}
+  float* amax;                // running max of the e4m3 epilogue's a
 };
 
 __device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P) {
@@ -145,6 +149,8 @@ __device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P) {
   U.in1 = P.in1;
   U.rstd = P.rstd;
   U.alpha = P.alpha;
+  U.scl = P.scl;
+  U.amax = P.amax;
   return U;
 }
 
@@ -425,6 +431,55 @@ __device__ __forceinline__ void epi_recomp_dh(const Params& p, const EpiUnit& P,
   }
 }
 
+// e4m3 forward of the ReLU^2 MLP: pre = acc * sx * s1, a = s * relu(pre)^2,
+// a -> e4m3(a * fp32(1 / s_post)) through a 32 x 32-byte box (map 0); the
+// largest a of the warp's rows goes to *amax (atomic max on the bits of a
+// non-negative float).
+template <int ACT>
+__device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, const EpiWarp& e,
+                                           uint32_t tb, int col0, int cb, int ce) {
+  const float deq = P.scl[0] * P.scl[1];
+  const float inv = 1.0f / P.scl[3];
+  const float s = p.scale;
+  const bool row_ok = e.row0 + e.lane < P.M;
+  float mx = 0.f;
+#pragma unroll 1
+  for (int c = cb; c < ce; c += 32) {
+    const int col = col0 + c;
+    if (col >= P.N) break;
+    uint32_t z[32];
+    __syncwarp();
+    tmem_ld32(tb + c, z);
+    tmem_wait_ld();
+    uint32_t q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int k = 4 * j + 2 * h;
+        const float p0 = fmaxf(__uint_as_float(z[k]) * deq, 0.f);
+        const float p1 = fmaxf(__uint_as_float(z[k + 1]) * deq, 0.f);
+        const float a0 = s * p0 * p0, a1 = s * p1 * p1;
+        mx = fmaxf(mx, fmaxf(a0, a1));
+        w |= static_cast<uint32_t>(pack_e4m3x2(a0 * inv, a1 * inv)) << (16 * h);
+      }
+      q[j] = w;
+    }
+    staging_acquire(e);
+    const uint32_t rb = e.stg + static_cast<uint32_t>(e.lane) * 32u;
+    st_shared_v4(rb, q[0], q[1], q[2], q[3]);
+    st_shared_v4(rb + 16, q[4], q[5], q[6], q[7]);
+    flush_chunk<1, 1024, false>(p, P, e, col);
+  }
+  if (P.amax) {
+    if (!row_ok) mx = 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (e.lane == 0 && mx > 0.f) atomicMax(reinterpret_cast<int*>(P.amax), __float_as_int(mx));
+  }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epi_plain(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                           uint32_t tb, int col0, int cb, int ce) {
@@ -437,7 +492,15 @@ __device__ __forceinline__ void epi_plain(const Params& p, const EpiUnit& P, con
     tmem_ld32(tb + c, d);
     tmem_wait_ld();
     staging_acquire(e);
-    if constexpr (EPI == EPI_STORE_BF16) {
+    if constexpr (EPI == EPI_STORE_BF16_F8) {
+      const float deq = p.scale * P.scl[3] * P.scl[2];
+      uint32_t q[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        q[j] = pack_bf16x2(deq * __uint_as_float(d[2 * j]), deq * __uint_as_float(d[2 * j + 1]));
+      stage_bf16(e.stg, e.lane, q);
+      flush_chunk<1, 2048, false>(p, P, e, col);
+    } else if constexpr (EPI == EPI_STORE_BF16) {
       uint32_t q[16];
       if (P.in0) {
         // the block's residual add: D = alpha * residual + acc
@@ -572,7 +635,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
   using C = Cfg<EPI, CG>;
   constexpr bool PAIR = CG == 2;
   constexpr int TILE_N = EpiTraits<EPI>::TILE_N;
-  constexpr uint32_t IDESC = idesc_bf16(C::TILE_M, MMA_N, A_MN, B_MN);
+  // e4m3 operands: a 128-byte k-block row holds 128 elements (bf16: 64)
+  constexpr bool F8 = EPI == EPI_ACT_FWD_F8 || EPI == EPI_STORE_BF16_F8;
+  constexpr int KE = F8 ? 2 * BK : BK;
+  constexpr uint32_t IDESC = F8 ? idesc_e4m3(C::TILE_M, MMA_N) : idesc_bf16(C::TILE_M, MMA_N, A_MN, B_MN);
   constexpr uint32_t IDESC_BMN = idesc_bf16(C::TILE_M, MMA_N, A_MN, true);
 
   // 1024-byte aligned stage ring (the 128-byte swizzle repeats every 1 KB)
@@ -683,7 +749,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
             // (the A boxes of an output with few rows cover only those rows)
             mbar_expect_tx(full, tx_bytes);
             const int seg = kb < L.kb0 ? 0 : 1;
-            const int kc = (seg == 0 ? kb : kb - L.kb0) * BK;
+            const int kc = (seg == 0 ? kb : kb - L.kb0) * KE;
             const uint32_t sA = base_s + stage * C::STAGE;
             load_stage<EPI, A_MN, B_MN, CG>(L, seg, kc, sA, sA + C::A_BYTES, full, pol);
             ++issued;
@@ -709,7 +775,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
               break;
             }
             const int seg = kb < L.kb0 ? 0 : 1;
-            const int kc = (seg == 0 ? kb : kb - L.kb0) * BK;
+            const int kc = (seg == 0 ? kb : kb - L.kb0) * KE;
             const uint32_t sA = base_s + stage * C::STAGE;
             load_stage<EPI, A_MN, B_MN, CG>(L, seg, kc, sA, sA + C::A_BYTES,
                                             full_lead + 8u * stage, pol);
@@ -787,8 +853,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
                                      : sdesc_sw128(sB + k * 32, 16, 1024);
             const uint32_t idesc = b_mn ? IDESC_BMN : IDESC;
             const uint32_t accum = (kb > kfirst || k > 0) ? 1u : 0u;
-            if constexpr (PAIR) tc_mma_bf16_pair(d, ad, bd, idesc, accum);
-            else tc_mma_bf16(d, ad, bd, idesc, accum);
+            if constexpr (F8) {
+              if constexpr (PAIR) tc_mma_f8_pair(d, ad, bd, idesc, accum);
+              else tc_mma_f8(d, ad, bd, idesc, accum);
+            } else {
+              if constexpr (PAIR) tc_mma_bf16_pair(d, ad, bd, idesc, accum);
+              else tc_mma_bf16(d, ad, bd, idesc, accum);
+            }
           }
           any = true;
           if constexpr (PAIR) tc_commit_pair(bar_s(EMPTY + stage), 3);
@@ -886,6 +957,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
           epi_dact<ACT, false>(p, P, e, tb, col0, cb, ce, pg, pu);
         } else if constexpr (EPI == EPI_DACT_RECOMP) {
           epi_recomp_dh(p, P, e, tb, col0, cb, dd);
+        } else if constexpr (EPI == EPI_ACT_FWD_F8) {
+          epi_act_f8<ACT>(p, P, e, tb, col0, cb, ce);
         } else {
           epi_plain<EPI>(p, P, e, tb, col0, cb, ce);
         }

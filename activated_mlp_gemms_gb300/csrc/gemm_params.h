@@ -30,7 +30,10 @@ enum Epi : int {
   // non-gated backward with the preact recomputed in the same tile:
   // segment 0 acc = p = x W1^T (accumulator 0), segment 1 acc = dh = dout Wd
   // (accumulator 1): a = s*act(p), dP = s*dh*act'(p)
-  EPI_DACT_RECOMP = 6
+  EPI_DACT_RECOMP = 6,
+  // e4m3 operands (tcgen05 kind::f8f6f4), dequant scales scl = {sx, s1, s2, s_post}:
+  EPI_ACT_FWD_F8 = 7,    // a = s*relu(acc*sx*s1)^2 -> e4m3(a / s_post) (map 0), amax(a) -> *amax
+  EPI_STORE_BF16_F8 = 8  // D = bf16(s * acc * s_post * s2)
 };
 
 // The function applied to the gate (gated MLPs) or to the preact (non-gated).
@@ -58,6 +61,8 @@ struct Prob {
                           // dG, dU / dP (derivative epilogues) are multiplied by rstd[row]
   float alpha;            // EPI_STORE_BF16 with in0 = residual [M, ld]: D = alpha*in0 + acc
   int pad_b;
+  const float* scl;       // e4m3 epilogues: the dequant scales {sx, s1, s2, s_post}
+  float* amax;            // EPI_ACT_FWD_F8: running max of a (atomic; may be null)
 };
 
 struct Params {  // 64-byte aligned through CUtensorMap
@@ -96,6 +101,11 @@ cudaError_t launch_postact(const void* G, const void* U, void* a, long long n, i
 // `resid` (bf16, n elements) the result is src + alpha * resid.
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, long long n, cudaStream_t stream,
                                bool pdl, const void* resid = nullptr, float alpha = 0.f);
+
+// e4m3 codes q = e4m3(fp32(src * fp32(1 / *scale))) of n bf16 values (saturating,
+// round to nearest even); with `amax`, atomic max of |src| into *amax.
+cudaError_t launch_quant_e4m3(const void* src, long long n, const float* scale, void* dst,
+                              float* amax, cudaStream_t stream, bool pdl);
 
 // Per-token RMS-norm scale rstd[m] = 1 / sqrt(mean_h x^2 + eps), x bf16 [M, H].
 cudaError_t launch_rstd(const void* x, float* rstd, int M, int H, float eps, cudaStream_t stream,

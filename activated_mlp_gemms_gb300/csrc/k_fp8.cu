@@ -1,0 +1,69 @@
+// e4m3 (FP8) kernels of the ReLU^2 MLP forward: the quantisation of bf16
+// tensors to e4m3 codes with a dequant scale (and their amax), and the two
+// GEMM instances: fc1 with the ReLU^2 epilogue that re-quantises its output,
+// and the down projection with a dequantising bf16 store.
+#include "gemm.cuh"
+
+namespace mlpk {
+
+// q = e4m3(fp32(x * fp32(1 / *scale))), saturating, 8 per thread per step
+// (one 16-byte load, one 8-byte store); |x|'s maximum into *amax.
+__global__ void __launch_bounds__(256) k_quant_e4m3(const __nv_bfloat16* __restrict__ src,
+                                                    long long n8, const float* __restrict__ scale,
+                                                    uint8_t* __restrict__ dst, float* amax) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const float inv = 1.0f / *scale;
+  float mx = 0.f;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint4 v = ld_global_v4(src + 8 * i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[2] = {0, 0};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = unpack_bf16x2(w[j]);
+      mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+      o[j >> 1] |= static_cast<uint32_t>(pack_e4m3x2(f.x * inv, f.y * inv)) << (16 * (j & 1));
+    }
+    *reinterpret_cast<uint2*>(dst + 8 * i) = make_uint2(o[0], o[1]);
+  }
+  if (amax) {
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+    if ((threadIdx.x & 31) == 0 && mx > 0.f) atomicMax(reinterpret_cast<int*>(amax), __float_as_int(mx));
+  }
+}
+
+cudaError_t launch_quant_e4m3(const void* src, long long n, const float* scale, void* dst,
+                              float* amax, cudaStream_t stream, bool pdl) {
+  const long long n8 = n / 8;  // n is a multiple of 8
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;
+  if (blocks < 1) blocks = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_quant_e4m3, static_cast<const __nv_bfloat16*>(src), n8, scale,
+                            static_cast<uint8_t*>(dst), amax);
+}
+
+template cudaError_t launch_gemm<EPI_ACT_FWD_F8, false, false, 1, ACT_RELU_SQ>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_ACT_FWD_F8, false, false, 1, ACT_RELU_SQ>();
+template cudaError_t launch_gemm<EPI_ACT_FWD_F8, false, false, 2, ACT_RELU_SQ>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_ACT_FWD_F8, false, false, 2, ACT_RELU_SQ>();
+template cudaError_t launch_gemm<EPI_STORE_BF16_F8, false, false, 1, 0>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_STORE_BF16_F8, false, false, 1, 0>();
+template cudaError_t launch_gemm<EPI_STORE_BF16_F8, false, false, 2, 0>(const Params&, int, cudaStream_t, bool);
+template int max_groups<EPI_STORE_BF16_F8, false, false, 2, 0>();
+
+}  // namespace mlpk

@@ -87,10 +87,11 @@ std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
 // zero and are not written.  bf16 operands use the 128-byte swizzle; the
 // epilogue's 32 x 32 output boxes use the 64-byte (bf16) or 128-byte (fp32)
 // swizzle of the staging buffers.
+// dtype: 0 bf16, 1 fp32, 2 e4m3 bytes (uint8).
 bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch,
-              uint32_t box0, uint32_t box1, bool f32 = false,
+              uint32_t box0, uint32_t box1, int dtype = 0,
               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
-  MapKey key{ptr, inner, outer, pitch, box0, box1, f32 ? 1 : 0, static_cast<int>(swz)};
+  MapKey key{ptr, inner, outer, pitch, box0, box1, dtype, static_cast<int>(swz)};
   {
     std::lock_guard<std::mutex> lk(g_map_mu);
     auto it = g_map_cache.find(key);
@@ -100,14 +101,16 @@ bool make_map(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
     }
   }
   if (!encode_fn_ok()) return false;
-  const uint64_t esize = f32 ? 4 : 2;
+  const uint64_t esize = dtype == 1 ? 4 : (dtype == 2 ? 1 : 2);
+  const CUtensorMapDataType dt = dtype == 1   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dtype == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {pitch * esize};
   cuuint32_t box[2] = {box0, box1};
   cuuint32_t estr[2] = {1, 1};
   CUtensorMap m;
-  CUresult r = g_encode(&m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                        2, const_cast<void*>(ptr), dims, strides, box, estr,
+  CUresult r = g_encode(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
@@ -208,6 +211,26 @@ struct Gemm {
     if (!make_map(&p.maps[nmaps], ptr, MN, K, MN, 64, BK)) ok = false;
     return nmaps++;
   }
+  // e4m3 operands [rows, K] (K bytes per row), boxes {128 k, box_rows}; the
+  // A operand's boxes are row-sized below 128 rows, as in kmajor_a.
+  int kmajor_u8(const void* ptr, int rows, int K, int box_rows) {
+    if (nmaps >= MAX_MAPS) { ok = false; return 0; }
+    if (!make_map(&p.maps[nmaps], ptr, K, rows, K, 2 * BK, box_rows, 2)) ok = false;
+    return nmaps++;
+  }
+  int kmajor_a_u8(const void* ptr, int rows, int K) {
+    const int box = rows < BM ? ((rows + 15) / 16) * 16 : BM;
+    p.a_tx_bytes = box * BK * 2;  // 128 bytes per row, as for bf16
+    return kmajor_u8(ptr, rows, K, box);
+  }
+  // e4m3 epilogue output [rows, cols], 32 x 32-byte boxes, no swizzle.
+  int output_u8(void* ptr, int rows, int cols) {
+    if (!ptr) return -1;
+    if (nmaps >= MAX_MAPS) { ok = false; return -1; }
+    if (!make_map(&p.maps[nmaps], ptr, cols, rows, cols, 32, 32, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
+      ok = false;
+    return nmaps++;
+  }
   // Epilogue output [rows, cols] (row pitch cols), stored in 32 x 32 boxes;
   // -1 when the output is not requested.
   int output(void* ptr, int rows, int cols, bool f32 = false) {
@@ -218,12 +241,13 @@ struct Gemm {
       ok = false;
     return nmaps++;
   }
-  Prob& add(int M, int N, int K0, int K1, int tile_n, int ksplit = 1) {
+  // ke: K elements per k-block (bf16 64, e4m3 128: a 128-byte row either way)
+  Prob& add(int M, int N, int K0, int K1, int tile_n, int ksplit = 1, int ke = BK) {
     Prob& P = p.prob[p.nprob++];
     P.M = M;
     P.N = N;
-    P.kb0 = (K0 + BK - 1) / BK;
-    P.kb1 = (K1 + BK - 1) / BK;
+    P.kb0 = (K0 + ke - 1) / ke;
+    P.kb1 = (K1 + ke - 1) / ke;
     P.tiles_m = (M + BM * cg - 1) / (BM * cg);
     P.tiles_n = (N + tile_n - 1) / tile_n;
     const int kbt = P.kb0 + P.kb1;
@@ -434,6 +458,8 @@ size_t split_bytes(const mlp_problem_t* p, int mode) {
 }
 
 size_t ws_size(const mlp_problem_t* p, int mode) {
+  // e4m3 forward: the control block + the e4m3 postact (one byte per element)
+  if (mode == MLP_MODE_FP8_FWD) return CTRL_BYTES + round256((size_t)p->M * p->I);
   size_t n = CTRL_BYTES + inter_bytes(p);  // control block + postact a
   if (mode == MLP_MODE_BWD_RECOMPUTE) n += inter_bytes(p) * (gated(p) ? 2 : 1);
   return n + split_bytes(p, mode);  // + the fp32 partial-sum region (small M only)
@@ -811,7 +837,7 @@ extern "C" {
 
 size_t mlp_workspace_size(const mlp_problem_t* p, int mode) {
   if (check_problem(p) != MLP_OK) return 0;
-  if (mode < MLP_MODE_FWD || mode > MLP_MODE_BWD_RECOMPUTE) return 0;
+  if (mode < MLP_MODE_FWD || mode > MLP_MODE_FP8_FWD) return 0;
   return ws_size(p, mode);
 }
 
@@ -852,6 +878,64 @@ int mlp_block_bwd(const mlp_problem_t* p, const mlp_block_t* b, const void* dy, 
   const Block blk{b->resid_lambda, b->eps, nullptr, rstd};
   return backward(&q, dy, x, Wg, Wu, Wd, G, U, dx, dWg, dWu, dWd, fuse_grad_accum, ws, ws_bytes,
                   stream, false, &blk);
+}
+
+int mlp_fp8_quantize(const void* src, long long n, const float* scale, void* dst, float* amax,
+                     void* stream) {
+  if (n < 0 || (n % 8) != 0) return MLP_ERR_INVALID_ARG;
+  if (n == 0) return MLP_OK;
+  MLP_TRY(need(src));
+  MLP_TRY(need(dst));
+  if (!scale) return MLP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return traced(MLP_KERNEL_QUANT, s,
+                [&] { return launch_quant_e4m3(src, n, scale, dst, amax, s, false); });
+}
+
+int mlp_fp8_fwd(const mlp_problem_t* p, const void* x8, const void* W1_8, const void* W2_8,
+                const float* scales, void* out, void* a8_save, float* amax_a, void* ws,
+                size_t ws_bytes, void* stream) {
+  MLP_TRY(check_problem(p));
+  if (p->act != MLP_ACT_RELU_SQ) return MLP_ERR_UNSUPPORTED;
+  if (p->H % 16 || p->I % 16) return MLP_ERR_ALIGNMENT;  // 16-byte e4m3 rows
+  MLP_TRY(need(x8));
+  MLP_TRY(need(W1_8));
+  MLP_TRY(need(W2_8));
+  MLP_TRY(need(out));
+  MLP_TRY(opt(a8_save));
+  if (!scales) return MLP_ERR_INVALID_ARG;
+  MLP_TRY(check_ws(p, MLP_MODE_FP8_FWD, ws, ws_bytes));
+  Call c;
+  MLP_TRY(begin_call(c, ws, stream));
+  void* a8 = a8_save ? a8_save : static_cast<char*>(ws) + CTRL_BYTES;
+  const int M = p->M, H = p->H, I = p->I;
+  {
+    // fc1 on e4m3 codes, ReLU^2, the postact re-quantised with s_post
+    Gemm g(*p, c.counter(), c.status, pick_cg(M));
+    g.p.scale = p->gate_mult;
+    const int mA = g.kmajor_a_u8(x8, M, H);
+    const int mB = g.kmajor_u8(W1_8, I, H, g.b_rows());
+    const int oA = g.output_u8(a8, M, I);
+    Prob& P = g.add(M, I, H, 0, MMA_N, 1, 2 * BK);
+    P.mapA0 = mA;
+    P.mapB0 = mB;
+    P.mapO[0] = oA;
+    P.scl = scales;
+    P.amax = amax_a;
+    MLP_TRY((run_act<EPI_ACT_FWD_F8, false, false, ACT_RELU_SQ>(g, c, MLP_KERNEL_GATE_UP)));
+  }
+  // the down projection on the re-quantised postact, dequantised to bf16
+  Gemm g(*p, c.counter(), c.status, pick_cg(M));
+  g.p.scale = p->down_mult;
+  const int mA = g.kmajor_a_u8(a8, M, I);
+  const int mB = g.kmajor_u8(W2_8, H, I, g.b_rows());
+  const int oO = g.output(out, M, H);
+  Prob& P = g.add(M, H, I, 0, MMA_N, 1, 2 * BK);
+  P.mapA0 = mA;
+  P.mapB0 = mB;
+  P.mapO[0] = oO;
+  P.scl = scales;
+  return run<EPI_STORE_BF16_F8, false, false>(g, c, MLP_KERNEL_DOWN);
 }
 
 int mlp_bwd(const mlp_problem_t* p, const void* dout, const void* x, const void* Wg,
@@ -950,6 +1034,7 @@ const char* mlp_kernel_name(int tag) {
     case MLP_KERNEL_DACT_RECOMPUTE: return "dact_recompute";
     case MLP_KERNEL_RSTD: return "rstd";
     case MLP_KERNEL_RMSNORM_BWD: return "rmsnorm_bwd";
+    case MLP_KERNEL_QUANT: return "quant_e4m3";
     default: return "unknown";
   }
 }

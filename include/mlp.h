@@ -109,7 +109,8 @@ typedef enum {
   MLP_MODE_FWD = 0,
   MLP_MODE_INFER = 1,
   MLP_MODE_BWD = 2,
-  MLP_MODE_BWD_RECOMPUTE = 3
+  MLP_MODE_BWD_RECOMPUTE = 3,
+  MLP_MODE_FP8_FWD = 4   /* mlp_fp8_fwd: the control block + an e4m3 [M,I] postact */
 } mlp_mode_t;
 
 /* Bytes of workspace a call in `mode` needs for problem `p` (0 on invalid
@@ -230,6 +231,39 @@ int mlp_block_bwd(const mlp_problem_t* p, const mlp_block_t* b, const void* dy, 
                   const float* rstd, void* dx, void* dWg, void* dWu, void* dWd,
                   int fuse_grad_accum, void* ws, size_t ws_bytes, void* stream);
 
+/* ---- FP8 (e4m3) forward of the ReLU^2 MLP ----
+ * modded-nanogpt gpt.py trains its ReLU^2 MLP with e4m3 operands and
+ * dequant scales (a value is its e4m3 code times the scale; the constants
+ * block above ReLUSqrdMLP and the _mlp_* buffers): the input's static scale
+ * FP8_MLP_X_SCALE = 2^-4, amax/448 weight scales, and a delayed scale for
+ * the ReLU^2 output (the last step's amax x 1.03 / 448) whose new amax the
+ * kernels record.  The quantisation reading (the kernels are not on the
+ * page): q = e4m3(fp32(v * fp32(1 / scale))), round to nearest even,
+ * saturating at +-448.  This is the forward; the FP8 backward (e5m2
+ * gradients) is not built. */
+
+/* e4m3 codes of n bf16 values (n a multiple of 8; 16-byte aligned src and
+ * dst): dst[i] = e4m3(src[i] * (1 / *scale)); with amax non-NULL, the
+ * largest |src[i]| is atomically max-ed into *amax (which the caller zeroes
+ * when it starts a new maximum).  scale and amax are device fp32 scalars. */
+int mlp_fp8_quantize(const void* src, long long n, const float* scale, void* dst, float* amax,
+                     void* stream);
+
+/* Forward on e4m3 codes (p->act must be MLP_ACT_RELU_SQ, H and I multiples of 16):
+ *   pre = (x8 W1_8^T) * sx * s1,   a = gate_mult * relu(pre)^2,
+ *   a8  = e4m3(a * (1 / s_post)),  *amax_a = max(*amax_a, max a),
+ *   out = down_mult * (a8 W2_8^T) * s_post * s2          (bf16 [M,H])
+ *   x8 [M,H], W1_8 [I,H], W2_8 [H,I]: e4m3 codes (one byte each, row-major)
+ *   scales: device fp32 {sx, s1, s2, s_post}
+ *   a8_save: e4m3 [M,I] out, or NULL (then the workspace holds it)
+ *   amax_a: device fp32 scalar, or NULL
+ * fc1 and the down projection are tcgen05 kind::f8f6f4 GEMMs (fp32
+ * accumulation); the ReLU^2, its re-quantisation and amax run in fc1's
+ * epilogue.  Workspace: mlp_workspace_size(p, MLP_MODE_FP8_FWD). */
+int mlp_fp8_fwd(const mlp_problem_t* p, const void* x8, const void* W1_8, const void* W2_8,
+                const float* scales, void* out, void* a8_save, float* amax_a, void* ws,
+                size_t ws_bytes, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mlp_status_string(int status);
 
@@ -306,7 +340,8 @@ typedef enum {
   MLP_KERNEL_DACT_RECOMPUTE = 7, /* non-gated recompute: x W1^T and dout Wd in one tile,
                                     epilogue postact and dP */
   MLP_KERNEL_RSTD = 8,          /* the block's per-token RMS-norm scale */
-  MLP_KERNEL_RMSNORM_BWD = 9    /* the block's RMS-norm derivative and residual gradient */
+  MLP_KERNEL_RMSNORM_BWD = 9,   /* the block's RMS-norm derivative and residual gradient */
+  MLP_KERNEL_QUANT = 10         /* bf16 -> e4m3 quantisation */
 } mlp_kernel_t;
 
 /* on != 0 starts recording, 0 stops (records already taken are kept). */

@@ -24,7 +24,7 @@ def L():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?[a-z_]+\s*\*?\s*(mlp_[a-z_]+)\s*\(", src, flags=re.M)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_]+\s*\*?\s*(mlp_[a-z0-9_]+)\s*\(", src, flags=re.M)
     return sorted(set(names))
 
 
@@ -35,7 +35,8 @@ def test_header_declares_the_abi():
                             "mlp_version", "mlp_trace_enable", "mlp_trace_read",
                             "mlp_kernel_name", "mlp_set_tile_policy",
                             "mlp_fwd_infer_noalloc", "mlp_set_wait_timeout_ms",
-                            "mlp_debug_set_flags", "mlp_block_fwd", "mlp_block_bwd"])
+                            "mlp_debug_set_flags", "mlp_block_fwd", "mlp_block_bwd",
+                            "mlp_fp8_quantize", "mlp_fp8_fwd"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -133,12 +134,27 @@ def test_block_validation(L):
     assert bwd(FAKE + 256) == -1  # dx aliases dy
 
 
+def test_fp8_validation_and_workspace(L):
+    p = m.problem(2048, 768, 3072, "relu_sq")
+    assert m.mlp_workspace_size(p, m.MODE_FP8_FWD) == 1024 + 2048 * 3072
+    ws = 1 << 40
+    f = lambda prob, scales=FAKE: L.mlp_fp8_fwd(  # noqa: E731
+        ctypes.byref(prob), FAKE, FAKE, FAKE, scales, FAKE, None, None, FAKE, ws, None)
+    assert f(m.problem(64, 128, 352)) == -3            # SwiGLU: unsupported
+    assert f(m.problem(64, 136, 352, "relu_sq")) == -2  # H % 16
+    assert f(p, scales=None) == -1
+    assert L.mlp_fp8_quantize(FAKE, 12, FAKE, FAKE, None, None) == -1   # n % 8
+    assert L.mlp_fp8_quantize(FAKE, 0, FAKE, FAKE, None, None) == 0     # nothing to do
+    assert L.mlp_fp8_quantize(FAKE, 16, None, FAKE, None, None) == -1   # no scale
+
+
 def test_kernel_names_and_empty_trace(L):
     assert m.mlp_kernel_name(2) == "dgated"
     assert m.mlp_kernel_name(6) == "convert"
     assert m.mlp_kernel_name(7) == "dact_recompute"
     assert m.mlp_kernel_name(8) == "rstd"
     assert m.mlp_kernel_name(9) == "rmsnorm_bwd"
+    assert m.mlp_kernel_name(10) == "quant_e4m3"
     assert m.mlp_kernel_name(99) == "unknown"
     assert m.mlp_trace_read() == []  # nothing recorded: no CUDA call is made
 
