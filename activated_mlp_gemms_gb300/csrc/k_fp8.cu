@@ -6,8 +6,22 @@
 
 namespace mlpk {
 
-// q = e4m3(fp32(x * fp32(1 / *scale))), saturating, 8 per thread per step
-// (one 16-byte load, one 8-byte store); |x|'s maximum into *amax.
+// q = e4m3(fp32(x * fp32(1 / *scale))), saturating, 8 values (one 16-byte
+// load, one 8-byte store) per vector; each thread loads four grid-strided
+// vectors before converting them, so that their loads are in flight
+// together.  |x|'s maximum goes to *amax.
+__device__ __forceinline__ uint2 quant8(uint4 v, float inv, float& mx) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[2] = {0, 0};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 f = unpack_bf16x2(w[j]);
+    mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+    o[j >> 1] |= static_cast<uint32_t>(pack_e4m3x2(f.x * inv, f.y * inv)) << (16 * (j & 1));
+  }
+  return make_uint2(o[0], o[1]);
+}
+
 __global__ void __launch_bounds__(256) k_quant_e4m3(const __nv_bfloat16* __restrict__ src,
                                                     long long n8, const float* __restrict__ scale,
                                                     uint8_t* __restrict__ dst, float* amax) {
@@ -15,18 +29,16 @@ __global__ void __launch_bounds__(256) k_quant_e4m3(const __nv_bfloat16* __restr
   pdl_launch_dependents();
   const float inv = 1.0f / *scale;
   float mx = 0.f;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
-       i += (long long)gridDim.x * blockDim.x) {
-    const uint4 v = ld_global_v4(src + 8 * i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[2] = {0, 0};
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += 4 * stride) {
+    uint4 v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = unpack_bf16x2(w[j]);
-      mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
-      o[j >> 1] |= static_cast<uint32_t>(pack_e4m3x2(f.x * inv, f.y * inv)) << (16 * (j & 1));
-    }
-    *reinterpret_cast<uint2*>(dst + 8 * i) = make_uint2(o[0], o[1]);
+    for (int u = 0; u < 4; ++u)
+      v[u] = (i + u * stride < n8) ? ld_global_v4(src + 8 * (i + u * stride)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * stride < n8)
+        *reinterpret_cast<uint2*>(dst + 8 * (i + u * stride)) = quant8(v[u], inv, mx);
   }
   if (amax) {
 #pragma unroll
