@@ -20,10 +20,19 @@ e4m3 operands with dequant scales (a value is its code times the scale):
   ``_refresh_delayed_scale``);
 * the down projection dequantised by the post scale times the down weight's
   scale.
+* the backward: the incoming gradient in e5m2 with the static scale
+  ``FP8_GRAD_SCALE = 2^-6``, the preact gradient in e5m2 with a delayed
+  scale (last step's amax times ``FP8_DPRE_HEADROOM = 1.25`` over 57344,
+  ``_mlp_dpre_scales``, ``_mlp_dpre_amax``), the down projection's backward
+  dequantised by ``down_scales * grad_scale`` (``_mlp_dq_bwd``).
 Readings where the page is silent (the kernels are not on it):
 * quantisation is q = e4m3(v * inv), inv = fp32(1 / scale) computed in fp32,
   v * inv in fp32, then rounded to nearest even on the e4m3 grid with
-  saturation at +-448 (e4m3fn has no infinity);
+  saturation at +-448 (e4m3fn has no infinity); e5m2 likewise, saturating
+  at +-57344;
+* the backward treats the postact's quantisation as the identity (its
+  gradient passes straight through) and takes ReLU^2's derivative from the
+  preact in full precision (the GPU path saves the preact in bf16);
 * the multipliers: ``gate_mult`` scales the ReLU^2 output before it is
   quantised, ``down_mult`` the dequantised output (both 1 on the page).
 """
@@ -32,6 +41,7 @@ from __future__ import annotations
 import numpy as np
 
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
 
 
 def e4m3(v):
@@ -46,6 +56,24 @@ def e4m3(v):
     r = np.round(a / ulp) * ulp                  # np.round: half to even
     r = np.minimum(r, E4M3_MAX)
     return np.where(a > 0, np.sign(v) * r, 0.0 * v)
+
+
+def e5m2(v):
+    """Round to the e5m2 grid (5 exponent bits with bias 15, 2 mantissa bits;
+    subnormals below 2^-14), nearest even, saturating at +-57344."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    e = np.maximum(ex - 1, -14)
+    ulp = np.ldexp(1.0, e - 2)
+    r = np.minimum(np.round(a / ulp) * ulp, E5M2_MAX)
+    return np.where(a > 0, np.sign(v) * r, 0.0 * v)
+
+
+def quantize_e5m2(v, scale):
+    """e5m2 codes of v with dequant scale `scale` (fp32 product with fp32(1/scale))."""
+    inv = np.float32(1.0) / np.float32(scale)
+    return e5m2((np.asarray(v, dtype=np.float32) * inv).astype(np.float64))
 
 
 def quantize(v, scale):
@@ -69,3 +97,22 @@ def fp8_relu_sq_forward(x8, W1_8, W2_8, sx, s1, s2, s_post, gate_mult=1.0, down_
     a8 = quantize(a, s_post)
     out = down_mult * (a8 @ W2_8.T) * (s_post * s2)
     return {"out": out, "a": a, "a8": a8, "amax_a": float(np.max(a)) if a.size else 0.0}
+
+
+def fp8_relu_sq_backward(dout, x8, W1_8, W2_8, a8, sx, s1, s2, s_post, sg, s_dpre,
+                         gate_mult=1.0, down_mult=1.0):
+    """The backward of ``fp8_relu_sq_forward`` on codes:
+    dout8 = e5m2 codes of dout (scale sg); da = down_mult (dout8 W2_8) sg s2;
+    dpre = gate_mult da 2 relu(pre) with pre = (x8 W1_8^T) sx s1;
+    dP8 = e5m2 codes of dpre (scale s_dpre);
+    dx = (dP8 W1_8) s_dpre s1;  dW1 = (dP8^T x8) s_dpre sx;
+    dW2 = down_mult (dout8^T a8) sg s_post.
+    Returns those and amax(|dpre|)."""
+    dout8 = quantize_e5m2(dout, sg)
+    pre = (x8 @ W1_8.T) * (sx * s1)
+    da = down_mult * (dout8 @ W2_8) * (sg * s2)
+    dpre = gate_mult * da * 2.0 * np.maximum(pre, 0.0)
+    dP8 = quantize_e5m2(dpre, s_dpre)
+    return {"dx": (dP8 @ W1_8) * (s_dpre * s1), "dW1": (dP8.T @ x8) * (s_dpre * sx),
+            "dW2": down_mult * (dout8.T @ a8) * (sg * s_post), "dout8": dout8, "dP8": dP8,
+            "dpre": dpre, "amax_dpre": float(np.max(np.abs(dpre))) if dpre.size else 0.0}

@@ -85,3 +85,66 @@ def test_planted_missing_dequant_is_caught():
     good = F8.fp8_relu_sq_forward(x8, W1, W2, 0.25, 0.5, 0.125, 0.125)["out"]
     bad = (F8.e4m3(np.maximum(x8 @ W1.T * 0.25, 0) ** 2 / 0.125) @ W2.T) * 0.125 * 0.125
     assert not np.array_equal(good, bad)
+
+
+def test_e5m2_matches_torch_cast_in_range():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(56)
+    v = np.concatenate([rng.standard_normal(20000) * s for s in (1e-5, 1e-2, 1, 300, 20000)])
+    v = v[np.abs(v) <= 57344]
+    grid = np.array([1.0, 1.25, 1.5, 2.0 ** -14, 2.0 ** -16, 2.0 ** -15])
+    v = np.concatenate([v, (grid[:-1] + grid[1:]) / 2, grid, -grid])
+    ref = torch.tensor(v, dtype=torch.float64).to(torch.float8_e5m2).to(torch.float64).numpy()
+    assert np.array_equal(F8.e5m2(v), ref)
+
+
+def test_e5m2_grid_facts():
+    assert F8.e5m2(57344.0) == 57344.0 and F8.e5m2(1e9) == 57344.0
+    assert F8.e5m2(2.0 ** -16) == 2.0 ** -16 and F8.e5m2(2.0 ** -17) == 0.0
+    assert F8.e5m2(1.125) == 1.0 and F8.e5m2(1.375) == 1.5  # ties to even mantissa
+
+
+@pytest.mark.parametrize("M,H,I", [(3, 6, 5), (5, 8, 4)])
+def test_fp8_backward_matches_finite_differences_of_the_dequantised_forward(M, H, I):
+    # Inputs chosen so that no quantisation rounds: one-hot token rows for x
+    # and dout, W1 in {-1..2}, W2 in {-1, 0, 1}, so that pre is in {-1..2},
+    # dout W2 in {-1, 0, 1} and dpre = 2 (dout W2) relu(pre) in {0, 2, 4}
+    # (exact e5m2 codes).  The backward must then be the derivative of the
+    # dequantised forward out = relu(x W1^T)^2 W2^T (postact quantisation
+    # as the identity): central differences.
+    rng = np.random.default_rng(57)
+    x8 = np.eye(H)[rng.integers(0, H, M)]
+    W1 = rng.integers(-1, 3, (I, H)).astype(float)
+    W2 = rng.integers(-1, 2, (H, I)).astype(float)
+    dout = np.eye(H)[rng.integers(0, H, M)] * rng.choice([-1.0, 1.0], (M, 1))
+    one = dict(sx=1.0, s1=1.0, s2=1.0, s_post=1.0, sg=1.0, s_dpre=1.0)
+    a8 = F8.fp8_relu_sq_forward(x8, W1, W2, 1.0, 1.0, 1.0, 1.0)["a8"]
+    bw = F8.fp8_relu_sq_backward(dout, x8, W1, W2, a8, **one)
+    assert np.array_equal(bw["dP8"], bw["dpre"])  # exact codes
+
+    def loss(x, W1_, W2_):
+        return float(np.sum(dout * ((np.maximum(x @ W1_.T, 0) ** 2) @ W2_.T)))
+    h = 1e-6
+    for name, arr, key in (("x", x8, "dx"), ("W1", W1, "dW1"), ("W2", W2, "dW2")):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = loss(x8, W1, W2)
+            arr[idx] = old - h
+            lm = loss(x8, W1, W2)
+            arr[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        assert np.max(np.abs(bw[key] - num)) <= 1e-5 * max(1.0, np.max(np.abs(num))), name
+
+
+def test_planted_missing_relu_grad_factor_is_caught():
+    rng = np.random.default_rng(58)
+    x8 = rng.integers(-2, 3, (4, 6)).astype(float)
+    W1 = rng.integers(-2, 3, (5, 6)).astype(float)
+    W2 = rng.integers(-2, 3, (6, 5)).astype(float)
+    dout = rng.integers(-2, 3, (4, 6)).astype(float)
+    a8 = F8.fp8_relu_sq_forward(x8, W1, W2, 1.0, 1.0, 1.0, 1.0)["a8"]
+    good = F8.fp8_relu_sq_backward(dout, x8, W1, W2, a8, 1.0, 1.0, 1.0, 1.0, 1.0, 1.0)["dx"]
+    bad = ((dout @ W2) * np.maximum(x8 @ W1.T, 0)) @ W1  # the factor 2 dropped
+    assert not np.array_equal(good, bad)
