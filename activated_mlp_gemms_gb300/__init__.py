@@ -24,7 +24,7 @@ __all__ = [
     "MODE_FWD", "MODE_INFER", "MODE_BWD", "MODE_BWD_RECOMPUTE", "mlp_trace_enable",
     "mlp_trace_read", "mlp_kernel_name", "mlp_set_tile_policy", "mlp_fwd_infer_noalloc",
     "Block", "block", "mlp_block_fwd", "mlp_block_bwd", "mlp_fp8_quantize", "mlp_fp8_fwd",
-    "MODE_FP8_FWD",
+    "MODE_FP8_FWD", "mlp_fp8_bwd", "MODE_FP8_BWD",
     "NOALLOC_SCRATCH_BYTES", "mlp_set_wait_timeout_ms", "mlp_debug_set_flags", "DEBUG_NO_WORK",
 ]
 
@@ -34,7 +34,7 @@ LIB_PATH = os.path.join(_HERE, "libmlp.so")
 ACTS = {"swiglu": 0, "relu_sq": 1, "gelu_tanh_approx": 2, "relu": 3, "reglu": 4, "geglu": 5,
         "glu": 6}
 GATED_ACTS = ("swiglu", "reglu", "geglu", "glu")
-MODE_FWD, MODE_INFER, MODE_BWD, MODE_BWD_RECOMPUTE, MODE_FP8_FWD = 0, 1, 2, 3, 4
+MODE_FWD, MODE_INFER, MODE_BWD, MODE_BWD_RECOMPUTE, MODE_FP8_FWD, MODE_FP8_BWD = 0, 1, 2, 3, 4, 5
 NOALLOC_SCRATCH_BYTES = 16 << 20  # MLP_NOALLOC_SCRATCH_BYTES
 DEBUG_NO_WORK = 1  # MLP_DEBUG_NO_WORK
 
@@ -84,8 +84,10 @@ def lib():
     L.mlp_bwd_recompute.restype = ctypes.c_int
     L.mlp_fp8_quantize.argtypes = [_VP, ctypes.c_longlong, _VP, _VP, _VP, _VP]
     L.mlp_fp8_quantize.restype = ctypes.c_int
-    L.mlp_fp8_fwd.argtypes = [P] + [_VP] * 7 + [_VP, ctypes.c_size_t, _VP]
+    L.mlp_fp8_fwd.argtypes = [P] + [_VP] * 8 + [_VP, ctypes.c_size_t, _VP]
     L.mlp_fp8_fwd.restype = ctypes.c_int
+    L.mlp_fp8_bwd.argtypes = [P] + [_VP] * 11 + [_VP, ctypes.c_size_t, _VP]
+    L.mlp_fp8_bwd.restype = ctypes.c_int
     B = ctypes.POINTER(Block)
     L.mlp_block_fwd.argtypes = [P, B] + [_VP] * 8 + [_VP, ctypes.c_size_t, _VP]
     L.mlp_block_fwd.restype = ctypes.c_int
@@ -270,8 +272,8 @@ def _u8(t, name):
     if t is None:
         return None
     if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()
-            and t.dtype in (torch.uint8, torch.float8_e4m3fn)):
-        raise ValueError(f"{name} must be a contiguous CUDA uint8 / float8_e4m3fn tensor")
+            and t.dtype in (torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)):
+        raise ValueError(f"{name} must be a contiguous CUDA uint8 / float8 tensor")
     return t.data_ptr()
 
 
@@ -284,14 +286,33 @@ def mlp_fp8_quantize(src, scale, dst, amax=None, stream=None):
 
 
 def mlp_fp8_fwd(prob: Problem, x8, W1_8, W2_8, scales, out, a8_save=None, amax_a=None, ws=None,
-                stream=None):
-    """e4m3 forward of the ReLU^2 MLP; scales = fp32 [4] device tensor {sx, s1, s2, s_post}."""
+                stream=None, pre_save=None):
+    """e4m3 forward of the ReLU^2 MLP; scales = fp32 device tensor {sx, s1, s2, s_post, ...};
+    pre_save (bf16 [M, I]) receives the preact for mlp_fp8_bwd."""
     ws = _ws(ws, prob, MODE_FP8_FWD, out.device)
     rc = lib().mlp_fp8_fwd(ctypes.byref(prob), _u8(x8, "x8"), _u8(W1_8, "W1_8"), _u8(W2_8, "W2_8"),
                            _ptr(scales, torch.float32, "scales"), _ptr(out, name="out"),
-                           _u8(a8_save, "a8_save"), _ptr(amax_a, torch.float32, "amax_a"),
+                           _u8(a8_save, "a8_save"), _ptr(pre_save, name="pre_save"),
+                           _ptr(amax_a, torch.float32, "amax_a"),
                            ws.data_ptr(), ws.numel(), _stream(stream))
     _check(rc, "mlp_fp8_fwd")
+    return ws
+
+
+def mlp_fp8_bwd(prob: Problem, dout, x8, W1_8, W2_8, pre, a8, scales, dx=None, dW1=None, dW2=None,
+                amax_dpre=None, ws=None, stream=None):
+    """8-bit backward of the ReLU^2 MLP (e5m2 gradients); scales = fp32 [6] device tensor
+    {sx, s1, s2, s_post, sg, s_dpre}; dx [M,H], dW1 [I,H], dW2 [H,I] bf16 outputs."""
+    ws = _ws(ws, prob, MODE_FP8_BWD, dout.device)
+    if scales is not None and scales.numel() < 6:
+        raise ValueError("scales must hold {sx, s1, s2, s_post, sg, s_dpre}")
+    rc = lib().mlp_fp8_bwd(ctypes.byref(prob), _ptr(dout, name="dout"), _u8(x8, "x8"),
+                           _u8(W1_8, "W1_8"), _u8(W2_8, "W2_8"), _ptr(pre, name="pre"),
+                           _u8(a8, "a8"), _ptr(scales, torch.float32, "scales"),
+                           _ptr(dx, name="dx"), _ptr(dW1, name="dW1"), _ptr(dW2, name="dW2"),
+                           _ptr(amax_dpre, torch.float32, "amax_dpre"),
+                           ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(rc, "mlp_fp8_bwd")
     return ws
 
 

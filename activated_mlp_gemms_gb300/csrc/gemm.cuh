@@ -23,7 +23,11 @@
 // arrive as boxes {64 (MN), 64 (K)} placed 8 KB apart.  The matching UMMA
 // descriptors: K-major SBO = 1024 B (8-row groups), start += 32 B per K=16
 // step; MN-major LBO = 8192 B (next 64-wide MN block), SBO = 1024 B (next 8
-// K rows), start += 2048 B per K=16 step.
+// K rows), start += 2048 B per K=16 step.  8-bit operands (e4m3 / e5m2)
+// keep the 128-byte rows, so a k-block is 128 elements: K-major boxes
+// {128 (K), rows} with the same descriptors (+32 B per K=32 step);
+// MN-major boxes {128 (MN), 128 (K)} of 16 KB, LBO = 16384 B, SBO = 1024 B,
+// start += 4096 B per K=32 step.
 #pragma once
 #include <atomic>
 
@@ -70,12 +74,15 @@ struct EpiTraits {
   // dU, a; dact: dP, a; plain: D) and bytes of one staged 32 x 32 box
   static constexpr int NOUT = (EPI == EPI_GATED_FWD || EPI == EPI_DGATED) ? 3
                               : (EPI == EPI_ACT_FWD || EPI == EPI_DACT ||
-                                 EPI == EPI_DACT_RECOMP)                  ? 2
-                                                                          : 1;
-  // bytes of a 32 x 32 output box: fp32 4096, bf16 2048, e4m3 1024
-  static constexpr int OUT_BYTES = (EPI == EPI_ACCUM_F32) ? 4096 : (EPI == EPI_ACT_FWD_F8) ? 1024
-                                                                                            : 2048;
-  static constexpr bool DACT = (EPI == EPI_DGATED || EPI == EPI_DACT);
+                                 EPI == EPI_DACT_RECOMP || EPI == EPI_ACT_FWD_F8) ? 2
+                                                                                  : 1;
+  // bytes of a staged 32 x 32 output box: fp32 4096, bf16 2048, 8-bit 1024
+  // (EPI_ACT_FWD_F8's e4m3 box takes the first 1024 B of a 2048-byte slot,
+  // its bf16 preact the second slot)
+  static constexpr int OUT_BYTES = (EPI == EPI_ACCUM_F32) ? 4096 : (EPI == EPI_DGRAD_F8) ? 1024
+                                                                                          : 2048;
+  // the epilogue reads saved preacts (in0 / in1), fetched ahead of the accumulator
+  static constexpr bool DACT = (EPI == EPI_DGATED || EPI == EPI_DACT || EPI == EPI_DGRAD_F8);
   // staged boxes per warp: at most two (a third output reuses the first box
   // once that box's store has read it), so the stage ring keeps 6 stages
   static constexpr int STG_BUFS = NOUT < 2 ? NOUT : 2;
@@ -134,10 +141,13 @@ struct EpiUnit {
   const void* in1;
   const float* rstd;          // per-row scale (nullptr: none)
   float alpha;                // residual scale
-  const float* scl;           // e4m3 dequant scales {sx, s1, s2, s_post}
-  float* amax;                // running max of the e4m3 epilogue's a
+  float deq;                  // 8-bit epilogues: *sa * *sb (the operands' dequant scales)
+  float mult;                 // ... the problem's multiplier
+  float inv;                  // ... fp32(1 / *sq), the 8-bit output's quantisation factor
+  float* amax;                // running max of the 8-bit epilogue's output
 };
 
+template <int EPI>
 __device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P) {
   EpiUnit U;
 #pragma unroll
@@ -149,8 +159,16 @@ __device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P) {
   U.in1 = P.in1;
   U.rstd = P.rstd;
   U.alpha = P.alpha;
-  U.scl = P.scl;
-  U.amax = P.amax;
+  U.deq = 1.f;
+  U.mult = 1.f;
+  U.inv = 1.f;
+  U.amax = nullptr;
+  if constexpr (is_f8(EPI)) {
+    U.deq = *P.sa * *P.sb;
+    U.mult = P.mult;
+    if (P.sq) U.inv = 1.0f / *P.sq;
+    U.amax = P.amax;
+  }
   return U;
 }
 
@@ -431,16 +449,18 @@ __device__ __forceinline__ void epi_recomp_dh(const Params& p, const EpiUnit& P,
   }
 }
 
-// e4m3 forward of the ReLU^2 MLP: pre = acc * sx * s1, a = s * relu(pre)^2,
-// a -> e4m3(a * fp32(1 / s_post)) through a 32 x 32-byte box (map 0); the
-// largest a of the warp's rows goes to *amax (atomic max on the bits of a
-// non-negative float).
+// e4m3 forward of the ReLU^2 MLP: pre = acc * sx * s1, a = mult * relu(pre)^2,
+// a -> e4m3(a * fp32(1 / s_post)) through a 32 x 32-byte box (map 0) and, if
+// requested, pre in bf16 through a 32 x 32 bf16 box (map 1, for the
+// backward); the largest a of the warp's rows goes to *amax (atomic max on
+// the bits of a non-negative float).
 template <int ACT>
 __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                            uint32_t tb, int col0, int cb, int ce) {
-  const float deq = P.scl[0] * P.scl[1];
-  const float inv = 1.0f / P.scl[3];
-  const float s = p.scale;
+  const float deq = P.deq;
+  const float inv = P.inv;
+  const float s = P.mult;
+  const bool want_pre = P.out[1] != nullptr;
   const bool row_ok = e.row0 + e.lane < P.M;
   float mx = 0.f;
 #pragma unroll 1
@@ -451,15 +471,16 @@ __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, co
     __syncwarp();
     tmem_ld32(tb + c, z);
     tmem_wait_ld();
-    uint32_t q[8];
+    uint32_t q[8], pp[16];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       uint32_t w = 0;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int k = 4 * j + 2 * h;
-        const float p0 = fmaxf(__uint_as_float(z[k]) * deq, 0.f);
-        const float p1 = fmaxf(__uint_as_float(z[k + 1]) * deq, 0.f);
+        const float z0 = __uint_as_float(z[k]) * deq, z1 = __uint_as_float(z[k + 1]) * deq;
+        pp[2 * j + h] = pack_bf16x2(z0, z1);
+        const float p0 = fmaxf(z0, 0.f), p1 = fmaxf(z1, 0.f);
         const float a0 = s * p0 * p0, a1 = s * p1 * p1;
         mx = fmaxf(mx, fmaxf(a0, a1));
         w |= static_cast<uint32_t>(pack_e4m3x2(a0 * inv, a1 * inv)) << (16 * h);
@@ -470,10 +491,67 @@ __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, co
     const uint32_t rb = e.stg + static_cast<uint32_t>(e.lane) * 32u;
     st_shared_v4(rb, q[0], q[1], q[2], q[3]);
     st_shared_v4(rb + 16, q[4], q[5], q[6], q[7]);
-    flush_chunk<1, 1024, false>(p, P, e, col);
+    if (want_pre) stage_bf16(e.stg + 2048, e.lane, pp);
+    flush_chunk<2, 2048, false>(p, P, e, col);
   }
   if (P.amax) {
     if (!row_ok) mx = 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (e.lane == 0 && mx > 0.f) atomicMax(reinterpret_cast<int*>(P.amax), __float_as_int(mx));
+  }
+}
+
+// e5m2 derivative of the 8-bit ReLU^2 MLP: dpre = deq * acc * 2 * relu(P)
+// with P the saved bf16 preact (in0), dpre -> e5m2(dpre * fp32(1 / *sq))
+// through a 32 x 32-byte box (map 0); the largest |dpre| of the warp's rows
+// goes to *amax.  P's chunk c+1 is loaded while chunk c is computed (the
+// caller loads chunk `cb` before waiting for the accumulator).
+__device__ __forceinline__ void epi_dgrad_f8(const Params& p, const EpiUnit& P, const EpiWarp& e,
+                                             uint32_t tb, int col0, int cb, int ce,
+                                             uint4 (&pg)[4]) {
+  const float dq2 = 2.f * P.mult * P.deq;
+  const float inv = P.inv;
+  const int row = e.row0 + e.lane;
+  float mx = 0.f;
+#pragma unroll 1
+  for (int c = cb; c < ce; c += 32) {
+    const int col = col0 + c;
+    if (col >= P.N) break;
+    uint4 ng[4], nu[4];
+    if (c + 32 < ce) dact_load<false>(P, row, col + 32, ng, nu);
+    uint32_t z[32];
+    __syncwarp();
+    tmem_ld32(tb + c, z);
+    tmem_wait_ld();
+    uint32_t q[8];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint32_t gw[4] = {pg[v].x, pg[v].y, pg[v].z, pg[v].w};
+      q[2 * v] = 0;
+      q[2 * v + 1] = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 pr = unpack_bf16x2(gw[j]);
+        const float d0 = dq2 * __uint_as_float(z[8 * v + 2 * j]) * fmaxf(pr.x, 0.f);
+        const float d1 = dq2 * __uint_as_float(z[8 * v + 2 * j + 1]) * fmaxf(pr.y, 0.f);
+        mx = fmaxf(mx, fmaxf(fabsf(d0), fabsf(d1)));
+        q[2 * v + (j >> 1)] |= static_cast<uint32_t>(pack_e5m2x2(d0 * inv, d1 * inv))
+                               << (16 * (j & 1));
+      }
+    }
+    staging_acquire(e);
+    const uint32_t rb = e.stg + static_cast<uint32_t>(e.lane) * 32u;
+    st_shared_v4(rb, q[0], q[1], q[2], q[3]);
+    st_shared_v4(rb + 16, q[4], q[5], q[6], q[7]);
+    flush_chunk<1, 1024, false>(p, P, e, col);
+    if (c + 32 < ce) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) pg[v] = ng[v];
+    }
+  }
+  if (P.amax) {
+    if (row >= P.M) mx = 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (e.lane == 0 && mx > 0.f) atomicMax(reinterpret_cast<int*>(P.amax), __float_as_int(mx));
@@ -493,7 +571,7 @@ __device__ __forceinline__ void epi_plain(const Params& p, const EpiUnit& P, con
     tmem_wait_ld();
     staging_acquire(e);
     if constexpr (EPI == EPI_STORE_BF16_F8) {
-      const float deq = p.scale * P.scl[3] * P.scl[2];
+      const float deq = P.mult * P.deq;
       uint32_t q[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
@@ -597,6 +675,8 @@ __device__ __forceinline__ UnitLoads unit_loads(const Params& p, const Prob& P, 
 //   B gated:   CG=1 the gate and the up rows (two {64, 128} boxes);
 //              CG=2 the leader stages the gate rows, the peer the up rows.
 //   B K-major: one box {64, 256 / CG};      B MN-major: 4 / CG boxes {64 n, 64 k}.
+//   8-bit operands: K-major boxes as above ({128 k, rows}); A MN-major one box
+//   {128 m, 128 k}; B MN-major 2 / CG boxes {128 n, 128 k}.
 //   EPI_DACT_RECOMP: segment 0 B K-major (W1), segment 1 B MN-major (Wd).
 template <int EPI, bool A_MN, bool B_MN, int CG>
 __device__ __forceinline__ void load_stage(const UnitLoads& L, int seg, int kc, uint32_t sA,
@@ -608,6 +688,8 @@ __device__ __forceinline__ void load_stage(const UnitLoads& L, int seg, int kc, 
   const CUtensorMap* mA = seg == 0 ? L.a0 : L.a1;
   if constexpr (!A_MN) {
     ld(sA, mA, kc, L.m0);
+  } else if constexpr (is_f8(EPI)) {
+    ld(sA, mA, L.m0, kc);
   } else {
     ld(sA, mA, L.m0, kc);
     ld(sA + 8192, mA, L.m0 + 64, kc);
@@ -621,6 +703,9 @@ __device__ __forceinline__ void load_stage(const UnitLoads& L, int seg, int kc, 
     const bool b_mn = EPI == EPI_DACT_RECOMP ? seg == 1 : B_MN;
     if (!b_mn) {
       ld(sB, mB, kc, L.n0);
+    } else if constexpr (is_f8(EPI)) {
+#pragma unroll
+      for (int j = 0; j < 2 / CG; ++j) ld(sB + j * 16384, mB, L.n0 + j * 128, kc);
     } else {
 #pragma unroll
       for (int j = 0; j < 4 / CG; ++j) ld(sB + j * 8192, mB, L.n0 + j * 64, kc);
@@ -635,10 +720,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
   using C = Cfg<EPI, CG>;
   constexpr bool PAIR = CG == 2;
   constexpr int TILE_N = EpiTraits<EPI>::TILE_N;
-  // e4m3 operands: a 128-byte k-block row holds 128 elements (bf16: 64)
-  constexpr bool F8 = EPI == EPI_ACT_FWD_F8 || EPI == EPI_STORE_BF16_F8;
+  // 8-bit operands: a 128-byte k-block row holds 128 elements (bf16: 64)
+  constexpr bool F8 = is_f8(EPI);
   constexpr int KE = F8 ? 2 * BK : BK;
-  constexpr uint32_t IDESC = F8 ? idesc_e4m3(C::TILE_M, MMA_N) : idesc_bf16(C::TILE_M, MMA_N, A_MN, B_MN);
+  constexpr uint32_t IDESC = idesc_bf16(C::TILE_M, MMA_N, A_MN, B_MN);
   constexpr uint32_t IDESC_BMN = idesc_bf16(C::TILE_M, MMA_N, A_MN, true);
 
   // 1024-byte aligned stage ring (the 128-byte swizzle repeats every 1 KB)
@@ -803,6 +888,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
+      // 8-bit operands: their formats come with the launch
+      const uint32_t idesc_8 = idesc_f8(C::TILE_M, MMA_N, p.f8_formats & 7, (p.f8_formats >> 3) & 7,
+                                        A_MN, B_MN);
+      (void)idesc_8;
       int stage = 0;
       uint32_t phase = 0;
       int slot = 0;
@@ -847,11 +936,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
           const bool b_mn = B_MN || seg1;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = A_MN ? sdesc_sw128(sA + k * 2048, 8192, 1024)
+            // MN-major: bf16 K=16 steps of 16 rows, 8-bit K=32 steps of 32 rows
+            constexpr uint32_t MN_STEP = F8 ? 4096 : 2048, MN_LBO = F8 ? 16384 : 8192;
+            const uint64_t ad = A_MN ? sdesc_sw128(sA + k * MN_STEP, MN_LBO, 1024)
                                      : sdesc_sw128(sA + k * 32, 16, 1024);
-            const uint64_t bd = b_mn ? sdesc_sw128(sB + k * 2048, 8192, 1024)
+            const uint64_t bd = b_mn ? sdesc_sw128(sB + k * MN_STEP, MN_LBO, 1024)
                                      : sdesc_sw128(sB + k * 32, 16, 1024);
-            const uint32_t idesc = b_mn ? IDESC_BMN : IDESC;
+            const uint32_t idesc = F8 ? idesc_8 : b_mn ? IDESC_BMN : IDESC;
             const uint32_t accum = (kb > kfirst || k > 0) ? 1u : 0u;
             if constexpr (F8) {
               if constexpr (PAIR) tc_mma_f8_pair(d, ad, bd, idesc, accum);
@@ -909,7 +1000,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
       if (unit < 0) break;
       const Work w = decode_unit(p, unit);
-      const EpiUnit P = epi_unit(p, p.prob[w.prob]);
+      const EpiUnit P = epi_unit<EPI>(p, p.prob[w.prob]);
       e.row0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
       e.rows_ok = e.row0 < P.M;
       e.rs = (P.rstd && e.row0 + lane < P.M) ? P.rstd[e.row0 + lane] : 1.f;
@@ -959,6 +1050,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
           epi_recomp_dh(p, P, e, tb, col0, cb, dd);
         } else if constexpr (EPI == EPI_ACT_FWD_F8) {
           epi_act_f8<ACT>(p, P, e, tb, col0, cb, ce);
+        } else if constexpr (EPI == EPI_DGRAD_F8) {
+          epi_dgrad_f8(p, P, e, tb, col0, cb, ce, pg);
         } else {
           epi_plain<EPI>(p, P, e, tb, col0, cb, ce);
         }

@@ -31,10 +31,20 @@ enum Epi : int {
   // segment 0 acc = p = x W1^T (accumulator 0), segment 1 acc = dh = dout Wd
   // (accumulator 1): a = s*act(p), dP = s*dh*act'(p)
   EPI_DACT_RECOMP = 6,
-  // e4m3 operands (tcgen05 kind::f8f6f4), dequant scales scl = {sx, s1, s2, s_post}:
-  EPI_ACT_FWD_F8 = 7,    // a = s*relu(acc*sx*s1)^2 -> e4m3(a / s_post) (map 0), amax(a) -> *amax
-  EPI_STORE_BF16_F8 = 8  // D = bf16(s * acc * s_post * s2)
+  // 8-bit operands (tcgen05 kind::f8f6f4; e4m3 or e5m2 per operand, Params::f8_formats)
+  // with the problem's dequant factor deq = mult * *sa * *sb:
+  EPI_ACT_FWD_F8 = 7,     // pre = deq'*acc (deq' = *sa * *sb), a = mult*relu(pre)^2 ->
+                          // e4m3(a / *sq) (map 0), optional bf16 pre (map 1), amax(a) -> *amax
+  EPI_STORE_BF16_F8 = 8,  // D = bf16(deq * acc)
+  EPI_DGRAD_F8 = 9        // dpre = deq*acc*2*relu(P) (in0 = P, bf16) -> e5m2(dpre / *sq)
+                          // (map 0), amax|dpre| -> *amax
 };
+
+__host__ __device__ constexpr bool is_f8(int epi) {
+  return epi == EPI_ACT_FWD_F8 || epi == EPI_STORE_BF16_F8 || epi == EPI_DGRAD_F8;
+}
+// 8-bit operand formats of Params::f8_formats (the kind::f8f6f4 type codes)
+constexpr int F8_E4M3 = 0, F8_E5M2 = 1;
 
 // The function applied to the gate (gated MLPs) or to the preact (non-gated).
 enum Act : int { ACT_SILU = 0, ACT_RELU_SQ = 1, ACT_GELU_TANH = 2, ACT_RELU = 3, ACT_SIGMOID = 4 };
@@ -61,8 +71,12 @@ struct Prob {
                           // dG, dU / dP (derivative epilogues) are multiplied by rstd[row]
   float alpha;            // EPI_STORE_BF16 with in0 = residual [M, ld]: D = alpha*in0 + acc
   int pad_b;
-  const float* scl;       // e4m3 epilogues: the dequant scales {sx, s1, s2, s_post}
-  float* amax;            // EPI_ACT_FWD_F8: running max of a (atomic; may be null)
+  // 8-bit epilogues: dequant factor mult * *sa * *sb; *sq the scale of an 8-bit output
+  const float* sa;
+  const float* sb;
+  const float* sq;
+  float mult;
+  float* amax;            // running max of |the quantised output| (atomic; may be null)
 };
 
 struct Params {  // 64-byte aligned through CUtensorMap
@@ -73,7 +87,7 @@ struct Params {  // 64-byte aligned through CUtensorMap
   int act;
   int group_m;            // L2 raster: tiles are visited in groups of group_m tile rows
   float scale;            // gate_mult * down_mult (activation epilogues)
-  int pad_;
+  int f8_formats;         // 8-bit MMAs: A's format (bits 0-2) and B's (bits 3-5), F8_*
   int debug_flags;        // MLP_DEBUG_* (testing only; 0 in normal use)
   int a_tx_bytes;         // bytes one CTA's A boxes bring per k-block (K-major A: rows x 128 B)
   int nmaps;              // tensor maps in use
@@ -102,10 +116,11 @@ cudaError_t launch_postact(const void* G, const void* U, void* a, long long n, i
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, long long n, cudaStream_t stream,
                                bool pdl, const void* resid = nullptr, float alpha = 0.f);
 
-// e4m3 codes q = e4m3(fp32(src * fp32(1 / *scale))) of n bf16 values (saturating,
-// round to nearest even); with `amax`, atomic max of |src| into *amax.
-cudaError_t launch_quant_e4m3(const void* src, long long n, const float* scale, void* dst,
-                              float* amax, cudaStream_t stream, bool pdl);
+// 8-bit codes q = f8(fp32(src * fp32(1 / *scale))) of n bf16 values, f8 = e4m3
+// (fmt F8_E4M3) or e5m2 (F8_E5M2), saturating, round to nearest even; with
+// `amax`, atomic max of |src| into *amax.
+cudaError_t launch_quant_f8(const void* src, long long n, const float* scale, void* dst,
+                            float* amax, int fmt, cudaStream_t stream, bool pdl);
 
 // Per-token RMS-norm scale rstd[m] = 1 / sqrt(mean_h x^2 + eps), x bf16 [M, H].
 cudaError_t launch_rstd(const void* x, float* rstd, int M, int H, float eps, cudaStream_t stream,

@@ -1,15 +1,16 @@
-// e4m3 (FP8) kernels of the ReLU^2 MLP forward: the quantisation of bf16
-// tensors to e4m3 codes with a dequant scale (and their amax), and the two
-// GEMM instances: fc1 with the ReLU^2 epilogue that re-quantises its output,
-// and the down projection with a dequantising bf16 store.
+// 8-bit (FP8) kernels of the ReLU^2 MLP forward: the quantisation of bf16
+// tensors to e4m3 or e5m2 codes with a dequant scale (and their amax), and
+// the forward GEMM instances: fc1 with the ReLU^2 epilogue that re-quantises
+// its output, and the down projection with a dequantising bf16 store.
 #include "gemm.cuh"
 
 namespace mlpk {
 
-// q = e4m3(fp32(x * fp32(1 / *scale))), saturating, 8 values (one 16-byte
+// q = f8(fp32(x * fp32(1 / *scale))), saturating, 8 values (one 16-byte
 // load, one 8-byte store) per vector; each thread loads four grid-strided
 // vectors before converting them, so that their loads are in flight
 // together.  |x|'s maximum goes to *amax.
+template <int FMT>
 __device__ __forceinline__ uint2 quant8(uint4 v, float inv, float& mx) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t o[2] = {0, 0};
@@ -17,14 +18,17 @@ __device__ __forceinline__ uint2 quant8(uint4 v, float inv, float& mx) {
   for (int j = 0; j < 4; ++j) {
     const float2 f = unpack_bf16x2(w[j]);
     mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
-    o[j >> 1] |= static_cast<uint32_t>(pack_e4m3x2(f.x * inv, f.y * inv)) << (16 * (j & 1));
+    const uint16_t c = FMT == F8_E5M2 ? pack_e5m2x2(f.x * inv, f.y * inv)
+                                      : pack_e4m3x2(f.x * inv, f.y * inv);
+    o[j >> 1] |= static_cast<uint32_t>(c) << (16 * (j & 1));
   }
   return make_uint2(o[0], o[1]);
 }
 
-__global__ void __launch_bounds__(256) k_quant_e4m3(const __nv_bfloat16* __restrict__ src,
-                                                    long long n8, const float* __restrict__ scale,
-                                                    uint8_t* __restrict__ dst, float* amax) {
+template <int FMT>
+__global__ void __launch_bounds__(256) k_quant_f8(const __nv_bfloat16* __restrict__ src,
+                                                  long long n8, const float* __restrict__ scale,
+                                                  uint8_t* __restrict__ dst, float* amax) {
   pdl_wait();
   pdl_launch_dependents();
   const float inv = 1.0f / *scale;
@@ -38,7 +42,7 @@ __global__ void __launch_bounds__(256) k_quant_e4m3(const __nv_bfloat16* __restr
 #pragma unroll
     for (int u = 0; u < 4; ++u)
       if (i + u * stride < n8)
-        *reinterpret_cast<uint2*>(dst + 8 * (i + u * stride)) = quant8(v[u], inv, mx);
+        *reinterpret_cast<uint2*>(dst + 8 * (i + u * stride)) = quant8<FMT>(v[u], inv, mx);
   }
   if (amax) {
 #pragma unroll
@@ -47,8 +51,8 @@ __global__ void __launch_bounds__(256) k_quant_e4m3(const __nv_bfloat16* __restr
   }
 }
 
-cudaError_t launch_quant_e4m3(const void* src, long long n, const float* scale, void* dst,
-                              float* amax, cudaStream_t stream, bool pdl) {
+cudaError_t launch_quant_f8(const void* src, long long n, const float* scale, void* dst,
+                            float* amax, int fmt, cudaStream_t stream, bool pdl) {
   const long long n8 = n / 8;  // n is a multiple of 8
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -65,8 +69,10 @@ cudaError_t launch_quant_e4m3(const void* src, long long n, const float* scale, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_quant_e4m3, static_cast<const __nv_bfloat16*>(src), n8, scale,
-                            static_cast<uint8_t*>(dst), amax);
+  auto s = static_cast<const __nv_bfloat16*>(src);
+  auto d = static_cast<uint8_t*>(dst);
+  if (fmt == F8_E5M2) return cudaLaunchKernelEx(&cfg, k_quant_f8<F8_E5M2>, s, n8, scale, d, amax);
+  return cudaLaunchKernelEx(&cfg, k_quant_f8<F8_E4M3>, s, n8, scale, d, amax);
 }
 
 template cudaError_t launch_gemm<EPI_ACT_FWD_F8, false, false, 1, ACT_RELU_SQ>(const Params&, int, cudaStream_t, bool);

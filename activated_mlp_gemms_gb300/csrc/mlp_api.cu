@@ -223,6 +223,12 @@ struct Gemm {
     p.a_tx_bytes = box * BK * 2;  // 128 bytes per row, as for bf16
     return kmajor_u8(ptr, rows, K, box);
   }
+  // 8-bit MN-major operand [K, MN] (MN bytes per row), boxes {128 mn, 128 k}
+  int mnmajor_u8(const void* ptr, int K, int MN) {
+    if (nmaps >= MAX_MAPS) { ok = false; return 0; }
+    if (!make_map(&p.maps[nmaps], ptr, MN, K, MN, 2 * BK, 2 * BK, 2)) ok = false;
+    return nmaps++;
+  }
   // e4m3 epilogue output [rows, cols], 32 x 32-byte boxes, no swizzle.
   int output_u8(void* ptr, int rows, int cols) {
     if (!ptr) return -1;
@@ -460,6 +466,9 @@ size_t split_bytes(const mlp_problem_t* p, int mode) {
 size_t ws_size(const mlp_problem_t* p, int mode) {
   // e4m3 forward: the control block + the e4m3 postact (one byte per element)
   if (mode == MLP_MODE_FP8_FWD) return CTRL_BYTES + round256((size_t)p->M * p->I);
+  // 8-bit backward: + the e5m2 codes of dout [M,H] and of dpre [M,I]
+  if (mode == MLP_MODE_FP8_BWD)
+    return CTRL_BYTES + round256((size_t)p->M * p->H) + round256((size_t)p->M * p->I);
   size_t n = CTRL_BYTES + inter_bytes(p);  // control block + postact a
   if (mode == MLP_MODE_BWD_RECOMPUTE) n += inter_bytes(p) * (gated(p) ? 2 : 1);
   return n + split_bytes(p, mode);  // + the fp32 partial-sum region (small M only)
@@ -837,7 +846,7 @@ extern "C" {
 
 size_t mlp_workspace_size(const mlp_problem_t* p, int mode) {
   if (check_problem(p) != MLP_OK) return 0;
-  if (mode < MLP_MODE_FWD || mode > MLP_MODE_FP8_FWD) return 0;
+  if (mode < MLP_MODE_FWD || mode > MLP_MODE_FP8_BWD) return 0;
   return ws_size(p, mode);
 }
 
@@ -889,12 +898,12 @@ int mlp_fp8_quantize(const void* src, long long n, const float* scale, void* dst
   if (!scale) return MLP_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return traced(MLP_KERNEL_QUANT, s,
-                [&] { return launch_quant_e4m3(src, n, scale, dst, amax, s, false); });
+                [&] { return launch_quant_f8(src, n, scale, dst, amax, F8_E4M3, s, false); });
 }
 
 int mlp_fp8_fwd(const mlp_problem_t* p, const void* x8, const void* W1_8, const void* W2_8,
-                const float* scales, void* out, void* a8_save, float* amax_a, void* ws,
-                size_t ws_bytes, void* stream) {
+                const float* scales, void* out, void* a8_save, void* pre_save, float* amax_a,
+                void* ws, size_t ws_bytes, void* stream) {
   MLP_TRY(check_problem(p));
   if (p->act != MLP_ACT_RELU_SQ) return MLP_ERR_UNSUPPORTED;
   if (p->H % 16 || p->I % 16) return MLP_ERR_ALIGNMENT;  // 16-byte e4m3 rows
@@ -903,6 +912,7 @@ int mlp_fp8_fwd(const mlp_problem_t* p, const void* x8, const void* W1_8, const 
   MLP_TRY(need(W2_8));
   MLP_TRY(need(out));
   MLP_TRY(opt(a8_save));
+  MLP_TRY(opt(pre_save));
   if (!scales) return MLP_ERR_INVALID_ARG;
   MLP_TRY(check_ws(p, MLP_MODE_FP8_FWD, ws, ws_bytes));
   Call c;
@@ -912,21 +922,24 @@ int mlp_fp8_fwd(const mlp_problem_t* p, const void* x8, const void* W1_8, const 
   {
     // fc1 on e4m3 codes, ReLU^2, the postact re-quantised with s_post
     Gemm g(*p, c.counter(), c.status, pick_cg(M));
-    g.p.scale = p->gate_mult;
     const int mA = g.kmajor_a_u8(x8, M, H);
     const int mB = g.kmajor_u8(W1_8, I, H, g.b_rows());
     const int oA = g.output_u8(a8, M, I);
+    const int oP = g.output(pre_save, M, I);
     Prob& P = g.add(M, I, H, 0, MMA_N, 1, 2 * BK);
     P.mapA0 = mA;
     P.mapB0 = mB;
     P.mapO[0] = oA;
-    P.scl = scales;
+    P.mapO[1] = oP;
+    P.sa = scales + 0;  // sx
+    P.sb = scales + 1;  // s1
+    P.sq = scales + 3;  // s_post
+    P.mult = p->gate_mult;
     P.amax = amax_a;
     MLP_TRY((run_act<EPI_ACT_FWD_F8, false, false, ACT_RELU_SQ>(g, c, MLP_KERNEL_GATE_UP)));
   }
   // the down projection on the re-quantised postact, dequantised to bf16
   Gemm g(*p, c.counter(), c.status, pick_cg(M));
-  g.p.scale = p->down_mult;
   const int mA = g.kmajor_a_u8(a8, M, I);
   const int mB = g.kmajor_u8(W2_8, H, I, g.b_rows());
   const int oO = g.output(out, M, H);
@@ -934,8 +947,130 @@ int mlp_fp8_fwd(const mlp_problem_t* p, const void* x8, const void* W1_8, const 
   P.mapA0 = mA;
   P.mapB0 = mB;
   P.mapO[0] = oO;
-  P.scl = scales;
+  P.sa = scales + 3;  // s_post
+  P.sb = scales + 2;  // s2
+  P.mult = p->down_mult;
   return run<EPI_STORE_BF16_F8, false, false>(g, c, MLP_KERNEL_DOWN);
+}
+
+int mlp_fp8_bwd(const mlp_problem_t* p, const void* dout, const void* x8, const void* W1_8,
+                const void* W2_8, const void* pre, const void* a8, const float* scales, void* dx,
+                void* dW1, void* dW2, float* amax_dpre, void* ws, size_t ws_bytes, void* stream) {
+  MLP_TRY(check_problem(p));
+  if (p->act != MLP_ACT_RELU_SQ) return MLP_ERR_UNSUPPORTED;
+  if (p->H % 16 || p->I % 16) return MLP_ERR_ALIGNMENT;
+  MLP_TRY(need(dout));
+  MLP_TRY(opt(dx));
+  MLP_TRY(opt(dW1));
+  MLP_TRY(opt(dW2));
+  if (!scales) return MLP_ERR_INVALID_ARG;
+  const bool need_dpre = dx || dW1;
+  if (need_dpre) {
+    MLP_TRY(need(W2_8));
+    MLP_TRY(need(pre));
+  }
+  if (dx) MLP_TRY(need(W1_8));
+  if (dW1) MLP_TRY(need(x8));
+  if (dW2) MLP_TRY(need(a8));
+  MLP_TRY(check_ws(p, MLP_MODE_FP8_BWD, ws, ws_bytes));
+  if (!need_dpre && !dW2) return MLP_OK;  // nothing requested
+  const int M = p->M, H = p->H, I = p->I;
+  Call c;
+  MLP_TRY(begin_call(c, ws, stream));
+  char* base = static_cast<char*>(ws) + CTRL_BYTES;
+  void* dout8 = base;
+  void* dP8 = base + round256((size_t)M * H);
+  // the 8-bit operands: A the e5m2 gradient codes, B the e4m3 weight / activation codes
+  const int fmts = F8_E5M2 | (F8_E4M3 << 3);
+  {
+    // dout -> e5m2 with the static gradient scale sg
+    const bool pdl = c.pdl();
+    MLP_TRY(traced(MLP_KERNEL_QUANT, c.stream, [&] {
+      return launch_quant_f8(dout, (long long)M * H, scales + 4, dout8, nullptr, F8_E5M2, c.stream,
+                             pdl);
+    }));
+  }
+  if (need_dpre) {
+    // dpre = gate_mult * down_mult * sg * s2 * (dout8 W2_8) * 2 relu(pre), to
+    // e5m2 with the delayed scale s_dpre; W2_8 [H,I]: B(n=i, k=h) is N-contiguous
+    Gemm g(*p, c.counter(), c.status, pick_cg(M));
+    g.p.f8_formats = fmts;
+    const int mA = g.kmajor_a_u8(dout8, M, H);
+    const int mB = g.mnmajor_u8(W2_8, H, I);
+    const int oP = g.output_u8(dP8, M, I);
+    Prob& P = g.add(M, I, H, 0, MMA_N, 1, 2 * BK);
+    P.mapA0 = mA;
+    P.mapB0 = mB;
+    P.mapO[0] = oP;
+    P.in0 = pre;
+    P.sa = scales + 4;  // sg
+    P.sb = scales + 2;  // s2
+    P.sq = scales + 5;  // s_dpre
+    P.mult = p->gate_mult * p->down_mult;
+    P.amax = amax_dpre;
+    MLP_TRY((run<EPI_DGRAD_F8, false, true>(g, c, MLP_KERNEL_DGATED)));
+  }
+  // dx and the weight gradients read only the codes above and the inputs:
+  // with both requested, the weight gradients run on the side stream
+  const bool want_w = dW1 || dW2;
+  Side* side = (dx && want_w && !g_trace_flag.load()) ? side_stream(c.stream) : nullptr;
+  std::unique_lock<std::mutex> side_lk;
+  if (side) {
+    side_lk = std::unique_lock<std::mutex>(side->mu);
+    MLP_TRY(cuda_err(cudaEventRecord(side->fork, c.stream)));
+  }
+  if (dx) {
+    // dx = s_dpre * s1 * (dP8 W1_8); W1_8 [I,H]: B(n=h, k=i) is N-contiguous
+    Gemm g(*p, c.counter(), c.status, pick_cg(M));
+    g.p.f8_formats = fmts;
+    const int mA = g.kmajor_a_u8(dP8, M, I);
+    const int mB = g.mnmajor_u8(W1_8, I, H);
+    const int oX = g.output(dx, M, H);
+    Prob& P = g.add(M, H, I, 0, MMA_N, 1, 2 * BK);
+    P.mapA0 = mA;
+    P.mapB0 = mB;
+    P.mapO[0] = oX;
+    P.sa = scales + 5;  // s_dpre
+    P.sb = scales + 1;  // s1
+    P.mult = 1.f;
+    MLP_TRY((run<EPI_STORE_BF16_F8, false, true>(g, c, MLP_KERNEL_DX)));
+  }
+  if (want_w) {
+    // one grouped launch over the M tokens, both operands MN-major:
+    //   dW1 = s_dpre * sx * dP8^T x8  ([I,H])   dW2 = down_mult * sg * s_post * dout8^T a8  ([H,I])
+    Call cw = c;
+    if (side) {
+      cw.stream = side->stream;
+      cw.launches = 0;
+      MLP_TRY(cuda_err(cudaStreamWaitEvent(side->stream, side->fork, 0)));
+    }
+    Gemm g(*p, c.counter(), c.status, pick_cg(H < I ? H : I));
+    g.p.f8_formats = fmts;
+    struct W { const void* A; int rows; const void* B; int cols; void* out; const float* sa;
+               const float* sb; float mult; };
+    W list[2];
+    int n = 0;
+    if (dW1) list[n++] = {dP8, I, x8, H, dW1, scales + 5, scales + 0, 1.f};
+    if (dW2) list[n++] = {dout8, H, a8, I, dW2, scales + 4, scales + 3, p->down_mult};
+    for (int i = 0; i < n; ++i) {
+      const int mA = g.mnmajor_u8(list[i].A, M, list[i].rows);
+      const int mB = g.mnmajor_u8(list[i].B, M, list[i].cols);
+      const int oW = g.output(list[i].out, list[i].rows, list[i].cols);
+      Prob& P = g.add(list[i].rows, list[i].cols, M, 0, MMA_N, 1, 2 * BK);
+      P.mapA0 = mA;
+      P.mapB0 = mB;
+      P.mapO[0] = oW;
+      P.sa = list[i].sa;
+      P.sb = list[i].sb;
+      P.mult = list[i].mult;
+    }
+    MLP_TRY((run<EPI_STORE_BF16_F8, true, true>(g, cw, MLP_KERNEL_WGRAD)));
+    if (side) {
+      MLP_TRY(cuda_err(cudaEventRecord(side->join, side->stream)));
+      MLP_TRY(cuda_err(cudaStreamWaitEvent(c.stream, side->join, 0)));
+    }
+  }
+  return MLP_OK;
 }
 
 int mlp_bwd(const mlp_problem_t* p, const void* dout, const void* x, const void* Wg,
@@ -1034,7 +1169,7 @@ const char* mlp_kernel_name(int tag) {
     case MLP_KERNEL_DACT_RECOMPUTE: return "dact_recompute";
     case MLP_KERNEL_RSTD: return "rstd";
     case MLP_KERNEL_RMSNORM_BWD: return "rmsnorm_bwd";
-    case MLP_KERNEL_QUANT: return "quant_e4m3";
+    case MLP_KERNEL_QUANT: return "quant_f8";
     default: return "unknown";
   }
 }

@@ -322,10 +322,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 x bf16 -> fp32.
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format;
 //   bit 15/16 A/B major (0 = K-major, 1 = MN-major); 17-22 N >> 3; 24-28 M >> 4.
-// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format 0),
-// fp32 accumulation, both operands K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
-  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+// Instruction descriptor of kind::f8f6f4: the same fields, with the 8-bit
+// A and B formats (0 = e4m3, 1 = e5m2) in bits 7-9 and 10-12.
+__host__ __device__ constexpr uint32_t idesc_f8(int m, int n, int a_fmt, int b_fmt, bool a_mn,
+                                                bool b_mn) {
+  return (1u << 4) | (static_cast<uint32_t>(a_fmt & 7) << 7) |
+         (static_cast<uint32_t>(b_fmt & 7) << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool a_mn, bool b_mn) {
@@ -411,6 +415,10 @@ __device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float
 // `lo` goes to the lower byte.
 __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
   return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+// The same to e5m2 codes (saturating at +-57344).
+__device__ __forceinline__ uint16_t pack_e5m2x2(float lo, float hi) {
+  return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E5M2));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

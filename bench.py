@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-trace", action="store_true")
     ap.add_argument("--fp8", action="store_true",
-                    help="also time the e4m3 forward (ReLU^2 workloads)")
+                    help="also time the FP8 forward and training step (ReLU^2 workloads)")
     ap.add_argument("--block", action="store_true",
                     help="also time the MLP block with its fused RMS norm and residual add")
     ap.add_argument("--sweep-m", action="store_true",
@@ -495,9 +495,13 @@ def run_ours(args, rank, world, local_rank):
 def fp8_forward(m, w, g, dev, flush, K, peaks):
     """The e4m3 forward (mlp_fp8_fwd) on the workload's weights quantised with
     amax/448 scales and x with the page's static 2^-4, against the bf16
-    inference forward; the codes are made once, outside the timing (the
-    input's quantisation is timed on its own).  The e4m3 peak is the
-    measured bf16 peak times the nominal ratio 2."""
+    inference forward; and the FP8 training step (the forward saving its
+    bf16 preact, then mlp_fp8_bwd with e5m2 gradients: the static 2^-6 for
+    dout, the delayed dpre scale as it settles) against the bf16 one
+    (mlp_fwd saving the preact, mlp_bwd).  The codes of x and the weights
+    are made once, outside the timing (the input's quantisation is timed on
+    its own).  The 8-bit peak is the measured bf16 peak times the nominal
+    ratio 2."""
     import torch
     M, H, I = w.M, w.H, w.I
     prob = m.problem(M, H, I, "relu_sq", w.gate_mult, w.down_mult)
@@ -512,17 +516,46 @@ def fp8_forward(m, w, g, dev, flush, K, peaks):
     # the post scale as the page's delayed one would settle: amax x 1.03 / 448
     pre = (g["x"][:256].float() @ g["Wg"].float().T).clamp(min=0) ** 2
     s_post = float(pre.max()) * w.gate_mult * 1.03 / 448.0
-    scales = torch.tensor([2.0 ** -4, s1, s2, s_post], dtype=torch.float32, device=dev)
-    out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    bf = torch.bfloat16
+    scales = torch.tensor([2.0 ** -4, s1, s2, s_post, 2.0 ** -6, 1.0], dtype=torch.float32,
+                          device=dev)
+    out = torch.empty(M, H, dtype=bf, device=dev)
     a8 = torch.empty(M, I, dtype=torch.uint8, device=dev)
+    pre_s = torch.empty(M, I, dtype=bf, device=dev)
     amax = torch.zeros(1, dtype=torch.float32, device=dev)
+    amax_d = torch.zeros(1, dtype=torch.float32, device=dev)
+    dx = torch.empty(M, H, dtype=bf, device=dev)
+    dW1 = torch.empty(I, H, dtype=bf, device=dev)
+    dW2 = torch.empty(H, I, dtype=bf, device=dev)
     ws8 = m.alloc_workspace(prob, m.MODE_FP8_FWD, dev)
+    wsb8 = m.alloc_workspace(prob, m.MODE_FP8_BWD, dev)
     wsi = m.alloc_workspace(prob, m.MODE_INFER, dev)
+    wsb = m.alloc_workspace(prob, m.MODE_BWD, dev)
     sx_t = scales[:1]
     xq = torch.empty_like(x8)
+
+    def fp8_fwd_train():
+        m.mlp_fp8_fwd(prob, x8, W1_8, W2_8, scales, out, a8, amax, ws=ws8, pre_save=pre_s)
+
+    def fp8_bwd():
+        m.mlp_fp8_bwd(prob, g["dout"], x8, W1_8, W2_8, pre_s, a8, scales, dx, dW1, dW2, amax_d,
+                      ws=wsb8)
+    # the delayed dpre scale as it settles: the last step's amax x 1.25 / 57344
+    fp8_fwd_train()
+    fp8_bwd()
+    torch.cuda.synchronize(dev)
+    scales[5] = float(amax_d.item()) * 1.25 / 57344.0
+
+    def bf16_train():
+        m.mlp_fwd(prob, g["x"], g["Wg"], None, g["Wd"], out, pre_s, ws=wsb)
+        m.mlp_bwd(prob, g["dout"], g["x"], g["Wg"], None, g["Wd"], pre_s, None, dx, dW1, None, dW2,
+                  ws=wsb)
     runs = {"fp8_ms": lambda: m.mlp_fp8_fwd(prob, x8, W1_8, W2_8, scales, out, a8, amax, ws=ws8),
             "bf16_ms": lambda: m.mlp_fwd_infer(prob, g["x"], g["Wg"], None, g["Wd"], out, ws=wsi),
-            "quantize_x_ms": lambda: m.mlp_fp8_quantize(g["x"], sx_t, xq)}
+            "quantize_x_ms": lambda: m.mlp_fp8_quantize(g["x"], sx_t, xq),
+            "fp8_bwd_ms": fp8_bwd,
+            "fp8_train_ms": lambda: (fp8_fwd_train(), fp8_bwd()),
+            "bf16_train_ms": bf16_train}
     res = {}
     for name, fn in runs.items():
         for _ in range(3):
@@ -544,6 +577,11 @@ def fp8_forward(m, w, g, dev, flush, K, peaks):
     res["bf16_tflops"] = f / (res["bf16_ms"] * 1e-3) / 1e12
     res["fp8_peak_tflops"] = peak
     res["fp8_frac"] = res["fp8_tflops"] / peak
+    ft = flops_of(w, "fwd") + flops_of(w, "bwd")
+    res["fp8_train_tflops"] = ft / (res["fp8_train_ms"] * 1e-3) / 1e12
+    res["fp8_bwd_tflops"] = flops_of(w, "bwd") / (res["fp8_bwd_ms"] * 1e-3) / 1e12
+    res["bf16_train_tflops"] = ft / (res["bf16_train_ms"] * 1e-3) / 1e12
+    res["fp8_train_frac"] = res["fp8_train_tflops"] / peak
     res["peak_source"] = "measured bf16 burst x 2 (e4m3 / bf16 nominal ratio)"
     return res
 

@@ -110,7 +110,8 @@ typedef enum {
   MLP_MODE_INFER = 1,
   MLP_MODE_BWD = 2,
   MLP_MODE_BWD_RECOMPUTE = 3,
-  MLP_MODE_FP8_FWD = 4   /* mlp_fp8_fwd: the control block + an e4m3 [M,I] postact */
+  MLP_MODE_FP8_FWD = 4,  /* mlp_fp8_fwd: the control block + an e4m3 [M,I] postact */
+  MLP_MODE_FP8_BWD = 5   /* mlp_fp8_bwd: the control block + e5m2 [M,H] and [M,I] codes */
 } mlp_mode_t;
 
 /* Bytes of workspace a call in `mode` needs for problem `p` (0 on invalid
@@ -231,7 +232,7 @@ int mlp_block_bwd(const mlp_problem_t* p, const mlp_block_t* b, const void* dy, 
                   const float* rstd, void* dx, void* dWg, void* dWu, void* dWd,
                   int fuse_grad_accum, void* ws, size_t ws_bytes, void* stream);
 
-/* ---- FP8 (e4m3) forward of the ReLU^2 MLP ----
+/* ---- FP8 forward and backward of the ReLU^2 MLP ----
  * modded-nanogpt gpt.py trains its ReLU^2 MLP with e4m3 operands and
  * dequant scales (a value is its e4m3 code times the scale; the constants
  * block above ReLUSqrdMLP and the _mlp_* buffers): the input's static scale
@@ -239,8 +240,10 @@ int mlp_block_bwd(const mlp_problem_t* p, const mlp_block_t* b, const void* dy, 
  * the ReLU^2 output (the last step's amax x 1.03 / 448) whose new amax the
  * kernels record.  The quantisation reading (the kernels are not on the
  * page): q = e4m3(fp32(v * fp32(1 / scale))), round to nearest even,
- * saturating at +-448.  This is the forward; the FP8 backward (e5m2
- * gradients) is not built. */
+ * saturating at +-448.  The backward quantises the incoming gradient to
+ * e5m2 with the static FP8_GRAD_SCALE = 2^-6 and the ReLU^2 derivative to
+ * e5m2 with a delayed scale (the last step's amax x 1.25 / 57344), whose new
+ * amax the kernels record; e5m2 saturates at +-57344. */
 
 /* e4m3 codes of n bf16 values (n a multiple of 8; 16-byte aligned src and
  * dst): dst[i] = e4m3(src[i] * (1 / *scale)); with amax non-NULL, the
@@ -254,15 +257,38 @@ int mlp_fp8_quantize(const void* src, long long n, const float* scale, void* dst
  *   a8  = e4m3(a * (1 / s_post)),  *amax_a = max(*amax_a, max a),
  *   out = down_mult * (a8 W2_8^T) * s_post * s2          (bf16 [M,H])
  *   x8 [M,H], W1_8 [I,H], W2_8 [H,I]: e4m3 codes (one byte each, row-major)
- *   scales: device fp32 {sx, s1, s2, s_post}
+ *   scales: device fp32 {sx, s1, s2, s_post} (mlp_fp8_bwd's first four)
  *   a8_save: e4m3 [M,I] out, or NULL (then the workspace holds it)
+ *   pre_save: bf16 [M,I] out (pre rounded to bf16, for mlp_fp8_bwd), or NULL
  *   amax_a: device fp32 scalar, or NULL
  * fc1 and the down projection are tcgen05 kind::f8f6f4 GEMMs (fp32
  * accumulation); the ReLU^2, its re-quantisation and amax run in fc1's
  * epilogue.  Workspace: mlp_workspace_size(p, MLP_MODE_FP8_FWD). */
 int mlp_fp8_fwd(const mlp_problem_t* p, const void* x8, const void* W1_8, const void* W2_8,
-                const float* scales, void* out, void* a8_save, float* amax_a, void* ws,
-                size_t ws_bytes, void* stream);
+                const float* scales, void* out, void* a8_save, void* pre_save, float* amax_a,
+                void* ws, size_t ws_bytes, void* stream);
+
+/* Backward on 8-bit codes, the chain rule through the forward above with
+ * straight-through quantisations (p->act MLP_ACT_RELU_SQ, H and I multiples of 16):
+ *   dout8 = e5m2(dout * (1 / sg)),
+ *   dpre  = gate_mult * down_mult * (dout8 W2_8) * sg * s2 * 2 relu(pre),
+ *   dP8   = e5m2(dpre * (1 / s_dpre)),  *amax_dpre = max(*amax_dpre, max |dpre|),
+ *   dx    = (dP8 W1_8) * s_dpre * s1                          (bf16 [M,H])
+ *   dW1   = (dP8^T x8) * s_dpre * sx                          (bf16 [I,H])
+ *   dW2   = down_mult * (dout8^T a8) * sg * s_post            (bf16 [H,I])
+ *   dout: bf16 [M,H];  pre: the forward's pre_save (bf16 [M,I]);  a8: its e4m3 postact
+ *   x8, W1_8, W2_8: the forward's e4m3 codes
+ *   scales: device fp32 {sx, s1, s2, s_post, sg, s_dpre}
+ *   dx, dW1, dW2: outputs, each NULL when not wanted (then its operands may be NULL)
+ *   amax_dpre: device fp32 scalar, or NULL
+ * All three GEMMs are tcgen05 kind::f8f6f4 (e5m2 x e4m3, fp32 accumulation)
+ * and read W1_8, W2_8, x8 and a8 in their row-major layout (MN-major
+ * operands): no transposed copies.  dx and the grouped weight gradients may
+ * run on a second stream, joined before the call returns.  Workspace:
+ * mlp_workspace_size(p, MLP_MODE_FP8_BWD). */
+int mlp_fp8_bwd(const mlp_problem_t* p, const void* dout, const void* x8, const void* W1_8,
+                const void* W2_8, const void* pre, const void* a8, const float* scales, void* dx,
+                void* dW1, void* dW2, float* amax_dpre, void* ws, size_t ws_bytes, void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mlp_status_string(int status);
@@ -341,7 +367,7 @@ typedef enum {
                                     epilogue postact and dP */
   MLP_KERNEL_RSTD = 8,          /* the block's per-token RMS-norm scale */
   MLP_KERNEL_RMSNORM_BWD = 9,   /* the block's RMS-norm derivative and residual gradient */
-  MLP_KERNEL_QUANT = 10         /* bf16 -> e4m3 quantisation */
+  MLP_KERNEL_QUANT = 10         /* bf16 -> e4m3 / e5m2 quantisation */
 } mlp_kernel_t;
 
 /* on != 0 starts recording, 0 stops (records already taken are kept). */

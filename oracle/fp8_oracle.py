@@ -32,7 +32,9 @@ Readings where the page is silent (the kernels are not on it):
   at +-57344;
 * the backward treats the postact's quantisation as the identity (its
   gradient passes straight through) and takes ReLU^2's derivative from the
-  preact in full precision (the GPU path saves the preact in bf16);
+  preact, recomputed here in full precision unless the saved preact is
+  passed in (the GPU path saves it in bf16; its parity tests pass the same
+  bf16 preact to both sides);
 * the multipliers: ``gate_mult`` scales the ReLU^2 output before it is
   quantised, ``down_mult`` the dequantised output (both 1 on the page).
 """
@@ -100,16 +102,18 @@ def fp8_relu_sq_forward(x8, W1_8, W2_8, sx, s1, s2, s_post, gate_mult=1.0, down_
 
 
 def fp8_relu_sq_backward(dout, x8, W1_8, W2_8, a8, sx, s1, s2, s_post, sg, s_dpre,
-                         gate_mult=1.0, down_mult=1.0):
+                         gate_mult=1.0, down_mult=1.0, pre=None):
     """The backward of ``fp8_relu_sq_forward`` on codes:
     dout8 = e5m2 codes of dout (scale sg); da = down_mult (dout8 W2_8) sg s2;
-    dpre = gate_mult da 2 relu(pre) with pre = (x8 W1_8^T) sx s1;
+    dpre = gate_mult da 2 relu(pre) with pre = (x8 W1_8^T) sx s1 (or the
+    saved preact ``pre`` when given);
     dP8 = e5m2 codes of dpre (scale s_dpre);
     dx = (dP8 W1_8) s_dpre s1;  dW1 = (dP8^T x8) s_dpre sx;
     dW2 = down_mult (dout8^T a8) sg s_post.
     Returns those and amax(|dpre|)."""
     dout8 = quantize_e5m2(dout, sg)
-    pre = (x8 @ W1_8.T) * (sx * s1)
+    if pre is None:
+        pre = (x8 @ W1_8.T) * (sx * s1)
     da = down_mult * (dout8 @ W2_8) * (sg * s2)
     dpre = gate_mult * da * 2.0 * np.maximum(pre, 0.0)
     dP8 = quantize_e5m2(dpre, s_dpre)

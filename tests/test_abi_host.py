@@ -36,7 +36,7 @@ def test_header_declares_the_abi():
                             "mlp_kernel_name", "mlp_set_tile_policy",
                             "mlp_fwd_infer_noalloc", "mlp_set_wait_timeout_ms",
                             "mlp_debug_set_flags", "mlp_block_fwd", "mlp_block_bwd",
-                            "mlp_fp8_quantize", "mlp_fp8_fwd"])
+                            "mlp_fp8_quantize", "mlp_fp8_fwd", "mlp_fp8_bwd"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -139,7 +139,7 @@ def test_fp8_validation_and_workspace(L):
     assert m.mlp_workspace_size(p, m.MODE_FP8_FWD) == 1024 + 2048 * 3072
     ws = 1 << 40
     f = lambda prob, scales=FAKE: L.mlp_fp8_fwd(  # noqa: E731
-        ctypes.byref(prob), FAKE, FAKE, FAKE, scales, FAKE, None, None, FAKE, ws, None)
+        ctypes.byref(prob), FAKE, FAKE, FAKE, scales, FAKE, None, None, None, FAKE, ws, None)
     assert f(m.problem(64, 128, 352)) == -3            # SwiGLU: unsupported
     assert f(m.problem(64, 136, 352, "relu_sq")) == -2  # H % 16
     assert f(p, scales=None) == -1
@@ -148,13 +148,40 @@ def test_fp8_validation_and_workspace(L):
     assert L.mlp_fp8_quantize(FAKE, 16, None, FAKE, None, None) == -1   # no scale
 
 
+def test_fp8_backward_validation_and_workspace(L):
+    p = m.problem(1000, 768, 3072, "relu_sq")
+    r = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    need = 1024 + r(1000 * 768) + r(1000 * 3072)
+    assert m.mlp_workspace_size(p, m.MODE_FP8_BWD) == need
+    ws = 1 << 40
+
+    def b(prob=p, dout=FAKE, x8=FAKE, W1=FAKE, W2=FAKE, pre=FAKE, a8=FAKE, scales=FAKE, dx=FAKE,
+          dW1=FAKE, dW2=FAKE, ws_bytes=ws):
+        return L.mlp_fp8_bwd(ctypes.byref(prob), dout, x8, W1, W2, pre, a8, scales, dx, dW1, dW2,
+                             None, FAKE, ws_bytes, None)
+    assert b(prob=m.problem(64, 128, 352)) == -3             # SwiGLU: unsupported
+    assert b(prob=m.problem(64, 136, 352, "relu_sq")) == -2  # H % 16
+    assert b(scales=None) == -1
+    assert b(dout=None) == -1
+    assert b(dout=FAKE + 8) == -2                 # 16-byte alignment
+    assert b(W1=None) == -1                       # dx needs W1_8
+    assert b(x8=None) == -1                       # dW1 needs x8
+    assert b(a8=None) == -1                       # dW2 needs a8
+    assert b(pre=None) == -1                      # the derivative needs the preact
+    assert b(W2=None) == -1                       # ... and W2_8
+    assert b(ws_bytes=need - 1) == -4
+    # nothing requested: returns before any CUDA call; absent operands of
+    # unrequested outputs are fine
+    assert b(dx=None, dW1=None, dW2=None, x8=None, W1=None, W2=None, pre=None, a8=None) == 0
+
+
 def test_kernel_names_and_empty_trace(L):
     assert m.mlp_kernel_name(2) == "dgated"
     assert m.mlp_kernel_name(6) == "convert"
     assert m.mlp_kernel_name(7) == "dact_recompute"
     assert m.mlp_kernel_name(8) == "rstd"
     assert m.mlp_kernel_name(9) == "rmsnorm_bwd"
-    assert m.mlp_kernel_name(10) == "quant_e4m3"
+    assert m.mlp_kernel_name(10) == "quant_f8"
     assert m.mlp_kernel_name(99) == "unknown"
     assert m.mlp_trace_read() == []  # nothing recorded: no CUDA call is made
 

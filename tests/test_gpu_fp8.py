@@ -1,12 +1,14 @@
-"""GPU parity of the e4m3 (FP8) forward of the ReLU^2 MLP (mlp_fp8_quantize,
-mlp_fp8_fwd) against the fp64 oracle's e4m3 emulation, through the C ABI."""
+"""GPU parity of the FP8 ReLU^2 MLP (mlp_fp8_quantize, mlp_fp8_fwd with its
+e4m3 operands, mlp_fp8_bwd with e5m2 gradients) against the fp64 oracle's
+8-bit emulation, through the C ABI."""
 import numpy as np
 import pytest
 import torch
 
 import activated_mlp_gemms_gb300 as m
 from activated_mlp_gemms_gb300.workloads import make_inputs, to_f64
-from oracle import E4M3_MAX, fp8_relu_sq_forward, quantize, rel_err
+from oracle import (E4M3_MAX, E5M2_MAX, fp8_relu_sq_backward, fp8_relu_sq_forward, quantize,
+                    rel_err)
 
 pytestmark = pytest.mark.gpu
 
@@ -81,3 +83,123 @@ def test_fp8_forward_parity(M, H, I, tile_policy):
     got = to_f64(out)
     assert np.all(np.isfinite(got))
     assert rel_err(got, ref["out"]) <= 2e-2, rel_err(got, ref["out"])
+
+
+# ---------------------------------------------------------------- backward
+def _f8_bytes(values, dtype):
+    """Oracle code values (exactly on the 8-bit grid) -> their bytes on the device."""
+    return torch.tensor(values, dtype=torch.float32).to(dtype).view(torch.uint8).cuda()
+
+
+def _e5m2_codes(t8):
+    return t8.view(torch.float8_e5m2).cpu().to(torch.float64).numpy()
+
+
+def _bwd_case(M, H, I, seed, gate_mult=1.0, down_mult=1.0):
+    """Oracle-made inputs of the backward (e4m3 codes, the bf16 preact, the
+    e4m3 postact) and fp32 scales {sx, s1, s2, s_post, sg, s_dpre}; the
+    delayed scales are taken from this step's amaxes."""
+    t = make_inputs(M, H, I, "relu_sq", seed=seed)
+    xd, W1d, W2d = to_f64(t["x"]), to_f64(t["Wg"]), to_f64(t["Wd"])
+    f32 = lambda v: float(np.float32(v))
+    sx = 2.0 ** -4
+    s1, s2 = f32(np.max(np.abs(W1d)) / E4M3_MAX), f32(np.max(np.abs(W2d)) / E4M3_MAX)
+    xc, W1c, W2c = quantize(xd, sx), quantize(W1d, s1), quantize(W2d, s2)
+    pre = (xc @ W1c.T) * (sx * s1)
+    s_post = f32(max(np.max(np.maximum(pre, 0) ** 2) * gate_mult, 1e-6) * 1.03 / E4M3_MAX)
+    fwd = fp8_relu_sq_forward(xc, W1c, W2c, sx, s1, s2, s_post, gate_mult, down_mult)
+    # the saved preact, in bf16 on both sides
+    pre_bf = torch.tensor(pre, dtype=torch.float32).to(torch.bfloat16)
+    pre_d = to_f64(pre_bf)
+    sg = 2.0 ** -6
+    probe = fp8_relu_sq_backward(to_f64(t["dout"]), xc, W1c, W2c, fwd["a8"], sx, s1, s2, s_post,
+                                 sg, 1.0, gate_mult, down_mult, pre=pre_d)
+    s_dpre = f32(max(probe["amax_dpre"], 1e-30) * 1.25 / E5M2_MAX)
+    scales = [sx, s1, s2, s_post, sg, s_dpre]
+    ref = fp8_relu_sq_backward(to_f64(t["dout"]), xc, W1c, W2c, fwd["a8"], *scales, gate_mult,
+                               down_mult, pre=pre_d)
+    dev = {"dout": t["dout"].cuda(), "x8": _f8_bytes(xc, torch.float8_e4m3fn),
+           "W1_8": _f8_bytes(W1c, torch.float8_e4m3fn), "W2_8": _f8_bytes(W2c, torch.float8_e4m3fn),
+           "pre": pre_bf.cuda(), "a8": _f8_bytes(fwd["a8"], torch.float8_e4m3fn),
+           "scales": torch.tensor(scales, dtype=torch.float32, device="cuda")}
+    return dev, ref
+
+
+def _codes_close(got, ref, max_frac):
+    """8-bit codes decided in fp32 (kernel) and fp64 (oracle): equal except
+    where the two straddle a rounding boundary, and then one step apart."""
+    diff = got != ref
+    assert diff.mean() <= max_frac, diff.mean()
+    if diff.any():
+        step = np.abs(got[diff] - ref[diff]) / np.maximum(np.abs(ref[diff]), 2.0 ** -16)
+        assert np.max(step) <= 0.5, np.max(step)
+
+
+@pytest.mark.parametrize("tile_policy", [1, 2], indirect=True)
+@pytest.mark.parametrize("M,H,I", [(64, 128, 352), (300, 256, 400), (1000, 768, 3072)])
+def test_fp8_backward_parity(M, H, I, tile_policy):
+    dev, ref = _bwd_case(M, H, I, seed=63)
+    dx = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dW1 = torch.full((I, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dW2 = torch.full((H, I), float("nan"), dtype=torch.bfloat16, device="cuda")
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+    ws = m.mlp_fp8_bwd(m.problem(M, H, I, "relu_sq"), dev["dout"], dev["x8"], dev["W1_8"],
+                       dev["W2_8"], dev["pre"], dev["a8"], dev["scales"], dx, dW1, dW2, amax)
+    torch.cuda.synchronize()
+    assert m.mlp_device_status(ws) == 0
+    # the workspace holds the e5m2 codes of dout, then those of dpre
+    off = 1024
+    dout8 = ws[off:off + M * H].view(M, H)
+    off += (M * H + 255) // 256 * 256
+    dP8 = ws[off:off + M * I].view(M, I)
+    assert np.array_equal(_e5m2_codes(dout8), ref["dout8"])
+    _codes_close(_e5m2_codes(dP8), ref["dP8"], 2e-3)
+    assert abs(float(amax.item()) - ref["amax_dpre"]) <= 1e-3 * ref["amax_dpre"]
+    for name, got in (("dx", dx), ("dW1", dW1), ("dW2", dW2)):
+        g = to_f64(got)
+        assert np.all(np.isfinite(g)), name
+        assert rel_err(g, ref[name]) <= 2e-2, (name, rel_err(g, ref[name]))
+
+
+def test_fp8_backward_multipliers_and_partial_outputs():
+    M, H, I = 200, 256, 512
+    dev, ref = _bwd_case(M, H, I, seed=64, gate_mult=0.5, down_mult=2.0)
+    prob = m.problem(M, H, I, "relu_sq", gate_mult=0.5, down_mult=2.0)
+    args = (dev["dout"], dev["x8"], dev["W1_8"], dev["W2_8"], dev["pre"], dev["a8"], dev["scales"])
+    # only dW2: no derivative GEMM, its operands may be absent
+    dW2 = torch.empty(H, I, dtype=torch.bfloat16, device="cuda")
+    m.mlp_fp8_bwd(prob, dev["dout"], None, None, None, None, dev["a8"], dev["scales"], dW2=dW2)
+    torch.cuda.synchronize()
+    assert rel_err(to_f64(dW2), ref["dW2"]) <= 2e-2
+    # only dx
+    dx = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    m.mlp_fp8_bwd(prob, *args, dx=dx)
+    torch.cuda.synchronize()
+    assert rel_err(to_f64(dx), ref["dx"]) <= 2e-2
+    # only dW1
+    dW1 = torch.empty(I, H, dtype=torch.bfloat16, device="cuda")
+    m.mlp_fp8_bwd(prob, *args, dW1=dW1)
+    torch.cuda.synchronize()
+    assert rel_err(to_f64(dW1), ref["dW1"]) <= 2e-2
+
+
+def test_fp8_forward_saves_the_bf16_preact():
+    M, H, I = 300, 256, 400
+    t = make_inputs(M, H, I, "relu_sq", seed=65)
+    xd, W1d, W2d = to_f64(t["x"]), to_f64(t["Wg"]), to_f64(t["Wd"])
+    sx = 2.0 ** -4
+    s1 = float(np.float32(np.max(np.abs(W1d)) / E4M3_MAX))
+    s2 = float(np.float32(np.max(np.abs(W2d)) / E4M3_MAX))
+    xc, W1c, W2c = quantize(xd, sx), quantize(W1d, s1), quantize(W2d, s2)
+    scales = torch.tensor([sx, s1, s2, 1.0], dtype=torch.float32, device="cuda")
+    out = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    pre = torch.full((M, I), float("nan"), dtype=torch.bfloat16, device="cuda")
+    m.mlp_fp8_fwd(m.problem(M, H, I, "relu_sq"), _f8_bytes(xc, torch.float8_e4m3fn),
+                  _f8_bytes(W1c, torch.float8_e4m3fn), _f8_bytes(W2c, torch.float8_e4m3fn), scales,
+                  out, pre_save=pre)
+    torch.cuda.synchronize()
+    ref = (xc @ W1c.T) * (np.float32(sx) * np.float32(s1))
+    got = to_f64(pre)
+    # bf16 rounding of the fp32 value: half an ulp (2^-9 relative), plus the
+    # accumulation order
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6 * np.max(np.abs(ref)))
