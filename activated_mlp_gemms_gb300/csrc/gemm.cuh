@@ -76,17 +76,18 @@ struct EpiTraits {
                               : (EPI == EPI_ACT_FWD || EPI == EPI_DACT ||
                                  EPI == EPI_DACT_RECOMP || EPI == EPI_ACT_FWD_F8) ? 2
                                                                                   : 1;
-  // bytes of a staged 32 x 32 output box: fp32 4096, bf16 2048, 8-bit 1024
-  // (EPI_ACT_FWD_F8's e4m3 box takes the first 1024 B of a 2048-byte slot,
-  // its bf16 preact the second slot)
-  static constexpr int OUT_BYTES = (EPI == EPI_ACCUM_F32) ? 4096 : (EPI == EPI_DGRAD_F8) ? 1024
-                                                                                          : 2048;
+  // bytes of a staged 32 x 32 output box: fp32 4096, bf16 2048 (the 8-bit
+  // epilogues stage their own boxes, below)
+  static constexpr int OUT_BYTES = (EPI == EPI_ACCUM_F32) ? 4096 : 2048;
   // the epilogue reads saved preacts (in0 / in1), fetched ahead of the accumulator
   static constexpr bool DACT = (EPI == EPI_DGATED || EPI == EPI_DACT || EPI == EPI_DGRAD_F8);
   // staged boxes per warp: at most two (a third output reuses the first box
   // once that box's store has read it), so the stage ring keeps 6 stages
   static constexpr int STG_BUFS = NOUT < 2 ? NOUT : 2;
-  static constexpr int STG_WARP = STG_BUFS * OUT_BYTES;
+  // 8-bit outputs: a 32 x 128-byte tile box (+ the bf16 preact's chunk box)
+  static constexpr int STG_WARP = EPI == EPI_ACT_FWD_F8  ? 4096 + 2048
+                                  : EPI == EPI_DGRAD_F8 ? 4096
+                                                        : STG_BUFS * OUT_BYTES;
 };
 
 __device__ __forceinline__ void record_timeout(const Params& p, volatile int* abort_flag) {
@@ -147,8 +148,9 @@ struct EpiUnit {
   float* amax;                // running max of the 8-bit epilogue's output
 };
 
+// deq, inv: the 8-bit epilogues' factors of this problem (read once per kernel)
 template <int EPI>
-__device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P) {
+__device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P, float deq, float inv) {
   EpiUnit U;
 #pragma unroll
   for (int o = 0; o < 3; ++o) U.out[o] = P.mapO[o] >= 0 ? &p.maps[P.mapO[o]] : nullptr;
@@ -164,9 +166,9 @@ __device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P) {
   U.inv = 1.f;
   U.amax = nullptr;
   if constexpr (is_f8(EPI)) {
-    U.deq = *P.sa * *P.sb;
+    U.deq = deq;
     U.mult = P.mult;
-    if (P.sq) U.inv = 1.0f / *P.sq;
+    U.inv = inv;
     U.amax = P.amax;
   }
   return U;
@@ -449,11 +451,35 @@ __device__ __forceinline__ void epi_recomp_dh(const Params& p, const EpiUnit& P,
   }
 }
 
+// 8-bit outputs are staged a whole tile row block at a time: the warp's 32
+// rows x 128 columns (one byte each) in one 32 x 128-byte box with the
+// 128-byte swizzle (16-byte unit u of row r at unit u ^ (r % 8): a warp's
+// row-per-thread 16-byte stores are conflict-free), stored by one TMA store
+// per tile.  Lane r writes bytes [32 c, 32 c + 32) of its row for chunk c.
+__device__ __forceinline__ void stage_f8_chunk(uint32_t buf, int r, int c, const uint32_t (&q)[8]) {
+  const uint32_t rb = buf + static_cast<uint32_t>(r) * 128u;
+  const uint32_t x = static_cast<uint32_t>(r) & 7u;
+  const uint32_t u = 2u * static_cast<uint32_t>(c);
+  st_shared_v4(rb + ((u ^ x) << 4), q[0], q[1], q[2], q[3]);
+  st_shared_v4(rb + (((u + 1u) ^ x) << 4), q[4], q[5], q[6], q[7]);
+}
+
+// Store the staged 8-bit box of output o at (col, row0) as a bulk group.
+__device__ __forceinline__ void store_f8_tile(const EpiUnit& P, const EpiWarp& e, int o,
+                                              uint32_t buf, int col) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (e.lane == 0) {
+    if (P.out[o]) tma_store_2d(P.out[o], buf, col, e.row0);
+    bulk_commit();
+  }
+}
+
 // e4m3 forward of the ReLU^2 MLP: pre = acc * sx * s1, a = mult * relu(pre)^2,
-// a -> e4m3(a * fp32(1 / s_post)) through a 32 x 32-byte box (map 0) and, if
-// requested, pre in bf16 through a 32 x 32 bf16 box (map 1, for the
-// backward); the largest a of the warp's rows goes to *amax (atomic max on
-// the bits of a non-negative float).
+// a -> e4m3(a * fp32(1 / s_post)) (map 0, staged per tile at stg) and, if
+// requested, pre in bf16 through a 32 x 32 bf16 box per chunk (map 1, at
+// stg + 4096; for the backward); the largest a of the warp's rows goes to
+// *amax (atomic max on the bits of a non-negative float).
 template <int ACT>
 __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                            uint32_t tb, int col0, int cb, int ce) {
@@ -462,6 +488,7 @@ __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, co
   const float s = P.mult;
   const bool want_pre = P.out[1] != nullptr;
   const bool row_ok = e.row0 + e.lane < P.M;
+  const uint32_t pbuf = e.stg + 4096u;
   float mx = 0.f;
 #pragma unroll 1
   for (int c = cb; c < ce; c += 32) {
@@ -487,13 +514,16 @@ __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, co
       }
       q[j] = w;
     }
+    // the previous chunk's preact box (and the previous tile's code box)
+    // must have been read before they are overwritten
     staging_acquire(e);
-    const uint32_t rb = e.stg + static_cast<uint32_t>(e.lane) * 32u;
-    st_shared_v4(rb, q[0], q[1], q[2], q[3]);
-    st_shared_v4(rb + 16, q[4], q[5], q[6], q[7]);
-    if (want_pre) stage_bf16(e.stg + 2048, e.lane, pp);
-    flush_chunk<2, 2048, false>(p, P, e, col);
+    stage_f8_chunk(e.stg, e.lane, (c - cb) >> 5, q);
+    if (want_pre) {
+      stage_bf16(pbuf, e.lane, pp);
+      store_box(p, P, e, 1, pbuf, col);
+    }
   }
+  if (col0 + cb < P.N) store_f8_tile(P, e, 0, e.stg, col0 + cb);
   if (P.amax) {
     if (!row_ok) mx = 0.f;
 #pragma unroll
@@ -504,52 +534,49 @@ __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, co
 
 // e5m2 derivative of the 8-bit ReLU^2 MLP: dpre = deq * acc * 2 * relu(P)
 // with P the saved bf16 preact (in0), dpre -> e5m2(dpre * fp32(1 / *sq))
-// through a 32 x 32-byte box (map 0); the largest |dpre| of the warp's rows
-// goes to *amax.  P's chunk c+1 is loaded while chunk c is computed (the
-// caller loads chunk `cb` before waiting for the accumulator).
+// (map 0, staged per tile); the largest |dpre| of the warp's rows goes to
+// *amax.  The caller loads P's first chunk before waiting for the
+// accumulator; the other three chunks of the tile are loaded here before the
+// first is used (the producer has prefetched the tile into L2).
 __device__ __forceinline__ void epi_dgrad_f8(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                              uint32_t tb, int col0, int cb, int ce,
                                              uint4 (&pg)[4]) {
   const float dq2 = 2.f * P.mult * P.deq;
   const float inv = P.inv;
   const int row = e.row0 + e.lane;
+  uint4 pr[3][4], unused[4];
+#pragma unroll
+  for (int i = 0; i < 3; ++i) dact_load<false>(P, row, col0 + cb + 32 * (i + 1), pr[i], unused);
   float mx = 0.f;
-#pragma unroll 1
-  for (int c = cb; c < ce; c += 32) {
-    const int col = col0 + c;
+#pragma unroll
+  for (int ci = 0; ci < 4; ++ci) {
+    const int col = col0 + cb + 32 * ci;
     if (col >= P.N) break;
-    uint4 ng[4], nu[4];
-    if (c + 32 < ce) dact_load<false>(P, row, col + 32, ng, nu);
     uint32_t z[32];
     __syncwarp();
-    tmem_ld32(tb + c, z);
+    tmem_ld32(tb + cb + 32 * ci, z);
     tmem_wait_ld();
     uint32_t q[8];
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-      const uint32_t gw[4] = {pg[v].x, pg[v].y, pg[v].z, pg[v].w};
+      const uint4 g4 = ci == 0 ? pg[v] : pr[ci - 1][v];
+      const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
       q[2 * v] = 0;
       q[2 * v + 1] = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float2 pr = unpack_bf16x2(gw[j]);
-        const float d0 = dq2 * __uint_as_float(z[8 * v + 2 * j]) * fmaxf(pr.x, 0.f);
-        const float d1 = dq2 * __uint_as_float(z[8 * v + 2 * j + 1]) * fmaxf(pr.y, 0.f);
+        const float2 pv = unpack_bf16x2(gw[j]);
+        const float d0 = dq2 * __uint_as_float(z[8 * v + 2 * j]) * fmaxf(pv.x, 0.f);
+        const float d1 = dq2 * __uint_as_float(z[8 * v + 2 * j + 1]) * fmaxf(pv.y, 0.f);
         mx = fmaxf(mx, fmaxf(fabsf(d0), fabsf(d1)));
         q[2 * v + (j >> 1)] |= static_cast<uint32_t>(pack_e5m2x2(d0 * inv, d1 * inv))
                                << (16 * (j & 1));
       }
     }
-    staging_acquire(e);
-    const uint32_t rb = e.stg + static_cast<uint32_t>(e.lane) * 32u;
-    st_shared_v4(rb, q[0], q[1], q[2], q[3]);
-    st_shared_v4(rb + 16, q[4], q[5], q[6], q[7]);
-    flush_chunk<1, 1024, false>(p, P, e, col);
-    if (c + 32 < ce) {
-#pragma unroll
-      for (int v = 0; v < 4; ++v) pg[v] = ng[v];
-    }
+    if (ci == 0) staging_acquire(e);  // the previous tile's box has been read
+    stage_f8_chunk(e.stg, e.lane, ci, q);
   }
+  if (col0 + cb < P.N) store_f8_tile(P, e, 0, e.stg, col0 + cb);
   if (P.amax) {
     if (row >= P.M) mx = 0.f;
 #pragma unroll
@@ -646,6 +673,10 @@ struct UnitLoads {
   int m0;                 // this CTA's first A row (K-major) / column (MN-major)
   int n0;                 // this CTA's first B row
   int kb0;                // k-blocks of segment 0
+  // derivative epilogues: the saved inputs' tile (this CTA's rows), prefetched into L2
+  const CUtensorMap* i0;  // nullptr: none
+  const CUtensorMap* i1;
+  int icol;               // the tile's first column
 };
 
 template <int EPI, int CG>
@@ -665,6 +696,15 @@ __device__ __forceinline__ UnitLoads unit_loads(const Params& p, const Prob& P, 
     L.b0 = &p.maps[P.mapB0];
     L.b1 = &p.maps[P.mapB1];
     L.n0 = w.tn * MMA_N + static_cast<int>(rank) * (MMA_N / CG);
+  }
+  L.i0 = nullptr;
+  L.i1 = nullptr;
+  L.icol = w.tn * MMA_N;
+  if constexpr (EpiTraits<EPI>::DACT) {
+    if (L.m0 < P.M) {  // rows past the output have no inputs to fetch
+      if (P.mapI0 >= 0) L.i0 = &p.maps[P.mapI0];
+      if (P.mapI1 >= 0) L.i1 = &p.maps[P.mapI1];
+    }
   }
   return L;
 }
@@ -824,6 +864,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
           if (done) break;
           const Work w = decode_unit(p, unit);
           const UnitLoads L = unit_loads<EPI, CG>(p, p.prob[w.prob], w, rank);
+          if constexpr (EpiTraits<EPI>::DACT) {
+            // the epilogue reads this tile's saved inputs a tile or two later
+            if (L.i0) tma_prefetch_l2_2d(L.i0, L.icol, L.m0);
+            if (L.i1) tma_prefetch_l2_2d(L.i1, L.icol, L.m0);
+          }
           for (int kb = w.kb_begin; kb < w.kb_end && ok; ++kb) {
             if (!mbar_wait<PAIR>(bar_s(EMPTY + stage), phase ^ 1u, lim, abort_flag)) {
               ok = false;
@@ -853,6 +898,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
           if (v < 0) break;
           const Work w = decode_unit(p, v);
           const UnitLoads L = unit_loads<EPI, CG>(p, p.prob[w.prob], w, rank);
+          if constexpr (EpiTraits<EPI>::DACT) {
+            if (L.i0) tma_prefetch_l2_2d(L.i0, L.icol, L.m0);
+            if (L.i1) tma_prefetch_l2_2d(L.i1, L.icol, L.m0);
+          }
           const uint32_t full_lead = lead(bar_s(FULL));
           for (int kb = w.kb_begin; kb < w.kb_end && ok; ++kb) {
             if (!mbar_wait<PAIR>(bar_s(EMPTY + stage), phase ^ 1u, lim, abort_flag)) {
@@ -986,6 +1035,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
     uint32_t sphase = 0;
     int acc = 0;
     uint32_t aphase = 0;
+    // 8-bit epilogues: each problem's dequant factor *sa * *sb and output
+    // quantisation factor 1 / *sq (device scalars), read once
+    float f8_deq[MAX_PROBS], f8_inv[MAX_PROBS];
+#pragma unroll
+    for (int i = 0; i < MAX_PROBS; ++i) {
+      f8_deq[i] = 1.f;
+      f8_inv[i] = 1.f;
+      if constexpr (is_f8(EPI)) {
+        if (i < p.nprob) {
+          f8_deq[i] = *p.prob[i].sa * *p.prob[i].sb;
+          if (p.prob[i].sq) f8_inv[i] = 1.0f / *p.prob[i].sq;
+        }
+      }
+    }
     while (true) {
       if (!mbar_wait<PAIR>(bar_s(SFULL + slot), sphase, lim, abort_flag)) {
         record_timeout(p, abort_flag);
@@ -1000,7 +1063,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
       if (unit < 0) break;
       const Work w = decode_unit(p, unit);
-      const EpiUnit P = epi_unit<EPI>(p, p.prob[w.prob]);
+      const int pi = w.prob;
+      const EpiUnit P = epi_unit<EPI>(p, p.prob[pi],
+                                      pi == 0 ? f8_deq[0] : pi == 1 ? f8_deq[1] : f8_deq[2],
+                                      pi == 0 ? f8_inv[0] : pi == 1 ? f8_inv[1] : f8_inv[2]);
       e.row0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
       e.rows_ok = e.row0 < P.M;
       e.rs = (P.rstd && e.row0 + lane < P.M) ? P.rstd[e.row0 + lane] : 1.f;

@@ -60,6 +60,8 @@ struct Prob {
   int mapA1, mapB1;       // segment 1 (EPI_GATED_FWD: mapB1 = the up weight;
                           // EPI_DACT_RECOMP: B is K-major in segment 0, MN-major in 1)
   int ld;                 // row pitch (elements) of the epilogue's outputs and inputs
+  int mapI0, mapI1;       // derivative epilogues: maps of in0 / in1 with boxes {256, 128}
+                          // whose tiles the producer prefetches into L2 (-1: none)
   int mapO[3];            // tensor maps of the epilogue's outputs (-1: output not written)
   void* out0;
   void* out1;

@@ -229,12 +229,21 @@ struct Gemm {
     if (!make_map(&p.maps[nmaps], ptr, MN, K, MN, 2 * BK, 2 * BK, 2)) ok = false;
     return nmaps++;
   }
-  // e4m3 epilogue output [rows, cols], 32 x 32-byte boxes, no swizzle.
+  // bf16 input [rows, cols] of a derivative epilogue, boxes {256, 128}: the
+  // producer prefetches each tile's rows into L2 ahead of the epilogue
+  int prefetch_map(const void* ptr, int rows, int cols) {
+    if (!ptr) return -1;
+    if (nmaps >= MAX_MAPS) { ok = false; return -1; }
+    if (!make_map(&p.maps[nmaps], ptr, cols, rows, cols, MMA_N, BM, 0, CU_TENSOR_MAP_SWIZZLE_NONE))
+      ok = false;
+    return nmaps++;
+  }
+  // 8-bit epilogue output [rows, cols]: one 32-row x 128-byte box per warp
+  // and tile, 128-byte swizzle.
   int output_u8(void* ptr, int rows, int cols) {
     if (!ptr) return -1;
     if (nmaps >= MAX_MAPS) { ok = false; return -1; }
-    if (!make_map(&p.maps[nmaps], ptr, cols, rows, cols, 32, 32, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
-      ok = false;
+    if (!make_map(&p.maps[nmaps], ptr, cols, rows, cols, 128, 32, 2)) ok = false;
     return nmaps++;
   }
   // Epilogue output [rows, cols] (row pitch cols), stored in 32 x 32 boxes;
@@ -266,6 +275,7 @@ struct Gemm {
     p.total_units += P.units;
     P.ld = N;
     P.mapO[0] = P.mapO[1] = P.mapO[2] = -1;
+    P.mapI0 = P.mapI1 = -1;
     return P;
   }
   // B rows per K-major box: a CTA stages 256 / cg of the 256 B rows
@@ -715,11 +725,15 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     const int oG = g.output(G, M, I);
     const int oU = gated(p) ? g.output(U, M, I) : -1;
     const int oA = g.output(a_out, M, I);
+    const int iG = g.prefetch_map(G, M, I);
+    const int iU = gated(p) ? g.prefetch_map(U, M, I) : -1;
     Prob& P = g.add(M, I, H, 0, MMA_N);
     P.mapA0 = mA;
     P.mapB0 = mB;
     P.in0 = G;
     P.in1 = U;
+    P.mapI0 = iG;
+    P.mapI1 = iU;
     P.rstd = blk ? blk->rstd : nullptr;  // dG, dU (dP) come out times 1/r
     // gated: dG, dU, a;  non-gated: dP, a
     P.mapO[0] = oG;
@@ -998,11 +1012,13 @@ int mlp_fp8_bwd(const mlp_problem_t* p, const void* dout, const void* x8, const 
     const int mA = g.kmajor_a_u8(dout8, M, H);
     const int mB = g.mnmajor_u8(W2_8, H, I);
     const int oP = g.output_u8(dP8, M, I);
+    const int iP = g.prefetch_map(pre, M, I);
     Prob& P = g.add(M, I, H, 0, MMA_N, 1, 2 * BK);
     P.mapA0 = mA;
     P.mapB0 = mB;
     P.mapO[0] = oP;
     P.in0 = pre;
+    P.mapI0 = iP;
     P.sa = scales + 4;  // sg
     P.sb = scales + 2;  // s2
     P.sq = scales + 5;  // s_dpre
