@@ -725,15 +725,13 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     const int oG = g.output(G, M, I);
     const int oU = gated(p) ? g.output(U, M, I) : -1;
     const int oA = g.output(a_out, M, I);
-    const int iG = g.prefetch_map(G, M, I);
-    const int iU = gated(p) ? g.prefetch_map(U, M, I) : -1;
+    // (no L2 prefetch of G/U here: with the long K of these GEMMs the
+    // epilogue keeps up, and the prefetch made the kernel 5-7 % slower)
     Prob& P = g.add(M, I, H, 0, MMA_N);
     P.mapA0 = mA;
     P.mapB0 = mB;
     P.in0 = G;
     P.in1 = U;
-    P.mapI0 = iG;
-    P.mapI1 = iU;
     P.rstd = blk ? blk->rstd : nullptr;  // dG, dU (dP) come out times 1/r
     // gated: dG, dU, a;  non-gated: dP, a
     P.mapO[0] = oG;
