@@ -49,6 +49,8 @@ def parse():
                     help="also time the MLP block with its fused RMS norm and residual add")
     ap.add_argument("--sweep-m", action="store_true",
                     help="also time the inference forward at decode-sized token counts")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count M (small cases for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args()
@@ -194,6 +196,9 @@ def run_ours(args, rank, world, local_rank):
     from activated_mlp_gemms_gb300.workloads import WORKLOADS, workload_inputs
 
     w = WORKLOADS[args.workload]
+    if args.tokens > 0:
+        import dataclasses
+        w = dataclasses.replace(w, M=args.tokens)
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     from activated_mlp_gemms_gb300 import _build
@@ -312,7 +317,7 @@ def run_ours(args, rank, world, local_rank):
         d = kernels[dom]
         peak = float(peaks["bf16_tflops"])
         ach = d["tflops"]
-        traffic = load_traffic(dom, w.name)
+        traffic = load_traffic(dom, w.name) if w == WORKLOADS[w.name] else None
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": (ach / peak) if ach else None, "traffic": traffic,
                 "peak_source": f"{peaks_src} bf16 burst ({'MEASURED_PEAKS.json' if peaks_src == 'measured' else 'recipe fallback'})"}
@@ -724,6 +729,9 @@ def oracle_sample(w, seconds, steps=1):
 def run_reference(args, rank, world):
     from activated_mlp_gemms_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.tokens > 0:
+        import dataclasses
+        w = dataclasses.replace(w, M=args.tokens)
     K, W = args.steps, args.warmup
     budget = 150.0  # seconds for the whole reference run
     per_step = max(0.5, budget / max(1, K + W))
