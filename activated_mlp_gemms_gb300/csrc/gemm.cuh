@@ -478,7 +478,7 @@ __device__ __forceinline__ void store_f8_tile(const EpiUnit& P, const EpiWarp& e
 // e4m3 forward of the ReLU^2 MLP: pre = acc * sx * s1, a = mult * relu(pre)^2,
 // a -> e4m3(a * fp32(1 / s_post)) (map 0, staged per tile at stg) and, if
 // requested, pre in bf16 through a 32 x 32 bf16 box per chunk (map 1, at
-// stg + 4096; for the backward); the largest a of the warp's rows goes to
+// stg + 4096; for the backward); the largest |a| of the warp's rows goes to
 // *amax (atomic max on the bits of a non-negative float).
 template <int ACT>
 __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, const EpiWarp& e,
@@ -509,7 +509,7 @@ __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, co
         pp[2 * j + h] = pack_bf16x2(z0, z1);
         const float p0 = fmaxf(z0, 0.f), p1 = fmaxf(z1, 0.f);
         const float a0 = s * p0 * p0, a1 = s * p1 * p1;
-        mx = fmaxf(mx, fmaxf(a0, a1));
+        mx = fmaxf(mx, fmaxf(fabsf(a0), fabsf(a1)));
         w |= static_cast<uint32_t>(pack_e4m3x2(a0 * inv, a1 * inv)) << (16 * h);
       }
       q[j] = w;

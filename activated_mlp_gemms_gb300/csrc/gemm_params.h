@@ -34,7 +34,7 @@ enum Epi : int {
   // 8-bit operands (tcgen05 kind::f8f6f4; e4m3 or e5m2 per operand, Params::f8_formats)
   // with the problem's dequant factor deq = mult * *sa * *sb:
   EPI_ACT_FWD_F8 = 7,     // pre = deq'*acc (deq' = *sa * *sb), a = mult*relu(pre)^2 ->
-                          // e4m3(a / *sq) (map 0), optional bf16 pre (map 1), amax(a) -> *amax
+                          // e4m3(a / *sq) (map 0), optional bf16 pre (map 1), amax|a| -> *amax
   EPI_STORE_BF16_F8 = 8,  // D = bf16(deq * acc)
   EPI_DGRAD_F8 = 9        // dpre = deq*acc*2*relu(P) (in0 = P, bf16) -> e5m2(dpre / *sq)
                           // (map 0), amax|dpre| -> *amax

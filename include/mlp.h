@@ -254,7 +254,7 @@ int mlp_fp8_quantize(const void* src, long long n, const float* scale, void* dst
 
 /* Forward on e4m3 codes (p->act must be MLP_ACT_RELU_SQ, H and I multiples of 16):
  *   pre = (x8 W1_8^T) * sx * s1,   a = gate_mult * relu(pre)^2,
- *   a8  = e4m3(a * (1 / s_post)),  *amax_a = max(*amax_a, max a),
+ *   a8  = e4m3(a * (1 / s_post)),  *amax_a = max(*amax_a, max |a|),
  *   out = down_mult * (a8 W2_8^T) * s_post * s2          (bf16 [M,H])
  *   x8 [M,H], W1_8 [I,H], W2_8 [H,I]: e4m3 codes (one byte each, row-major)
  *   scales: device fp32 {sx, s1, s2, s_post} (mlp_fp8_bwd's first four)

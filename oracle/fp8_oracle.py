@@ -93,12 +93,13 @@ def weight_scale(W):
 def fp8_relu_sq_forward(x8, W1_8, W2_8, sx, s1, s2, s_post, gate_mult=1.0, down_mult=1.0):
     """The forward on e4m3 codes: pre = (x8 W1_8^T) sx s1,
     a = gate_mult relu(pre)^2, a8 = quantize(a, s_post),
-    out = down_mult (a8 W2_8^T) s_post s2.  Returns out, a, a8 and amax(a)."""
+    out = down_mult (a8 W2_8^T) s_post s2.  Returns out, a, a8 and amax(|a|)
+    (the magnitude a delayed scale must cover; a >= 0 unless gate_mult < 0)."""
     pre = (x8 @ W1_8.T) * (sx * s1)
     a = gate_mult * np.maximum(pre, 0.0) ** 2
     a8 = quantize(a, s_post)
     out = down_mult * (a8 @ W2_8.T) * (s_post * s2)
-    return {"out": out, "a": a, "a8": a8, "amax_a": float(np.max(a)) if a.size else 0.0}
+    return {"out": out, "a": a, "a8": a8, "amax_a": float(np.max(np.abs(a))) if a.size else 0.0}
 
 
 def fp8_relu_sq_backward(dout, x8, W1_8, W2_8, a8, sx, s1, s2, s_post, sg, s_dpre,

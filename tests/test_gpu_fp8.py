@@ -203,3 +203,131 @@ def test_fp8_forward_saves_the_bf16_preact():
     # bf16 rounding of the fp32 value: half an ulp (2^-9 relative), plus the
     # accumulation order
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6 * np.max(np.abs(ref)))
+
+
+def test_fp8_negative_gate_mult_and_amax_of_magnitudes():
+    """gate_mult < 0 flips the postact's sign: its e4m3 codes are negative and
+    the recorded amax is the largest |a|."""
+    M, H, I = 300, 256, 400
+    t = make_inputs(M, H, I, "relu_sq", seed=66)
+    xd, W1d, W2d = to_f64(t["x"]), to_f64(t["Wg"]), to_f64(t["Wd"])
+    f32 = lambda v: float(np.float32(v))  # noqa: E731
+    sx = 2.0 ** -4
+    s1, s2 = f32(np.max(np.abs(W1d)) / E4M3_MAX), f32(np.max(np.abs(W2d)) / E4M3_MAX)
+    xc, W1c, W2c = quantize(xd, sx), quantize(W1d, s1), quantize(W2d, s2)
+    pre = (xc @ W1c.T) * (sx * s1)
+    gm = -0.75
+    s_post = f32(np.max(np.maximum(pre, 0) ** 2) * abs(gm) * 1.03 / E4M3_MAX)
+    scales = torch.tensor([sx, s1, s2, s_post], dtype=torch.float32, device="cuda")
+    out = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    a8 = torch.empty(M, I, dtype=torch.uint8, device="cuda")
+    amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+    m.mlp_fp8_fwd(m.problem(M, H, I, "relu_sq", gate_mult=gm), _f8_bytes(xc, torch.float8_e4m3fn),
+                  _f8_bytes(W1c, torch.float8_e4m3fn), _f8_bytes(W2c, torch.float8_e4m3fn), scales,
+                  out, a8, amax)
+    torch.cuda.synchronize()
+    ref = fp8_relu_sq_forward(xc, W1c, W2c, sx, s1, s2, s_post, gate_mult=gm)
+    got = _codes(a8)
+    assert np.all(got <= 0) and np.any(got < 0)
+    diff = got != ref["a8"]
+    assert diff.mean() < 2e-3, diff.mean()
+    assert abs(float(amax.item()) - ref["amax_a"]) <= 1e-4 * ref["amax_a"]
+    assert rel_err(to_f64(out), ref["out"]) <= 2e-2
+
+
+def test_fp8_training_step_in_a_cuda_graph():
+    """The FP8 forward (saving the preact) and backward captured into a CUDA
+    graph, after a direct call has created the backward's second stream:
+    replays give the direct call's outputs bitwise (no split-K, no
+    order-dependent accumulation; the amaxes are maxima)."""
+    M, H, I = 1000, 768, 3072
+    dev, ref_o = _bwd_case(M, H, I, seed=67)
+    prob = m.problem(M, H, I, "relu_sq")
+    bf = torch.bfloat16
+    pre = torch.empty(M, I, dtype=bf, device="cuda")
+    a8 = torch.empty(M, I, dtype=torch.uint8, device="cuda")
+    ws8 = m.alloc_workspace(prob, m.MODE_FP8_FWD)
+    wsb = m.alloc_workspace(prob, m.MODE_FP8_BWD)
+
+    def bufs():
+        return {"out": torch.empty(M, H, dtype=bf, device="cuda"),
+                "dx": torch.empty(M, H, dtype=bf, device="cuda"),
+                "dW1": torch.empty(I, H, dtype=bf, device="cuda"),
+                "dW2": torch.empty(H, I, dtype=bf, device="cuda"),
+                "amax_a": torch.zeros(1, dtype=torch.float32, device="cuda"),
+                "amax_d": torch.zeros(1, dtype=torch.float32, device="cuda")}
+
+    def step(r):
+        m.mlp_fp8_fwd(prob, dev["x8"], dev["W1_8"], dev["W2_8"], dev["scales"], r["out"], a8,
+                      r["amax_a"], ws=ws8, pre_save=pre)
+        m.mlp_fp8_bwd(prob, dev["dout"], dev["x8"], dev["W1_8"], dev["W2_8"], pre, a8,
+                      dev["scales"], r["dx"], r["dW1"], r["dW2"], r["amax_d"], ws=wsb)
+    ref, got = bufs(), bufs()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(ref)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(got)
+    for _ in range(2):
+        for k, v in got.items():
+            v.fill_(0.0 if k.startswith("amax") else float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for k in ref:
+            assert torch.equal(got[k], ref[k]), k
+    # and the direct call is the oracle's backward (its own inputs, same scales)
+    for name in ("dx", "dW1", "dW2"):
+        assert rel_err(to_f64(ref[name]), ref_o[name]) <= 2e-2, name
+
+
+def test_fp8_delayed_scaling_loop():
+    """Three training steps with the page's delayed-scale refresh between
+    them (post: amax x 1.03 / 448; dpre: amax x 1.25 / 57344): every step's
+    recorded amaxes match the oracle's; from a deliberately wrong first
+    scale (1.0) the second and third steps run on the refreshed scales,
+    nothing saturates, and the outputs match the oracle run with the same
+    scales."""
+    M, H, I = 512, 256, 512
+    t = make_inputs(M, H, I, "relu_sq", seed=68)
+    xd, W1d, W2d, dout = to_f64(t["x"]), to_f64(t["Wg"]), to_f64(t["Wd"]), t["dout"].cuda()
+    f32 = lambda v: float(np.float32(v))  # noqa: E731
+    sx = 2.0 ** -4
+    s1, s2 = f32(np.max(np.abs(W1d)) / E4M3_MAX), f32(np.max(np.abs(W2d)) / E4M3_MAX)
+    xc, W1c, W2c = quantize(xd, sx), quantize(W1d, s1), quantize(W2d, s2)
+    x8, W1_8, W2_8 = (_f8_bytes(v, torch.float8_e4m3fn) for v in (xc, W1c, W2c))
+    # the oracle's own saved preact, in bf16 (the kernels save theirs)
+    pre_o = to_f64(torch.tensor((xc @ W1c.T) * (sx * s1), dtype=torch.float64).to(torch.bfloat16))
+    prob = m.problem(M, H, I, "relu_sq")
+    bf = torch.bfloat16
+    scales = torch.tensor([sx, s1, s2, 1.0, 2.0 ** -6, 1.0], dtype=torch.float32, device="cuda")
+    out = torch.empty(M, H, dtype=bf, device="cuda")
+    pre = torch.empty(M, I, dtype=bf, device="cuda")
+    a8 = torch.empty(M, I, dtype=torch.uint8, device="cuda")
+    dx = torch.empty(M, H, dtype=bf, device="cuda")
+    amax_a = torch.zeros(1, dtype=torch.float32, device="cuda")
+    amax_d = torch.zeros(1, dtype=torch.float32, device="cuda")
+    for step in range(3):
+        amax_a.zero_()
+        amax_d.zero_()
+        m.mlp_fp8_fwd(prob, x8, W1_8, W2_8, scales, out, a8, amax_a, pre_save=pre)
+        m.mlp_fp8_bwd(prob, dout, x8, W1_8, W2_8, pre, a8, scales, dx=dx, amax_dpre=amax_d)
+        torch.cuda.synchronize()
+        sc = [float(v) for v in scales.cpu().numpy()]
+        fw = fp8_relu_sq_forward(xc, W1c, W2c, *sc[:4])
+        bw = fp8_relu_sq_backward(to_f64(dout), xc, W1c, W2c, fw["a8"], *sc, pre=pre_o)
+        assert abs(float(amax_a.item()) - fw["amax_a"]) <= 1e-3 * fw["amax_a"]
+        assert abs(float(amax_d.item()) - bw["amax_dpre"]) <= 1e-3 * bw["amax_dpre"]
+        if step > 0:  # scales from the recorded maxima: nothing saturates
+            assert np.max(np.abs(_codes(a8))) <= E4M3_MAX
+            assert np.max(np.abs(fw["a"])) / sc[3] < E4M3_MAX
+            assert rel_err(to_f64(out), fw["out"]) <= 2e-2
+            assert rel_err(to_f64(dx), bw["dx"]) <= 2e-2
+        # the page's refresh: last step's amax times the headroom over the
+        # format's max (taken from the oracle's amaxes, which the kernels'
+        # recorded ones match above, so that both sides get the same scales)
+        scales[3] = f32(fw["amax_a"] * 1.03 / E4M3_MAX)
+        scales[5] = f32(bw["amax_dpre"] * 1.25 / E5M2_MAX)

@@ -57,6 +57,10 @@ def test_fp8_forward_exact_on_representable_inputs():
     assert np.array_equal(fw["a8"], F8.e4m3(a / s_post))
     assert np.array_equal(fw["out"], (fw["a8"] @ W2.T) * s_post * s2)
     assert fw["amax_a"] == np.max(a)
+    # a negative gate_mult flips the postact's sign; the amax is of |a|
+    fn = F8.fp8_relu_sq_forward(x8, W1, W2, sx, s1, s2, s_post, gate_mult=-0.5)
+    assert np.array_equal(fn["a8"], -F8.e4m3(0.5 * a / s_post))
+    assert fn["amax_a"] == 0.5 * np.max(a)
 
 
 def test_fp8_forward_close_to_the_bf16_definition():
