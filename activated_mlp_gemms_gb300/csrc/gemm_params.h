@@ -124,6 +124,19 @@ cudaError_t launch_f32_to_bf16(const float* src, void* dst, long long n, cudaStr
 cudaError_t launch_quant_f8(const void* src, long long n, const float* scale, void* dst,
                             float* amax, int fmt, cudaStream_t stream, bool pdl);
 
+// Decode-sized forward (M <= DECODE_MAX_M) on the CUDA cores: the gate/up
+// (or fc1) pass with its activation (a, and G/U or P when given), and the
+// down projection out = a Wd^T.  `act` is a device activation (Act).  Each
+// CTA stages the M token rows of its K (H, then I) whole in shared memory:
+// M * K * 2 <= DECODE_MAX_TOKEN_BYTES.
+constexpr int DECODE_MAX_M = 2;
+constexpr int DECODE_MAX_TOKEN_BYTES = 100 * 1024;
+cudaError_t launch_decode_act(const void* x, const void* Wg, const void* Wu, void* a, void* G,
+                              void* U, int M, int H, int I, int act, bool gated, float s,
+                              cudaStream_t stream, bool pdl);
+cudaError_t launch_decode_down(const void* a, const void* Wd, void* out, int M, int H, int I,
+                               cudaStream_t stream, bool pdl);
+
 // Per-token RMS-norm scale rstd[m] = 1 / sqrt(mean_h x^2 + eps), x bf16 [M, H].
 cudaError_t launch_rstd(const void* x, float* rstd, int M, int H, float eps, cudaStream_t stream,
                         bool pdl);

@@ -166,6 +166,15 @@ int device_act(int act) {
 
 std::atomic<int> g_tile_policy{0};  // 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles
 
+// The forward of at most DECODE_MAX_M tokens runs on the CUDA cores (a
+// weight stream) unless a tile policy forces the tensor-core path, or its
+// token rows do not fit a CTA's shared memory.
+bool decode_path(const mlp_problem_t* p) {
+  const long long k = p->H > p->I ? p->H : p->I;
+  return p->M <= DECODE_MAX_M && (long long)p->M * k * 2 <= DECODE_MAX_TOKEN_BYTES &&
+         g_tile_policy.load() == 0;
+}
+
 // CTA-group size for a GEMM whose output has `rows` rows: pairs (256-row
 // tiles) unless the output fits one 128-row tile.
 int pick_cg(int rows) {
@@ -649,6 +658,18 @@ int forward(const mlp_problem_t* p, const void* x, const void* Wg, const void* W
   Call c;
   MLP_TRY(begin_call(c, ws, stream));
   void* a = static_cast<char*>(ws) + CTRL_BYTES;
+  if (!blk && decode_path(p)) {
+    // a few tokens: two weight-streaming passes on the CUDA cores
+    const bool pdl0 = c.pdl();
+    MLP_TRY(traced(MLP_KERNEL_GATE_UP, c.stream, [&] {
+      return launch_decode_act(x, Wg, Wu, a, G_save, U_save, p->M, p->H, p->I, device_act(p->act),
+                               gated(p), p->gate_mult * p->down_mult, c.stream, pdl0);
+    }));
+    const bool pdl1 = c.pdl();
+    return traced(MLP_KERNEL_DOWN, c.stream, [&] {
+      return launch_decode_down(a, Wd, out, p->M, p->H, p->I, c.stream, pdl1);
+    });
+  }
   const int split = bf16_split(p->M, p->H, split_k_of(p, mode));
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + split_offset(p, mode));
   if (split > 1)

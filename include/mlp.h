@@ -134,7 +134,12 @@ size_t mlp_workspace_size(const mlp_problem_t* p, int mode);
  *   G_save bf16 [M,I]  out, optional: the gate preact x Wg^T (non-gated: x W1^T)
  *   U_save bf16 [M,I]  out, optional: the up preact x Wu^T (NULL when non-gated)
  * Pass G_save/U_save as NULL for the recompute mode (save only x).  The
- * bf16 values written to `out` are bitwise identical to mlp_fwd_infer's. */
+ * bf16 values written to `out` are bitwise identical to mlp_fwd_infer's.
+ * With one or two tokens (decode; M * max(H, I) * 2 <= 100 KiB), unless a
+ * tile policy is set (below), the forward streams the weights on the CUDA
+ * cores instead of the tensor cores: each warp reads whole weight rows
+ * front to back and accumulates the M dot products in fp32 (two kernels,
+ * no split-K region used). */
 int mlp_fwd(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu,
             const void* Wd, void* out, void* G_save, void* U_save,
             void* ws, size_t ws_bytes, void* stream);
@@ -330,6 +335,8 @@ int mlp_fwd_infer_noalloc(const mlp_problem_t* p, const void* x, const void* Wg,
  *     256 x 256 tiles computed by a CTA pair (tcgen05 cta_group::2), the
  *     others 128 x 256 tiles on one CTA;
  * 1 = always single-CTA tiles;  2 = always CTA-pair tiles.
+ * Policies 1 and 2 also keep forwards of one or two tokens on the tensor
+ * cores (policy 0 streams their weights on the CUDA cores).
  * Process-wide; returns MLP_ERR_INVALID_ARG for other values.  Results of
  * the two tile shapes agree to rounding (same fp32 accumulation order). */
 int mlp_set_tile_policy(int policy);
