@@ -46,7 +46,8 @@ def test_quantize_codes_are_bit_exact(scale):
 
 
 @pytest.mark.parametrize("tile_policy", [1, 2], indirect=True)
-@pytest.mark.parametrize("M,H,I", [(64, 128, 352), (300, 256, 400), (1000, 768, 3072)])
+@pytest.mark.parametrize("M,H,I", [(1, 128, 256), (7, 256, 400), (64, 128, 352), (300, 256, 400),
+                                   (1000, 768, 3072)])
 def test_fp8_forward_parity(M, H, I, tile_policy):
     t = make_inputs(M, H, I, "relu_sq", seed=62)
     x, W1, W2 = t["x"].cuda(), t["Wg"].cuda(), t["Wd"].cuda()
@@ -75,7 +76,7 @@ def test_fp8_forward_parity(M, H, I, tile_policy):
     # fp64 one; they may differ where the two straddle a rounding boundary,
     # and then by one code step
     diff = got_a8 != ref["a8"]
-    assert diff.mean() < 2e-3, diff.mean()
+    assert diff.sum() <= max(1, 2e-3 * diff.size), diff.mean()
     if diff.any():
         step = np.abs(got_a8[diff] - ref["a8"][diff]) / np.maximum(np.abs(ref["a8"][diff]), 2.0 ** -9)
         assert np.max(step) <= 0.25
@@ -129,14 +130,15 @@ def _codes_close(got, ref, max_frac):
     """8-bit codes decided in fp32 (kernel) and fp64 (oracle): equal except
     where the two straddle a rounding boundary, and then one step apart."""
     diff = got != ref
-    assert diff.mean() <= max_frac, diff.mean()
+    assert diff.sum() <= max(1, max_frac * diff.size), diff.mean()
     if diff.any():
         step = np.abs(got[diff] - ref[diff]) / np.maximum(np.abs(ref[diff]), 2.0 ** -16)
         assert np.max(step) <= 0.5, np.max(step)
 
 
 @pytest.mark.parametrize("tile_policy", [1, 2], indirect=True)
-@pytest.mark.parametrize("M,H,I", [(64, 128, 352), (300, 256, 400), (1000, 768, 3072)])
+@pytest.mark.parametrize("M,H,I", [(1, 128, 256), (7, 256, 400), (64, 128, 352), (300, 256, 400),
+                                   (1000, 768, 3072)])
 def test_fp8_backward_parity(M, H, I, tile_policy):
     dev, ref = _bwd_case(M, H, I, seed=63)
     dx = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device="cuda")
