@@ -844,24 +844,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       bool ok = true;
       // testing hook: publish no work, so the consumers' bounded waits expire
       const bool publish_nothing = leader && (p.debug_flags & 1);
+      bool first_pub = true;
       while (ok && !publish_nothing) {
         if (leader) {
-          // fetch the next unit early; publish this one to the pair's rings
-          const bool done = unit >= p.total_units;
-          const int next = done ? unit : ncl + atomicAdd(p.counter, 1);
-          if (!mbar_wait<PAIR>(bar_s(SEMPTY + slot), sphase ^ 1u, lim, abort_flag)) {
-            ok = false;
-            break;
+          // Publishes unit v (-1: no more work) to the pair's rings.  A unit
+          // is published while the previous one is still being loaded (at
+          // its middle k-block), so that the peer and the consumers find it
+          // in the ring when they get there.  Kernels with an MN-major A
+          // (the weight gradients) publish each unit as they start loading
+          // it instead: measured, the early publication made them 1-3 %
+          // slower while it made the others 1-7 % faster.
+          auto publish = [&](int v) -> bool {
+            if (!mbar_wait<PAIR>(bar_s(SEMPTY + slot), sphase ^ 1u, lim, abort_flag)) return false;
+            sched[slot] = v;
+            if constexpr (PAIR) {
+              st_shared_cluster_u32(peer(smem_u32(sched + slot)), static_cast<uint32_t>(v));
+              mbar_arrive_cluster(peer(bar_s(SFULL + slot)));
+            }
+            mbar_arrive(bar_s(SFULL + slot));
+            if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
+            return true;
+          };
+          constexpr bool EARLY_PUB = !A_MN;
+          if (!EARLY_PUB || first_pub) {
+            first_pub = false;
+            if (!publish(unit < p.total_units ? unit : -1)) {
+              ok = false;
+              break;
+            }
           }
-          const int v = done ? -1 : unit;
-          sched[slot] = v;
-          if constexpr (PAIR) {
-            st_shared_cluster_u32(peer(smem_u32(sched + slot)), static_cast<uint32_t>(v));
-            mbar_arrive_cluster(peer(bar_s(SFULL + slot)));
-          }
-          mbar_arrive(bar_s(SFULL + slot));
-          if (++slot == SCHED_SLOTS) { slot = 0; sphase ^= 1u; }
-          if (done) break;
+          if (unit >= p.total_units) break;
+          // the next unit, fetched now and needed when it is published
+          const int next = ncl + atomicAdd(p.counter, 1);
+          bool published = !EARLY_PUB;
           const Work w = decode_unit(p, unit);
           const UnitLoads L = unit_loads<EPI, CG>(p, p.prob[w.prob], w, rank);
           if constexpr (EpiTraits<EPI>::DACT) {
@@ -884,7 +899,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
             load_stage<EPI, A_MN, B_MN, CG>(L, seg, kc, sA, sA + C::A_BYTES, full, pol);
             ++issued;
             if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+            if (!published && kb == w.kb_begin + (w.kb_end - w.kb_begin) / 2) {
+              if (!publish(next < p.total_units ? next : -1)) {
+                ok = false;
+                break;
+              }
+              published = true;
+            }
           }
+          if (ok && !published && !publish(next < p.total_units ? next : -1)) ok = false;
           unit = next;
         } else {
           // peer of a pair: take units from the ring the leader fills
