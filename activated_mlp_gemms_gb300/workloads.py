@@ -114,3 +114,20 @@ def closed_form_inputs(M, H, I, act="swiglu"):
     gated = act in GATED_ACTS
     return {"x": x.to(bf), "Wg": w(I, H, 0).to(bf), "Wu": w(I, H, 1).to(bf) if gated else None,
             "Wd": w(H, I, 2).to(bf), "dout": dout.to(bf)}
+
+
+def fp8_closed_form_codes(M, H, I):
+    """Deterministic 8-bit inputs with no RNG for the stored FP8 fixture:
+    integer codes (exact in e4m3) x8[m,h] = (3m + 5h + 1) mod 9 - 4,
+    W1_8[i,h] = (5i + 3h + 2) mod 7 - 3, W2_8[h,i] = (7h + 2i + 1) mod 5 - 2,
+    and dout[m,h] = ((m + 3h) mod 11 - 5) / 8 (exact in bf16).  Returns
+    float64 tensors of the codes' values and a bf16 dout."""
+    m = torch.arange(M, dtype=torch.float64)[:, None]
+    h = torch.arange(H, dtype=torch.float64)[None, :]
+    i_r = torch.arange(I, dtype=torch.float64)[:, None]
+    h_r = torch.arange(H, dtype=torch.float64)[:, None]
+    i_c = torch.arange(I, dtype=torch.float64)[None, :]
+    return {"x8": torch.remainder(3 * m + 5 * h + 1, 9) - 4,
+            "W1_8": torch.remainder(5 * i_r + 3 * h + 2, 7) - 3,
+            "W2_8": torch.remainder(7 * h_r + 2 * i_c + 1, 5) - 2,
+            "dout": ((torch.remainder(m + 3 * h, 11) - 5) / 8).to(torch.bfloat16)}

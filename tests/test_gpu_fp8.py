@@ -333,3 +333,56 @@ def test_fp8_delayed_scaling_loop():
         # recorded ones match above, so that both sides get the same scales)
         scales[3] = f32(fw["amax_a"] * 1.03 / E4M3_MAX)
         scales[5] = f32(bw["amax_dpre"] * 1.25 / E5M2_MAX)
+
+
+def test_fp8_golden_closed_form():
+    """The stored closed-form fixture (integer codes, power-of-two scales,
+    written by the oracle alone): every product and sum of fc1 and of the
+    derivative is exact in fp32, so the e4m3 postact's and the e5m2 codes
+    and both amaxes match bit for bit; out, dx, dW1, dW2 within the bf16
+    tolerance."""
+    import json
+    import os
+    from activated_mlp_gemms_gb300.workloads import fp8_closed_form_codes
+    path = os.path.join(os.path.dirname(__file__), "golden", "fp8_closed_form.json")
+    with open(path) as f:
+        g = json.load(f)
+    sc = g["scales"]
+    for tile_policy in (1, 2):
+        m.mlp_set_tile_policy(tile_policy)
+        try:
+            for c in g["cases"]:
+                M, H, I = c["M"], c["H"], c["I"]
+                t = fp8_closed_form_codes(M, H, I)
+                x8, W1_8, W2_8 = (_f8_bytes(t[k].numpy(), torch.float8_e4m3fn)
+                                  for k in ("x8", "W1_8", "W2_8"))
+                scales = torch.tensor([sc["sx"], sc["s1"], sc["s2"], sc["s_post"], sc["sg"],
+                                       c["s_dpre"]], dtype=torch.float32, device="cuda")
+                prob = m.problem(M, H, I, "relu_sq", c["gate_mult"], c["down_mult"])
+                bf = torch.bfloat16
+                out = torch.full((M, H), float("nan"), dtype=bf, device="cuda")
+                a8 = torch.empty(M, I, dtype=torch.uint8, device="cuda")
+                amax_a = torch.zeros(1, dtype=torch.float32, device="cuda")
+                m.mlp_fp8_fwd(prob, x8, W1_8, W2_8, scales, out, a8, amax_a)
+                pre = torch.tensor(c["pre_bf16"], dtype=torch.float64).to(bf).cuda()
+                dx = torch.full((M, H), float("nan"), dtype=bf, device="cuda")
+                dW1 = torch.full((I, H), float("nan"), dtype=bf, device="cuda")
+                dW2 = torch.full((H, I), float("nan"), dtype=bf, device="cuda")
+                amax_d = torch.zeros(1, dtype=torch.float32, device="cuda")
+                ws = m.mlp_fp8_bwd(prob, t["dout"].cuda(), x8, W1_8, W2_8, pre, a8, scales, dx,
+                                   dW1, dW2, amax_d)
+                torch.cuda.synchronize()
+                assert m.mlp_device_status(ws) == 0
+                assert np.array_equal(_codes(a8), np.array(c["a8"]))
+                off = 1024
+                dout8 = ws[off:off + M * H].view(M, H)
+                off += (M * H + 255) // 256 * 256
+                dP8 = ws[off:off + M * I].view(M, I)
+                assert np.array_equal(_e5m2_codes(dout8), np.array(c["dout8"]))
+                assert np.array_equal(_e5m2_codes(dP8), np.array(c["dP8"]))
+                assert float(amax_a.item()) == c["amax_a"]
+                assert float(amax_d.item()) == c["amax_dpre"]
+                for name, got in (("out", out), ("dx", dx), ("dW1", dW1), ("dW2", dW2)):
+                    assert rel_err(to_f64(got), np.array(c[name])) <= 2e-2, name
+        finally:
+            m.mlp_set_tile_policy(0)
