@@ -121,3 +121,35 @@ def fp8_relu_sq_backward(dout, x8, W1_8, W2_8, a8, sx, s1, s2, s_post, sg, s_dpr
     return {"dx": (dP8 @ W1_8) * (s_dpre * s1), "dW1": (dP8.T @ x8) * (s_dpre * sx),
             "dW2": down_mult * (dout8.T @ a8) * (sg * s_post), "dout8": dout8, "dP8": dP8,
             "dpre": dpre, "amax_dpre": float(np.max(np.abs(dpre))) if dpre.size else 0.0}
+
+
+def fp8_relu_sq_sampled(dout, x8, W1_8, W2_8, sx, s1, s2, s_post, sg, s_dpre, rows, units,
+                        gate_mult=1.0, down_mult=1.0, round_pre=None):
+    """``fp8_relu_sq_forward`` and ``fp8_relu_sq_backward`` restricted to the
+    token rows ``rows`` (out and dx) and the intermediate units ``units``
+    (rows of dW1 and columns of dW2, each still reduced over all tokens):
+    the same definition, evaluated on the subsets it needs.  The backward's
+    saved preact is ``round_pre(pre)`` (the identity when None; the GPU path
+    saves it rounded to bf16)."""
+    rp = round_pre if round_pre is not None else (lambda v: v)
+    dout8 = quantize_e5m2(dout, sg)
+
+    def pre_of(xs, ws):
+        return (xs @ ws.T) * (sx * s1)
+
+    def a8_of(pre):
+        return quantize(gate_mult * np.maximum(pre, 0.0) ** 2, s_post)
+
+    def dP8_of(dout8_rows, W2_cols, pre):
+        da = down_mult * (dout8_rows @ W2_cols) * (sg * s2)
+        return quantize_e5m2(gate_mult * da * 2.0 * np.maximum(rp(pre), 0.0), s_dpre)
+
+    # token rows: every unit of these tokens
+    pre_r = pre_of(x8[rows], W1_8)
+    out = down_mult * (a8_of(pre_r) @ W2_8.T) * (s_post * s2)
+    dx = (dP8_of(dout8[rows], W2_8, pre_r) @ W1_8) * (s_dpre * s1)
+    # intermediate units: every token of these units
+    pre_u = pre_of(x8, W1_8[units])
+    dW1 = (dP8_of(dout8, W2_8[:, units], pre_u).T @ x8) * (s_dpre * sx)
+    dW2 = down_mult * (dout8.T @ a8_of(pre_u)) * (sg * s_post)
+    return {"out": out, "dx": dx, "dW1": dW1, "dW2": dW2}

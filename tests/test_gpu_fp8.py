@@ -386,3 +386,60 @@ def test_fp8_golden_closed_form():
                     assert rel_err(to_f64(got), np.array(c[name])) <= 2e-2, name
         finally:
             m.mlp_set_tile_policy(0)
+
+
+def test_fp8_full_size_sampled():
+    """The ReLU^2 workload at full size (49152 x 768 x 3072) through the FP8
+    forward (saving the preact) and backward, in the launch configuration
+    the benchmark times; parity on sampled token rows (out, dx) and sampled
+    intermediate units (rows of dW1, columns of dW2, each reduced over all
+    tokens), computed by the oracle on its own codes and preacts."""
+    from activated_mlp_gemms_gb300.workloads import WORKLOADS, workload_inputs
+    from oracle import fp8_relu_sq_sampled, quantize_e5m2
+    w = WORKLOADS["nanogpt_relu_sq"]
+    M, H, I = w.M, w.H, w.I
+    t = workload_inputs(w)
+    xd, W1d, W2d, doutd = (to_f64(t[k]) for k in ("x", "Wg", "Wd", "dout"))
+    f32 = lambda v: float(np.float32(v))  # noqa: E731
+    sx = 2.0 ** -4
+    s1, s2 = f32(np.max(np.abs(W1d)) / E4M3_MAX), f32(np.max(np.abs(W2d)) / E4M3_MAX)
+    xc, W1c, W2c = quantize(xd, sx), quantize(W1d, s1), quantize(W2d, s2)
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(M, size=48, replace=False))
+    rows[0], rows[-1] = 0, M - 1
+    units = np.sort(rng.choice(I, size=24, replace=False))
+    units[0], units[-1] = 0, I - 1
+
+    def round_pre(v):  # the saved preact's bf16 rounding
+        return to_f64(torch.tensor(v, dtype=torch.float64).to(torch.bfloat16))
+    # delayed scales as they settle, from the oracle's own sampled rows
+    pre_r = (xc[rows] @ W1c.T) * (sx * s1)
+    s_post = f32(np.max(np.maximum(pre_r, 0) ** 2) * 1.03 / E4M3_MAX)
+    sg = 2.0 ** -6
+    da = (quantize_e5m2(doutd[rows], sg) @ W2c) * (sg * s2)
+    s_dpre = f32(np.max(np.abs(da * 2 * np.maximum(round_pre(pre_r), 0))) * 1.25 / E5M2_MAX)
+    scales = [sx, s1, s2, s_post, sg, s_dpre]
+    ref = fp8_relu_sq_sampled(doutd, xc, W1c, W2c, *scales, rows, units, round_pre=round_pre)
+
+    prob = m.problem(M, H, I, "relu_sq")
+    bf = torch.bfloat16
+    x8, W1_8, W2_8 = (_f8_bytes(v, torch.float8_e4m3fn) for v in (xc, W1c, W2c))
+    sc = torch.tensor(scales, dtype=torch.float32, device="cuda")
+    out = torch.full((M, H), float("nan"), dtype=bf, device="cuda")
+    pre = torch.empty(M, I, dtype=bf, device="cuda")
+    a8 = torch.empty(M, I, dtype=torch.uint8, device="cuda")
+    dx = torch.full((M, H), float("nan"), dtype=bf, device="cuda")
+    dW1 = torch.full((I, H), float("nan"), dtype=bf, device="cuda")
+    dW2 = torch.full((H, I), float("nan"), dtype=bf, device="cuda")
+    m.mlp_fp8_fwd(prob, x8, W1_8, W2_8, sc, out, a8, pre_save=pre)
+    ws = m.mlp_fp8_bwd(prob, t["dout"].cuda(), x8, W1_8, W2_8, pre, a8, sc, dx, dW1, dW2)
+    torch.cuda.synchronize()
+    assert m.mlp_device_status(ws) == 0
+    r_t, u_t = torch.as_tensor(rows), torch.as_tensor(units)
+    errs = {"out": rel_err(to_f64(out[r_t]), ref["out"]),
+            "dx": rel_err(to_f64(dx[r_t]), ref["dx"]),
+            "dW1": rel_err(to_f64(dW1[u_t]), ref["dW1"]),
+            "dW2": rel_err(to_f64(dW2[:, u_t]), ref["dW2"])}
+    assert all(e <= 2e-2 for e in errs.values()), errs
+    for v in (out, dx, dW1, dW2):
+        assert torch.isfinite(v.float()).all()

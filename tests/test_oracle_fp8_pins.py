@@ -152,3 +152,30 @@ def test_planted_missing_relu_grad_factor_is_caught():
     good = F8.fp8_relu_sq_backward(dout, x8, W1, W2, a8, 1.0, 1.0, 1.0, 1.0, 1.0, 1.0)["dx"]
     bad = ((dout @ W2) * np.maximum(x8 @ W1.T, 0)) @ W1  # the factor 2 dropped
     assert not np.array_equal(good, bad)
+
+
+def test_fp8_sampled_equals_the_full_definition():
+    """The sampled oracle (token rows, intermediate units) is the full
+    forward and backward restricted to those rows and units, bit for bit."""
+    rng = np.random.default_rng(57)
+    M, H, I = 24, 32, 40
+    x = rng.standard_normal((M, H))
+    W1 = rng.standard_normal((I, H)) / np.sqrt(H)
+    W2 = rng.standard_normal((H, I)) / np.sqrt(I)
+    dout = rng.standard_normal((M, H))
+    sx, s1, s2 = 2.0 ** -4, F8.weight_scale(W1), F8.weight_scale(W2)
+    x8, W1_8, W2_8 = F8.quantize(x, sx), F8.quantize(W1, s1), F8.quantize(W2, s2)
+    s_post, sg, s_dpre = 2.0 ** -9, 2.0 ** -6, 2.0 ** -12
+    gm, dm = 0.75, 1.5
+    round_pre = lambda v: np.round(v * 64) / 64  # noqa: E731  (any fixed rounding)
+    fw = F8.fp8_relu_sq_forward(x8, W1_8, W2_8, sx, s1, s2, s_post, gm, dm)
+    pre = (x8 @ W1_8.T) * (sx * s1)
+    bw = F8.fp8_relu_sq_backward(dout, x8, W1_8, W2_8, fw["a8"], sx, s1, s2, s_post, sg, s_dpre,
+                                 gm, dm, pre=round_pre(pre))
+    rows, units = np.array([0, 5, 23]), np.array([1, 17, 39])
+    sm = F8.fp8_relu_sq_sampled(dout, x8, W1_8, W2_8, sx, s1, s2, s_post, sg, s_dpre, rows, units,
+                                gm, dm, round_pre=round_pre)
+    assert np.array_equal(sm["out"], fw["out"][rows])
+    assert np.array_equal(sm["dx"], bw["dx"][rows])
+    assert np.array_equal(sm["dW1"], bw["dW1"][units])
+    assert np.array_equal(sm["dW2"], bw["dW2"][:, units])
