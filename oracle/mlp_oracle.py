@@ -300,3 +300,22 @@ def flops(M, H, I, act, mode):
     if mode == "bwd_recompute":
         return (16 if g else 10) * mhi
     raise ValueError(mode)
+
+
+def block_sampled(rows, cols, dy, x, Wg, Wu, Wd, act="relu_sq", gate_mult=1.0, down_mult=1.0,
+                  resid_lambda=1.0, post_lambda=1.0, eps=2.0 ** -7, dW_prev=None):
+    """``block_forward`` / ``block_backward`` restricted to the token rows
+    ``rows`` (y, dx) and the intermediate units ``cols`` (rows of dWg/dWu,
+    columns of dWd, each summed over all tokens).  The norm is per token, so
+    the rows' outputs need only their own rows of ``x`` and ``dy``; the units'
+    gradients need every token's normalised input."""
+    rows = np.asarray(rows)
+    n, r = rms_norm(x, eps)
+    tr = sampled_token_rows(rows, post_lambda * dy, n, Wg, Wu, Wd, act, gate_mult, down_mult)
+    nr, dn = n[rows], tr["dx"]
+    y = resid_lambda * x[rows] + post_lambda * tr["out"]
+    dx = resid_lambda * dy[rows] + (dn - nr * np.mean(dn * nr, axis=-1, keepdims=True)) / r[rows]
+    cu = sampled_inter_units(cols, post_lambda * dy, n, Wg, Wu, Wd, act, gate_mult, down_mult,
+                             dW_prev=dW_prev)
+    return {"y": y, "dx": dx, **cu}
+

@@ -111,3 +111,36 @@ def test_block_output_over_its_input():
     got = _run(t, M, H, I, act, 1.0, 1.0, False, inplace=True)
     ref = _oracle(t, act, 1.0, 1.0, False)
     assert rel_err(to_f64(got["y"]), ref["y"]) <= TOL_BF16
+
+
+@pytest.mark.parametrize("name", ["llama7b_swiglu", "nanogpt_relu_sq"])
+def test_block_full_size_sampled(name):
+    """The block at the workloads' full sizes (saved preacts; the ReLU^2
+    workload with fp32 gradient accumulation): parity on sampled token rows
+    (y, dx) and sampled intermediate units (rows of dWg/dWu, columns of dWd,
+    each reduced over all tokens), computed by the oracle."""
+    from activated_mlp_gemms_gb300.workloads import WORKLOADS, workload_inputs
+    from oracle import block_sampled
+    w = WORKLOADS[name]
+    t = workload_inputs(w)
+    got = _run(t, w.M, w.H, w.I, w.act, w.gate_mult, w.down_mult, w.fuse_grad_accum)
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(w.M, size=48, replace=False))
+    rows[0], rows[-1] = 0, w.M - 1
+    cols = np.sort(rng.choice(w.I, size=24, replace=False))
+    cols[0], cols[-1] = 0, w.I - 1
+    a = {k: to_f64(v) if v is not None else None for k, v in t.items()}
+    prev = ({"dWg": a["dWg_prev"], "dWu": a.get("dWu_prev"), "dWd": a["dWd_prev"]}
+            if w.fuse_grad_accum else None)
+    ref = block_sampled(rows, cols, a["dout"], a["x"], a["Wg"], a["Wu"], a["Wd"], w.act,
+                        w.gate_mult, w.down_mult, **LAMBDAS, dW_prev=prev)
+    r_t, c_t = torch.as_tensor(rows), torch.as_tensor(cols)
+    errs = {"y": rel_err(to_f64(got["y"][r_t]), ref["y"]),
+            "dx": rel_err(to_f64(got["dx"][r_t]), ref["dx"]),
+            "dWg": rel_err(to_f64(got["dWg"][c_t]), ref["dWg"]),
+            "dWd": rel_err(to_f64(got["dWd"][:, c_t]), ref["dWd"])}
+    if w.gated:
+        errs["dWu"] = rel_err(to_f64(got["dWu"][c_t]), ref["dWu"])
+    tol_w = TOL_F32 if w.fuse_grad_accum else TOL_BF16
+    for k, e in errs.items():
+        assert e <= (tol_w if k.startswith("dW") else TOL_BF16), (name, errs)

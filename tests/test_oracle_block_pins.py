@@ -156,3 +156,27 @@ def test_planted_rms_norm_mistakes_are_caught(monkeypatch):
 
     bad = wrong(dy, x, Wg, Wu, Wd, "relu_sq", **KW)["dx"]
     assert O.rel_err(bad, good) > 1e-3
+
+
+@pytest.mark.parametrize("act", ["swiglu", "relu_sq"])
+def test_block_sampled_equals_the_full_definition(act):
+    """The sampled block oracle is the full block restricted to the chosen
+    token rows and intermediate units."""
+    rng = np.random.default_rng(58)
+    M, H, I = 9, 6, 7
+    x = rng.standard_normal((M, H))
+    dy = rng.standard_normal((M, H))
+    Wg = rng.standard_normal((I, H))
+    Wu = rng.standard_normal((I, H)) if act == "swiglu" else None
+    Wd = rng.standard_normal((H, I))
+    kw = dict(gate_mult=1.125, down_mult=2.0, resid_lambda=1.1 ** 0.5, post_lambda=0.8, eps=0.01)
+    fw = O.block_forward(x, Wg, Wu, Wd, act, **kw)
+    bw = O.block_backward(dy, x, Wg, Wu, Wd, act, **kw)
+    rows, cols = [0, 4, 8], [1, 6]
+    sm = O.block_sampled(rows, cols, dy, x, Wg, Wu, Wd, act, **kw)
+    np.testing.assert_allclose(sm["y"], fw["y"][rows], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(sm["dx"], bw["dx"][rows], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(sm["dWg"], bw["dWg"][cols], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(sm["dWd"], bw["dWd"][:, cols], rtol=1e-13, atol=1e-13)
+    if act == "swiglu":
+        np.testing.assert_allclose(sm["dWu"], bw["dWu"][cols], rtol=1e-13, atol=1e-13)
