@@ -129,41 +129,90 @@ def load_traffic(kernel, workload):
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples SM clocks and throttle reasons during a timed region.
+
+    One `nvidia-smi --query-gpu=timestamp,... -lms 20` process takes a sample
+    every 20 ms from before the region starts until just after it ends, when
+    it is stopped with SIGINT (nvidia-smi then exits normally).  Samples are
+    attributed to the region by their own timestamps, so output buffering
+    does not matter; the ones inside the region and the first one after it
+    are kept.  If the loop yields nothing, one single query is taken."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
-    def __init__(self, index):
+    def __init__(self, index, exe="nvidia-smi"):
         self.index = index
+        self.exe = exe
+        self.lines = []  # (sample time, fields) as read
         self.samples = []
-        self._stop = threading.Event()
-        self._t = threading.Thread(target=self._run, daemon=True)
+        self._proc = None
+        self._t = None
+        self._first = threading.Event()
+        self.t0 = self.t1 = None
 
-    def _one(self):
+    @staticmethod
+    def _stamp(s):
+        import datetime
         try:
-            r = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+            return datetime.datetime.strptime(s.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def _reader(self):
+        for line in self._proc.stdout:
+            f = [x.strip() for x in line.strip().split(",")]
+            if len(f) >= 9:
+                t = self._stamp(f[0])
+                if t is not None:
+                    self.lines.append((t, f[1:]))
+                    self._first.set()
+
+    def _single(self):
+        try:
+            r = subprocess.run([self.exe, "-i", str(self.index), "--query-gpu=" + self.FIELDS,
                                 "--format=csv,noheader,nounits"], capture_output=True, text=True,
                                timeout=10)
             if r.returncode == 0 and r.stdout.strip():
-                self.samples.append([x.strip() for x in r.stdout.strip().split(",")])
-        except Exception:
+                return [x.strip() for x in r.stdout.strip().splitlines()[0].split(",")]
+        except (OSError, subprocess.SubprocessError):
             pass
-
-    def _run(self):
-        while not self._stop.is_set():
-            self._one()
-            self._stop.wait(0.05)
+        return None
 
     def __enter__(self):
-        self._t.start()
+        try:
+            self._proc = subprocess.Popen(
+                [self.exe, "-i", str(self.index), "--query-gpu=timestamp," + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._reader, daemon=True)
+            self._t.start()
+            self._first.wait(1.0)  # start once samples flow (or after 1 s if output is buffered)
+        except OSError:
+            self._proc = None
+        self.t0 = time.time()
         return self
 
     def __exit__(self, *a):
-        self._stop.set()
-        self._t.join(timeout=15)
+        import signal
+        self.t1 = time.time()
+        if self._proc is not None:
+            time.sleep(3 * self.PERIOD_MS / 1000.0)  # let one sample past the region be taken
+            self._proc.send_signal(signal.SIGINT)
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+                self._proc.wait(timeout=5)
+            self._t.join(timeout=5)
+        inside = [f for t, f in self.lines if self.t0 <= t <= self.t1]
+        after = [f for t, f in sorted(self.lines, key=lambda x: x[0]) if t > self.t1][:1]
+        self.samples = inside + after
         if not self.samples:
-            self._one()
+            one = self._single()
+            if one:
+                self.samples = [one]
 
     def summary(self):
         if not self.samples:
@@ -318,8 +367,11 @@ def run_ours(args, rank, world, local_rank):
         peak = float(peaks["bf16_tflops"])
         ach = d["tflops"]
         traffic = load_traffic(dom, w.name) if w == WORKLOADS[w.name] else None
+        # the burst peak; the sustained one (the power-capped GEMM loop) beside it
+        sus = float(peaks.get("bf16_tflops_sustained", 0.0)) or None
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": (ach / peak) if ach else None, "traffic": traffic,
+                "peak_sustained": sus, "frac_of_sustained": (ach / sus) if (ach and sus) else None,
                 "peak_source": f"{peaks_src} bf16 burst ({'MEASURED_PEAKS.json' if peaks_src == 'measured' else 'recipe fallback'})"}
     clocks = sampler.summary()
 
@@ -689,6 +741,21 @@ def infer_m_sweep(m, w, g, dev, flush, peaks):
 
 # ------------------------------------------------------------ CPU oracle
 
+def oracle_threads():
+    """Threads the oracle's numpy BLAS calls run on."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except ImportError:
+        pass
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            return int(os.environ[v])
+    return len(os.sched_getaffinity(0))
+
+
 def oracle_sample(w, seconds, steps=1):
     """Time the fp64 oracle on a bounded token sample of the workload."""
     import numpy as np
@@ -719,8 +786,7 @@ def oracle_sample(w, seconds, steps=1):
     f = flops_of(type("W", (), {"M": n, "H": w.H, "I": w.I, "gated": w.gated})(), "fwd") + \
         flops_of(type("W", (), {"M": n, "H": w.H, "I": w.I, "gated": w.gated})(), "bwd")
     tpt = sum(times) / len(times)
-    cores = os.cpu_count()
-    return {"value": f / tpt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": f / tpt / 1e12, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
             "sample": f"{n} of {w.M} tokens (full H={w.H}, I={w.I}), oracle forward+backward in "
                       f"numpy fp64, {len(times)} pass(es), {tpt:.2f} s each",
             "seconds_per_pass": tpt, "tokens": n}, tpt
@@ -760,7 +826,7 @@ def run_reference(args, rank, world):
     W_ = type("W", (), {"M": n, "H": w.H, "I": w.I, "gated": w.gated})()
     f = flops_of(W_, "fwd") + flops_of(W_, "bwd")
     val = f / sec / 1e12
-    cpu = {"value": val, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+    cpu = {"value": val, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
            "sample": f"{n} of {w.M} tokens per step (full H={w.H}, I={w.I}), oracle "
                      f"forward+backward in numpy fp64"}
     return {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,

@@ -1,0 +1,102 @@
+"""Host-side pieces of bench.py that need no GPU: the clock sampler (against
+a fake nvidia-smi) and the reference arm's JSON line (the fp64 oracle on a
+small workload)."""
+import json
+import os
+import subprocess
+import sys
+import time
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+FAKE = r'''#!{python}
+import datetime, sys, time
+args = sys.argv[1:]
+sm, state = {sm}, "{state}"
+row = [str(sm), "2070", "1000.5", "0x0", "Not Active", "Not Active", "Not Active", state]
+if "-lms" in args:
+    period = int(args[args.index("-lms") + 1]) / 1000.0
+    try:
+        while True:
+            ts = datetime.datetime.now().strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+            sys.stdout.write(", ".join([ts] + row) + "\n")
+            {flush}
+            time.sleep(period)
+    except KeyboardInterrupt:
+        sys.exit(0)
+print(", ".join(row))
+'''
+
+
+def _fake(tmp_path, sm=2070, state="Not Active", flush=True):
+    p = tmp_path / "nvidia-smi"
+    p.write_text(FAKE.format(python=sys.executable, sm=sm, state=state,
+                             flush="sys.stdout.flush()" if flush else "pass"))
+    p.chmod(0o755)
+    return str(p)
+
+
+def _region(sampler, seconds):
+    with sampler:
+        time.sleep(seconds)
+    return sampler.summary()
+
+
+def test_clock_sampler_takes_samples_inside_the_region(tmp_path):
+    s = bench.ClockSampler(0, exe=_fake(tmp_path))
+    c = _region(s, 0.3)
+    # a sample every 20 ms over 0.3 s (the fake's own startup aside)
+    assert c is not None and c["samples"] >= 6
+    assert c["sm_mhz"] == 2070.0 and c["sm_max_mhz"] == 2070.0 and c["reasons"] == []
+    # every kept sample but the last lies inside the region
+    ts = sorted(t for t, _ in s.lines)
+    assert sum(1 for t in ts if s.t0 <= t <= s.t1) == c["samples"] - 1
+
+
+def test_clock_sampler_reports_throttle_reasons(tmp_path):
+    c = _region(bench.ClockSampler(0, exe=_fake(tmp_path, sm=1545, state="Active")), 0.2)
+    assert c["sm_mhz"] == 1545.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_with_block_buffered_output(tmp_path):
+    # nothing arrives until the loop exits on SIGINT; the timestamps still
+    # place the samples inside the region
+    c = _region(bench.ClockSampler(0, exe=_fake(tmp_path, flush=False)), 0.3)
+    assert c is not None and c["samples"] >= 6
+
+
+def test_clock_sampler_without_nvidia_smi(tmp_path):
+    s = bench.ClockSampler(0, exe=str(tmp_path / "missing"))
+    assert _region(s, 0.01) is None
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_swiglu", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [x for x in r.stdout.splitlines() if x.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["value"] > 0
+    assert d["config"]["workload"] == "tiny_swiglu"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.parametrize("world", [2])
+def test_reference_arm_runs_on_rank_zero_only(world):
+    env = dict(os.environ, RANK="1", WORLD_SIZE=str(world), LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_swiglu", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
+    assert r.returncode == 0 and r.stdout.strip() == ""
