@@ -111,6 +111,13 @@ struct DecGroup {
   }
 };
 
+// The warp's rows of pass `pass`.
+template <int RPW>
+__device__ __forceinline__ void dec_rows(int gw, int nw, int pass, int (&row)[RPW]) {
+#pragma unroll
+  for (int j = 0; j < RPW; ++j) row[j] = gw + (pass * RPW + j) * nw;
+}
+
 template <int ACT, int MODE, int MT>
 __global__ void __launch_bounds__(DEC_THREADS, dec_ctas<MODE>()) k_decode(
     const __nv_bfloat16* __restrict__ T, const __nv_bfloat16* __restrict__ W0,
@@ -121,6 +128,30 @@ __global__ void __launch_bounds__(DEC_THREADS, dec_ctas<MODE>()) k_decode(
   constexpr int NMAT = G::NMAT;
   constexpr int RPW = G::RPW;
   extern __shared__ uint4 tok[];  // [MT][K / 8], token rows m >= M as zeros
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = gridDim.x * DEC_WARPS;
+  const int gw = warp * gridDim.x + blockIdx.x;
+  const __nv_bfloat16* const W[2] = {W0, W1};
+  const int ngroups = (K / 8 + 32 * G::CPL - 1) / (32 * G::CPL);
+  // The warp's work is one sequence of load groups over all its passes
+  // (step i = group i % ngroups of pass i / ngroups), with two groups in
+  // flight throughout: the first groups of a pass are requested before the
+  // previous pass's sums are reduced and stored.
+  int npass = 0;
+  if (gw < R) npass = min(passes, (R - gw + RPW * nw - 1) / (RPW * nw));
+  const int nsteps = npass * ngroups;
+  int rows_a[RPW], rows_b[RPW];  // rows of the steps in buffers A and B
+  G ga, gb;
+  // The weights do not depend on the previous kernel: the first two groups
+  // are requested before waiting for it.
+  if (nsteps > 0) {
+    dec_rows<RPW>(gw, nw, 0, rows_a);
+    ga.load(W, rows_a, R, K, 0, lane);
+  }
+  if (nsteps > 1) {
+    dec_rows<RPW>(gw, nw, 1 / ngroups, rows_b);
+    gb.load(W, rows_b, R, K, 1 % ngroups, lane);
+  }
   // the tokens may be the previous kernel's output (the postact)
   pdl_wait();
   for (int idx = threadIdx.x; idx < MT * (K / 8); idx += DEC_THREADS) {
@@ -129,35 +160,18 @@ __global__ void __launch_bounds__(DEC_THREADS, dec_ctas<MODE>()) k_decode(
   }
   __syncthreads();
   pdl_launch_dependents();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nw = gridDim.x * DEC_WARPS;
-  const int gw = warp * gridDim.x + blockIdx.x;
-  const __nv_bfloat16* const W[2] = {W0, W1};
-  const int ngroups = (K / 8 + 32 * G::CPL - 1) / (32 * G::CPL);
 
-  for (int pass = 0; pass < passes; ++pass) {
-    int row[RPW];
-#pragma unroll
-    for (int j = 0; j < RPW; ++j) row[j] = gw + (pass * RPW + j) * nw;
-    if (row[0] >= R) break;  // warp-uniform: no rows left
-    float acc[NMAT][RPW][MT];
+  float acc[NMAT][RPW][MT];
+  auto clear = [&] {
 #pragma unroll
     for (int a = 0; a < NMAT; ++a)
 #pragma unroll
       for (int j = 0; j < RPW; ++j)
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[a][j][m] = 0.f;
-    // two load groups in flight: group g+1 is requested before group g is used
-    G ga, gb;
-    ga.load(W, row, R, K, 0, lane);
-    for (int g = 0; g < ngroups; g += 2) {
-      if (g + 1 < ngroups) gb.load(W, row, R, K, g + 1, lane);
-      ga.fma(tok, K, g, lane, acc);
-      if (g + 2 < ngroups) ga.load(W, row, R, K, g + 2, lane);
-      if (g + 1 < ngroups) gb.fma(tok, K, g + 1, lane, acc);
-    }
-
-    // warp sums; lane j * MT + m then owns (row j, token m)
+  };
+  // warp sums of a finished pass; lane j * MT + m stores (row j, token m)
+  auto finish = [&](const int (&row)[RPW]) {
 #pragma unroll
     for (int a = 0; a < NMAT; ++a)
 #pragma unroll
@@ -187,6 +201,27 @@ __global__ void __launch_bounds__(DEC_THREADS, dec_ctas<MODE>()) k_decode(
           out[o] = __float2bfloat16_rn(s * act_f<ACT>(y0));
           if (o1) o1[o] = __float2bfloat16_rn(y0);
         }
+      }
+    }
+    clear();
+  };
+
+  clear();
+  for (int i = 0; i < nsteps; i += 2) {
+    // step i from buffer A (step i + 1 is in flight in buffer B)
+    ga.fma(tok, K, i % ngroups, lane, acc);
+    if (i % ngroups == ngroups - 1) finish(rows_a);
+    if (i + 2 < nsteps) {
+      dec_rows<RPW>(gw, nw, (i + 2) / ngroups, rows_a);
+      ga.load(W, rows_a, R, K, (i + 2) % ngroups, lane);
+    }
+    if (i + 1 < nsteps) {
+      // step i + 1 from buffer B (step i + 2 is in flight in buffer A)
+      gb.fma(tok, K, (i + 1) % ngroups, lane, acc);
+      if ((i + 1) % ngroups == ngroups - 1) finish(rows_b);
+      if (i + 3 < nsteps) {
+        dec_rows<RPW>(gw, nw, (i + 3) / ngroups, rows_b);
+        gb.load(W, rows_b, R, K, (i + 3) % ngroups, lane);
       }
     }
   }
