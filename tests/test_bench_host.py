@@ -100,3 +100,45 @@ def test_reference_arm_runs_on_rank_zero_only(world):
                         "--workload", "tiny_swiglu", "--steps", "1", "--warmup", "0"],
                        capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+# Per-config work of one step (GEMM flops = 2 x multiply-adds), as the scope
+# table states them: fwd, bwd (incl. any recompute GEMM), and the model
+# flops of fwd + bwd without the recompute.
+STATED_TFLOP = {
+    "tiny_swiglu": (17.3e-6, 34.6e-6, 51.9e-6),
+    "llama7b_swiglu": (0.554, 1.108, 1.662),
+    "falcon_h1_swiglu": (0.490, 0.979, 1.469),
+    "nanogpt_relu_sq": (0.464, 1.160, 1.392),
+    "llama3_8b_swiglu": (2.886, 7.697, 8.659),
+}
+
+
+@pytest.mark.parametrize("name", sorted(STATED_TFLOP))
+def test_step_flops_match_the_stated_work(name):
+    from activated_mlp_gemms_gb300.workloads import WORKLOADS
+    w = WORKLOADS[name]
+    fwd, bwd, model = STATED_TFLOP[name]
+    got_fwd = bench.flops_of(w, "fwd") / 1e12
+    got_bwd = bench.flops_of(w, bench.mode_of(w)) / 1e12
+    got_model = (bench.flops_of(w, "fwd") + bench.flops_of(w, "bwd")) / 1e12
+    for got, want in ((got_fwd, fwd), (got_bwd, bwd), (got_model, model)):
+        assert abs(got - want) <= 0.0011 * want, (name, got, want)
+
+
+@pytest.mark.parametrize("name", sorted(STATED_TFLOP))
+def test_kernel_flops_add_up_to_the_step(name):
+    # the kernels one step launches, each once (the recompute backward runs
+    # the gated gate/up kernel a second time; the non-gated one fuses it)
+    from activated_mlp_gemms_gb300.workloads import WORKLOADS
+    w = WORKLOADS[name]
+    k = bench.kernel_flops(w)
+    launched = ["gate_up_act", "down_proj", "dx", "wgrad"]
+    if w.recompute and not w.gated:
+        launched.append("dact_recompute")
+    else:
+        launched.append("dgated")
+        if w.recompute:
+            launched.append("gate_up_act")
+    step = bench.flops_of(w, "fwd") + bench.flops_of(w, bench.mode_of(w))
+    assert sum(k[n] for n in launched) == pytest.approx(step, rel=1e-12)
