@@ -1,11 +1,14 @@
 // gemm.cuh -- the persistent, warp-specialised tcgen05 GEMM with the MLP's
 // fused epilogues.
 //
-// One CTA per SM (320 threads, ~195 KB shared memory, all 512 TMEM columns):
+// One CTA per SM (320 threads, up to 227 KB shared memory, all 512 TMEM
+// columns):
 //   warp 0     TMA producer and tile scheduler: fetches work units from a
 //              global atomic counter (first unit = blockIdx.x), publishes
 //              them through a shared-memory ring, and streams the A/B
-//              k-blocks of each unit into a 4-stage shared-memory ring.
+//              k-blocks of each unit into a ring of as many stages as fit
+//              beside the epilogue's staging buffers (six 32 KB stages for
+//              a CTA pair, see Cfg).
 //   warp 1     allocates TMEM; one lane issues tcgen05.mma (M=128, N=256,
 //              K=16) into one of two 256-column fp32 accumulators and
 //              commits stage releases / accumulator-full signals.

@@ -142,3 +142,16 @@ def test_kernel_flops_add_up_to_the_step(name):
             launched.append("gate_up_act")
     step = bench.flops_of(w, "fwd") + bench.flops_of(w, bench.mode_of(w))
     assert sum(k[n] for n in launched) == pytest.approx(step, rel=1e-12)
+
+
+def test_device_code_hash_ignores_comments_only(tmp_path):
+    d = tmp_path / "csrc"
+    d.mkdir()
+    (d / "k.cu").write_text("int f(int x) {  // doubles\n  return 2 * x; /* plain */\n}\n")
+    (d / "mlp_api.cu").write_text("host code\n")
+    h0 = bench.csrc_hash(str(d))
+    (d / "k.cu").write_text("// a header\nint f(int x) {\n    return 2 * x;\n}\n")
+    (d / "mlp_api.cu").write_text("other host code\n")
+    assert bench.csrc_hash(str(d)) == h0
+    (d / "k.cu").write_text("int f(int x) { return 3 * x; }\n")
+    assert bench.csrc_hash(str(d)) != h0
