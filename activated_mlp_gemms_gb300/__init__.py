@@ -342,7 +342,8 @@ def mlp_trace_read(capacity: int = 4096):
 
 
 def mlp_set_tile_policy(policy: int) -> None:
-    """0 = automatic, 1 = single-CTA 128x256 tiles, 2 = CTA-pair 256x256 tiles."""
+    """0 = automatic, 1 = single-CTA 128x256 tiles, 2 = CTA-pair 256x256 tiles,
+    3 = automatic tiles with the gated forward's two GEMMs as separate launches."""
     _check(lib().mlp_set_tile_policy(int(policy)), "mlp_set_tile_policy")
 
 

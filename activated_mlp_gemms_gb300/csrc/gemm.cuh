@@ -55,10 +55,11 @@ __device__ __forceinline__ Work decode_unit(const Params& p, int unit) {
   int ks = u / tiles;
   int t = u - ks * tiles;
   // grouped raster: walk group_m tile rows down a column, then the next column
-  int per_group = p.group_m * P.tiles_n;
+  const int gm = P.group_m > 0 ? P.group_m : p.group_m;
+  int per_group = gm * P.tiles_n;
   int g = t / per_group;
-  int first_m = g * p.group_m;
-  int gsz = min(P.tiles_m - first_m, p.group_m);
+  int first_m = g * gm;
+  int gsz = min(P.tiles_m - first_m, gm);
   int r = t - g * per_group;
   Work w;
   w.prob = pi;
@@ -70,12 +71,19 @@ __device__ __forceinline__ Work decode_unit(const Params& p, int unit) {
   return w;
 }
 
+// The units of a problem that run the gated forward epilogue.
+template <int EPI>
+__device__ __forceinline__ bool gated_unit(int prob) {
+  return EPI == EPI_GATED_FWD || (EPI == EPI_FWD_FUSED && prob == 0);
+}
+
 template <int EPI>
 struct EpiTraits {
+  // output columns of a tile (EPI_FWD_FUSED: per problem, tile_n_of)
   static constexpr int TILE_N = (EPI == EPI_GATED_FWD) ? 128 : 256;
   // outputs staged per chunk (gated fwd: a, G, U; act fwd: a, P; dgated: dG,
   // dU, a; dact: dP, a; plain: D) and bytes of one staged 32 x 32 box
-  static constexpr int NOUT = (EPI == EPI_GATED_FWD || EPI == EPI_DGATED) ? 3
+  static constexpr int NOUT = (EPI == EPI_GATED_FWD || EPI == EPI_DGATED || EPI == EPI_FWD_FUSED) ? 3
                               : (EPI == EPI_ACT_FWD || EPI == EPI_DACT ||
                                  EPI == EPI_DACT_RECOMP || EPI == EPI_ACT_FWD_F8) ? 2
                                                                                   : 1;
@@ -92,6 +100,11 @@ struct EpiTraits {
                                   : EPI == EPI_DGRAD_F8 ? 4096
                                                         : STG_BUFS * OUT_BYTES;
 };
+
+template <int EPI>
+__device__ __forceinline__ int tile_n_of(int prob) {
+  return gated_unit<EPI>(prob) ? 128 : EpiTraits<EPI>::TILE_N;
+}
 
 __device__ __forceinline__ void record_timeout(const Params& p, volatile int* abort_flag) {
   *abort_flag = 1;
@@ -641,6 +654,36 @@ __device__ __forceinline__ void epi_plain(const Params& p, const EpiUnit& P, con
   }
 }
 
+// EPI_FWD_FUSED: the producer thread of a down unit waits (bounded) until
+// every gate/up tile of its 256-row block is stored, then orders its TMA
+// loads of the postact after that.  False on expiry or abort.
+__device__ __forceinline__ bool wait_block_ready(const Params& p, int tm, uint64_t limit_ns,
+                                                 volatile int* abort) {
+  const int* ctr = p.dep + tm;
+  if (ld_acquire_gpu(ctr) < p.dep_target) {
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t n = 0;
+    while (ld_acquire_gpu(ctr) < p.dep_target) {
+      if ((++n & 15u) == 0 && (*abort || globaltimer_ns() - t0 > limit_ns)) return false;
+      __nanosleep(64);
+    }
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
+// EPI_FWD_FUSED: one epilogue warp's share of a gate/up tile is stored.  Lane
+// 0, which issued the warp's TMA stores, waits for them to complete and
+// counts the warp for the tile's 256-row block (release).
+__device__ __forceinline__ void signal_block_part(const Params& p, int tm, int lane) {
+  if (lane == 0) {
+    bulk_wait_all();
+    fence_proxy_async_global();
+    red_release_gpu_add(p.dep + tm, 1);
+  }
+  __syncwarp();
+}
+
 // -------------------------------------------------------------------- kernel
 // Per-CTA-group constants.  CG = 1: one CTA computes a 128 x 256 tile and
 // stages all 256 B rows.  CG = 2: a CTA pair computes a 256 x 256 tile with
@@ -690,7 +733,7 @@ __device__ __forceinline__ UnitLoads unit_loads(const Params& p, const Prob& P, 
   L.a1 = &p.maps[P.mapA1];
   L.m0 = w.tm * (BM * CG) + static_cast<int>(rank) * BM;
   L.kb0 = P.kb0;
-  if constexpr (EPI == EPI_GATED_FWD) {
+  if (gated_unit<EPI>(w.prob)) {
     // CG=1: both weights' rows; CG=2: the leader stages the gate rows, the peer the up rows
     L.b0 = &p.maps[(CG == 2 && rank != 0) ? P.mapB1 : P.mapB0];
     L.b1 = &p.maps[P.mapB1];
@@ -762,7 +805,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   using C = Cfg<EPI, CG>;
   constexpr bool PAIR = CG == 2;
-  constexpr int TILE_N = EpiTraits<EPI>::TILE_N;
+  static_assert(EPI != EPI_FWD_FUSED || CG == 2, "the fused forward runs on CTA pairs");
   // 8-bit operands: a 128-byte k-block row holds 128 elements (bf16: 64)
   constexpr bool F8 = is_f8(EPI);
   constexpr int KE = F8 ? 2 * BK : BK;
@@ -887,6 +930,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
             if (L.i0) tma_prefetch_l2_2d(L.i0, L.icol, L.m0);
             if (L.i1) tma_prefetch_l2_2d(L.i1, L.icol, L.m0);
           }
+          if constexpr (EPI == EPI_FWD_FUSED) {
+            // a down unit reads the postact of its rows
+            if (w.prob == 1 && !wait_block_ready(p, w.tm, lim, abort_flag)) {
+              ok = false;
+              break;
+            }
+          }
           for (int kb = w.kb_begin; kb < w.kb_end && ok; ++kb) {
             if (!mbar_wait<PAIR>(bar_s(EMPTY + stage), phase ^ 1u, lim, abort_flag)) {
               ok = false;
@@ -927,6 +977,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
           if constexpr (EpiTraits<EPI>::DACT) {
             if (L.i0) tma_prefetch_l2_2d(L.i0, L.icol, L.m0);
             if (L.i1) tma_prefetch_l2_2d(L.i1, L.icol, L.m0);
+          }
+          if constexpr (EPI == EPI_FWD_FUSED) {
+            if (w.prob == 1 && !wait_block_ready(p, w.tm, lim, abort_flag)) {
+              ok = false;
+              break;
+            }
           }
           const uint32_t full_lead = lead(bar_s(FULL));
           for (int kb = w.kb_begin; kb < w.kb_end && ok; ++kb) {
@@ -1052,7 +1108,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quadrant this warp may access
     const int half = (warp - 2) >> 2;  // which half of the tile's columns
-    const int cb = half * (TILE_N / 2), ce = cb + TILE_N / 2;
     EpiWarp e;
     e.stg = stg_s + static_cast<uint32_t>(warp - 2) * EpiTraits<EPI>::STG_WARP;
     e.lane = lane;
@@ -1096,7 +1151,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       e.row0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
       e.rows_ok = e.row0 < P.M;
       e.rs = (P.rstd && e.row0 + lane < P.M) ? P.rstd[e.row0 + lane] : 1.f;
-      const int col0 = w.tn * TILE_N;
+      const int tile_n = tile_n_of<EPI>(pi);
+      const int cb = half * (tile_n / 2), ce = cb + tile_n / 2;
+      const int col0 = w.tn * tile_n;
       uint4 pg[4], pu[4];
       uint32_t dd[EPI == EPI_DACT_RECOMP ? 64 : 1];  // s*act'(p) between the two phases
       (void)dd;
@@ -1132,6 +1189,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       if (e.rows_ok) {  // warp-uniform: rows past the output need no epilogue
         if constexpr (EPI == EPI_GATED_FWD) {
           epi_gated_fwd<ACT>(p, P, e, tb, col0, cb, ce);
+        } else if constexpr (EPI == EPI_FWD_FUSED) {
+          if (pi == 0) epi_gated_fwd<ACT>(p, P, e, tb, col0, cb, ce);
+          else epi_plain<EPI_STORE_BF16>(p, P, e, tb, col0, cb, ce);
         } else if constexpr (EPI == EPI_ACT_FWD) {
           epi_act_fwd<ACT>(p, P, e, tb, col0, cb, ce);
         } else if constexpr (EPI == EPI_DGATED) {
@@ -1156,6 +1216,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       }
       acc ^= 1;
       if (acc == 0) aphase ^= 1u;
+      if constexpr (EPI == EPI_FWD_FUSED) {
+        // the down units of this block wait for every warp's gate/up stores
+        if (pi == 0) signal_block_part(p, w.tm, lane);
+      }
     }
     // the last stores must finish before the kernel (and its shared memory) ends
     if (lane == 0) bulk_wait_all();

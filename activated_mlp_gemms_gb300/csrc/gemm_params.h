@@ -36,8 +36,14 @@ enum Epi : int {
   EPI_ACT_FWD_F8 = 7,     // pre = deq'*acc (deq' = *sa * *sb), a = mult*relu(pre)^2 ->
                           // e4m3(a / *sq) (map 0), optional bf16 pre (map 1), amax|a| -> *amax
   EPI_STORE_BF16_F8 = 8,  // D = bf16(deq * acc)
-  EPI_DGRAD_F8 = 9        // dpre = deq*acc*2*relu(P) (in0 = P, bf16) -> e5m2(dpre / *sq)
+  EPI_DGRAD_F8 = 9,       // dpre = deq*acc*2*relu(P) (in0 = P, bf16) -> e5m2(dpre / *sq)
                           // (map 0), amax|dpre| -> *amax
+  // The gated forward in one launch: problem 0 is the gate/up GEMM with the
+  // EPI_GATED_FWD epilogue, problem 1 the down projection with the
+  // EPI_STORE_BF16 epilogue, reading problem 0's postact.  A down unit of a
+  // 256-row block starts once every gate/up tile of that block is stored
+  // (Params::dep), so the down tiles fill the SMs the gate/up tail leaves idle.
+  EPI_FWD_FUSED = 10
 };
 
 __host__ __device__ constexpr bool is_f8(int epi) {
@@ -53,7 +59,7 @@ enum Act : int { ACT_SILU = 0, ACT_RELU_SQ = 1, ACT_GELU_TANH = 2, ACT_RELU = 3,
 struct Prob {
   int M, N;               // output rows / columns
   int kb0, kb1;           // k-blocks of K-segment 0 and 1 (kb1 = 0: one segment)
-  int tiles_m, tiles_n;   // output tiles (tile N = 128 for EPI_GATED_FWD, else 256)
+  int tiles_m, tiles_n;   // output tiles (tile N = 128 for a gated forward, else 256)
   int ksplit, kper;       // split-K factor, k-blocks per split
   int unit_begin, units;  // this problem's slice of the global work-unit range
   int mapA0, mapB0;       // tensor maps of segment 0
@@ -72,7 +78,7 @@ struct Prob {
   const float* rstd;      // per output row: gate/up accumulators (activation forward) and
                           // dG, dU / dP (derivative epilogues) are multiplied by rstd[row]
   float alpha;            // EPI_STORE_BF16 with in0 = residual [M, ld]: D = alpha*in0 + acc
-  int pad_b;
+  int group_m;            // L2 raster group of this problem (0: Params::group_m)
   // 8-bit epilogues: dequant factor mult * *sa * *sb; *sq the scale of an 8-bit output
   const float* sa;
   const float* sb;
@@ -93,9 +99,11 @@ struct Params {  // 64-byte aligned through CUtensorMap
   int debug_flags;        // MLP_DEBUG_* (testing only; 0 in normal use)
   int a_tx_bytes;         // bytes one CTA's A boxes bring per k-block (K-major A: rows x 128 B)
   int nmaps;              // tensor maps in use
-  int pad3_;
+  int dep_target;         // EPI_FWD_FUSED: dep count of a complete 256-row block
   int* counter;           // dynamic tile scheduler counter, zero at launch
   int* status;            // device status word (MLP_ERR_TIMEOUT on a bounded-wait expiry)
+  int* dep;               // EPI_FWD_FUSED: per 256-row block, the gate/up epilogue warps whose
+                          // stores have completed (one count per warp and tile; zero at launch)
   unsigned long long timeout_ns;
 };
 

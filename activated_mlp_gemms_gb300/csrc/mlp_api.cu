@@ -35,9 +35,14 @@ using namespace mlpk;
 
 namespace {
 
-constexpr size_t CTRL_BYTES = 1024;  // status word + tile-scheduler counters
-constexpr int COUNTER_BASE = 16;     // counters start at int index 16 (byte 64)
-constexpr int MAX_COUNTERS = (CTRL_BYTES / 4) - COUNTER_BASE;
+// The workspace's control block (zeroed by every call): the status word
+// (int 0), the tile-scheduler counters (ints 16..127) and the fused
+// forward's per-block counts (ints 128..255).
+constexpr size_t CTRL_BYTES = 1024;
+constexpr int COUNTER_BASE = 16;
+constexpr int MAX_COUNTERS = 112;
+constexpr int DEP_BASE = 128;
+constexpr int MAX_DEP_BLOCKS = 128;  // 256-row blocks of a fused forward: M <= 32768
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -164,15 +169,18 @@ int device_act(int act) {
   }
 }
 
-std::atomic<int> g_tile_policy{0};  // 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles
+// 0 auto, 1 single-CTA tiles, 2 CTA-pair tiles, 3 auto with the gated
+// forward's two GEMMs as separate launches
+std::atomic<int> g_tile_policy{0};
 
 // The forward of at most DECODE_MAX_M tokens runs on the CUDA cores (a
 // weight stream) unless a tile policy forces the tensor-core path, or its
 // token rows do not fit a CTA's shared memory.
 bool decode_path(const mlp_problem_t* p) {
   const long long k = p->H > p->I ? p->H : p->I;
+  const int pol = g_tile_policy.load();
   return p->M <= DECODE_MAX_M && (long long)p->M * k * 2 <= DECODE_MAX_TOKEN_BYTES &&
-         g_tile_policy.load() == 0;
+         (pol == 0 || pol == 3);
 }
 
 // CTA-group size for a GEMM whose output has `rows` rows: pairs (256-row
@@ -404,11 +412,15 @@ int run_act(Gemm& g, Call& c, int tag) {
     return traced(tag, c.stream,
                   [&] { return launch_gemm<EPI, A_MN, B_MN, 2, ACT>(g.p, 2 * n, c.stream, pdl); });
   }
-  const int sms = num_sms();
-  const int n = g.p.total_units < sms ? g.p.total_units : sms;
-  return traced(tag, c.stream, [&] {
-    return launch_gemm<EPI, A_MN, B_MN, 1, ACT>(g.p, n < 1 ? 1 : n, c.stream, pdl);
-  });
+  if constexpr (EPI == EPI_FWD_FUSED) {
+    return MLP_ERR_UNSUPPORTED;  // CTA pairs only
+  } else {
+    const int sms = num_sms();
+    const int n = g.p.total_units < sms ? g.p.total_units : sms;
+    return traced(tag, c.stream, [&] {
+      return launch_gemm<EPI, A_MN, B_MN, 1, ACT>(g.p, n < 1 ? 1 : n, c.stream, pdl);
+    });
+  }
 }
 
 // Kernels without an activation epilogue.
@@ -644,6 +656,51 @@ int launch_down(const mlp_problem_t* p, Call& c, const void* a, const void* Wd, 
   return run<EPI_STORE_BF16, false, false>(g, c, MLP_KERNEL_DOWN);
 }
 
+// The gated forward as one launch (EPI_FWD_FUSED) on CTA pairs: problem 0
+// is the gate/up GEMM (a, and G/U when saved), problem 1 the down
+// projection out = a Wd^T (+ alpha * resid for the block).  A down unit
+// waits until its 256-row block of a is stored; the down units are rastered
+// block by block, so the first ones claimed belong to the blocks whose
+// gate/up tiles finish first.  The per-block counts live in the control
+// block (zeroed by begin_call).
+bool fused_forward(const mlp_problem_t* p, int split) {
+  return gated(p) && split == 1 && g_tile_policy.load() == 0 && pick_cg(p->M) == 2 &&
+         (p->M + 2 * BM - 1) / (2 * BM) <= MAX_DEP_BLOCKS;
+}
+
+int launch_fwd_fused(const mlp_problem_t* p, Call& c, const void* x, const void* Wg,
+                     const void* Wu, const void* Wd, void* a, void* G_out, void* U_out, void* out,
+                     const float* rstd, const void* resid, float alpha) {
+  Gemm g(*p, c.counter(), c.status, 2);
+  const int mX = g.kmajor_a(x, p->M, p->H);
+  const int mG = g.kmajor(Wg, p->I, p->H, 128);
+  const int mU = g.kmajor(Wu, p->I, p->H, 128);
+  const int oA = g.output(a, p->M, p->I);
+  const int oG = g.output(G_out, p->M, p->I);
+  const int oU = g.output(U_out, p->M, p->I);
+  const int mA = g.kmajor_a(a, p->M, p->I);
+  const int mD = g.kmajor(Wd, p->H, p->I, g.b_rows());
+  const int oO = g.output(out, p->M, p->H);
+  Prob& P0 = g.add(p->M, p->I, p->H, 0, 128);
+  P0.mapA0 = mX;
+  P0.mapB0 = mG;
+  P0.mapB1 = mU;
+  P0.mapO[0] = oA;
+  P0.mapO[1] = oG;
+  P0.mapO[2] = oU;
+  P0.rstd = rstd;
+  Prob& P1 = g.add(p->M, p->H, p->I, 0, MMA_N);
+  P1.mapA0 = mA;
+  P1.mapB0 = mD;
+  P1.mapO[0] = oO;
+  P1.in0 = resid;  // the epilogue reads the residual tile before storing over it
+  P1.alpha = alpha;
+  P1.group_m = 1;
+  g.p.dep = c.status + DEP_BASE;
+  g.p.dep_target = P0.tiles_n * 2 * NUM_EPI_WARPS;  // every epilogue warp of the pair, per tile
+  return run_gated<EPI_FWD_FUSED, false, false>(g, c, MLP_KERNEL_FWD_FUSED);
+}
+
 int forward(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu, const void* Wd,
             void* out, void* G_save, void* U_save, void* ws, size_t ws_bytes, void* stream,
             int mode, const Block* blk = nullptr) {
@@ -681,6 +738,9 @@ int forward(const mlp_problem_t* p, const void* x, const void* Wg, const void* W
       return launch_rstd(x, blk->rstd_out, p->M, p->H, blk->eps, c.stream, pdl);
     }));
   }
+  if (fused_forward(p, split))
+    return launch_fwd_fused(p, c, x, Wg, Wu, Wd, a, G_save, U_save, out,
+                            blk ? blk->rstd : nullptr, blk ? x : nullptr, blk ? blk->alpha : 0.f);
   MLP_TRY(launch_fwd_act(p, c, x, Wg, Wu, a, G_save, U_save, blk ? blk->rstd : nullptr));
   return launch_down(p, c, a, Wd, out, part, split, blk ? x : nullptr, blk ? blk->alpha : 0.f);
 }
@@ -1148,7 +1208,7 @@ int mlp_device_status(const void* ws, void* stream) {
 const char* mlp_version(void) { return "0.1.0"; }
 
 int mlp_set_tile_policy(int policy) {
-  if (policy < 0 || policy > 2) return MLP_ERR_INVALID_ARG;
+  if (policy < 0 || policy > 3) return MLP_ERR_INVALID_ARG;
   g_tile_policy.store(policy);
   return MLP_OK;
 }
@@ -1205,6 +1265,7 @@ const char* mlp_kernel_name(int tag) {
     case MLP_KERNEL_RSTD: return "rstd";
     case MLP_KERNEL_RMSNORM_BWD: return "rmsnorm_bwd";
     case MLP_KERNEL_QUANT: return "quant_f8";
+    case MLP_KERNEL_FWD_FUSED: return "fwd_fused";
     default: return "unknown";
   }
 }

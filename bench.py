@@ -95,6 +95,7 @@ def kernel_flops(w):
         "dx": (4 if g else 2) * mhi,
         "wgrad": (6 if g else 4) * mhi,
         "dact_recompute": 4 * mhi,  # non-gated recompute: x W1^T and dout Wd
+        "fwd_fused": (6 if g else 4) * mhi,  # gated forward: gate/up and down in one launch
     }
 
 

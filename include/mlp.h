@@ -334,9 +334,11 @@ int mlp_fwd_infer_noalloc(const mlp_problem_t* p, const void* x, const void* Wg,
  * 0 = automatic (default): GEMMs whose output has more than 128 rows use
  *     256 x 256 tiles computed by a CTA pair (tcgen05 cta_group::2), the
  *     others 128 x 256 tiles on one CTA;
- * 1 = always single-CTA tiles;  2 = always CTA-pair tiles.
+ * 1 = always single-CTA tiles;  2 = always CTA-pair tiles;
+ * 3 = as 0, but the gated forward's gate/up and down GEMMs run as two
+ *     launches (policy 0 runs them as one; see MLP_KERNEL_FWD_FUSED).
  * Policies 1 and 2 also keep forwards of one or two tokens on the tensor
- * cores (policy 0 streams their weights on the CUDA cores).
+ * cores (policies 0 and 3 stream their weights on the CUDA cores).
  * Process-wide; returns MLP_ERR_INVALID_ARG for other values.  Results of
  * the two tile shapes agree to rounding (same fp32 accumulation order). */
 int mlp_set_tile_policy(int policy);
@@ -374,7 +376,10 @@ typedef enum {
                                     epilogue postact and dP */
   MLP_KERNEL_RSTD = 8,          /* the block's per-token RMS-norm scale */
   MLP_KERNEL_RMSNORM_BWD = 9,   /* the block's RMS-norm derivative and residual gradient */
-  MLP_KERNEL_QUANT = 10         /* bf16 -> e4m3 / e5m2 quantisation */
+  MLP_KERNEL_QUANT = 10,        /* bf16 -> e4m3 / e5m2 quantisation */
+  MLP_KERNEL_FWD_FUSED = 11     /* the gated forward's gate/up and down GEMMs in one launch
+                                   (CTA-pair tiles, M <= 32768): a down tile starts once the
+                                   postact of its 256 rows is stored */
 } mlp_kernel_t;
 
 /* on != 0 starts recording, 0 stops (records already taken are kept). */

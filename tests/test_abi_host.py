@@ -187,9 +187,9 @@ def test_kernel_names_and_empty_trace(L):
 
 
 def test_tile_policy_values(L):
-    assert L.mlp_set_tile_policy(3) == -1
+    assert L.mlp_set_tile_policy(4) == -1
     assert L.mlp_set_tile_policy(-1) == -1
-    for v in (1, 2, 0):
+    for v in (1, 2, 3, 0):
         assert L.mlp_set_tile_policy(v) == 0
 
 

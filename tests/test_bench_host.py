@@ -133,15 +133,18 @@ def test_kernel_flops_add_up_to_the_step(name):
     from activated_mlp_gemms_gb300.workloads import WORKLOADS
     w = WORKLOADS[name]
     k = bench.kernel_flops(w)
-    launched = ["gate_up_act", "down_proj", "dx", "wgrad"]
-    if w.recompute and not w.gated:
-        launched.append("dact_recompute")
-    else:
-        launched.append("dgated")
-        if w.recompute:
-            launched.append("gate_up_act")
     step = bench.flops_of(w, "fwd") + bench.flops_of(w, bench.mode_of(w))
-    assert sum(k[n] for n in launched) == pytest.approx(step, rel=1e-12)
+    # the gated forward runs as one fused launch or as two
+    forwards = [["gate_up_act", "down_proj"]] + ([["fwd_fused"]] if w.gated else [])
+    for fwd in forwards:
+        launched = fwd + ["dx", "wgrad"]
+        if w.recompute and not w.gated:
+            launched.append("dact_recompute")
+        else:
+            launched.append("dgated")
+            if w.recompute:
+                launched.append("gate_up_act")
+        assert sum(k[n] for n in launched) == pytest.approx(step, rel=1e-12), launched
 
 
 def test_device_code_hash_ignores_comments_only(tmp_path):
