@@ -45,10 +45,11 @@
  *     validated before anything is enqueued; on a validation error nothing
  *     is enqueued and outputs are untouched.
  *   - Workspace: `ws` is caller-owned device scratch of at least
- *     mlp_workspace_size(p, mode) bytes, 256-byte aligned.  Its first bytes
- *     hold the device status word and the tile-scheduler counters; every
- *     call clears them on the stream before its kernels run.  Calls that
- *     share one workspace must be ordered (same stream, or synchronised).
+ *     mlp_workspace_size(p, mode) bytes, 256-byte aligned.  Its first 1 KB
+ *     holds the device status word, the tile-scheduler counters and the
+ *     one-launch gated forward's per-block counts; every call clears it on
+ *     the stream before its kernels run.  Calls that share one workspace
+ *     must be ordered (same stream, or synchronised).
  *   - Device-side errors (a bounded wait that expired) are recorded in the
  *     workspace status word; read it with mlp_device_status.
  */
