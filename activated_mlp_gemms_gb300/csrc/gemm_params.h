@@ -137,7 +137,7 @@ cudaError_t launch_quant_f8(const void* src, long long n, const float* scale, vo
 // down projection out = a Wd^T.  `act` is a device activation (Act).  Each
 // CTA stages the M token rows of its K (H, then I) whole in shared memory:
 // M * K * 2 <= DECODE_MAX_TOKEN_BYTES.
-constexpr int DECODE_MAX_M = 2;
+constexpr int DECODE_MAX_M = 4;
 constexpr int DECODE_MAX_TOKEN_BYTES = 100 * 1024;
 cudaError_t launch_decode_act(const void* x, const void* Wg, const void* Wu, void* a, void* G,
                               void* U, int M, int H, int I, int act, bool gated, float s,

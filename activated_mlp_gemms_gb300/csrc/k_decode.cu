@@ -1,7 +1,7 @@
-// Decode-sized forward (one or two tokens) on the CUDA cores.
+// Decode-sized forward (one to four tokens) on the CUDA cores.
 //
-// With one or two tokens every weight element is used once or twice: the
-// forward is a weight stream, bound by HBM.  The tensor-core path reads its
+// With a few tokens every weight element is used a few times: the forward
+// is a weight stream, bound by HBM.  The tensor-core path reads its
 // K-major weight boxes 128 bytes per row at a time, scattered over 128 rows,
 // and streams at ~4 TB/s.  Here each warp owns whole weight rows and reads
 // them front to back, 512 contiguous bytes per warp-wide 16-byte load, with
@@ -36,10 +36,12 @@ constexpr int DEC_WARPS = DEC_THREADS / 32;
 // chunks per lane in one load group (two groups in flight)
 template <int MODE>
 __host__ __device__ constexpr int dec_ctas() { return 2; }
-template <int MODE>
-__host__ __device__ constexpr int dec_rpw() { return 2; }
-template <int MODE>
-__host__ __device__ constexpr int dec_cpl() { return MODE == DEC_GATED ? 2 : 4; }
+// (the gated pass with three or four tokens takes one row per matrix, so
+// that its weights, tokens and sums fit 128 registers)
+template <int MODE, int MT>
+__host__ __device__ constexpr int dec_rpw() { return MODE == DEC_GATED && MT > 2 ? 1 : 2; }
+template <int MODE, int MT>
+__host__ __device__ constexpr int dec_cpl() { return MODE == DEC_GATED && MT <= 2 ? 2 : 4; }
 
 // 8 bf16 (one 16-byte vector) -> 8 floats (exact).
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
@@ -63,8 +65,8 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
 template <int MODE, int MT>
 struct DecGroup {
   static constexpr int NMAT = MODE == DEC_GATED ? 2 : 1;
-  static constexpr int RPW = dec_rpw<MODE>();
-  static constexpr int CPL = dec_cpl<MODE>();
+  static constexpr int RPW = dec_rpw<MODE, MT>();
+  static constexpr int CPL = dec_cpl<MODE, MT>();
   uint4 w[CPL][NMAT][RPW];
 
   // the group's chunks: chunk (g * CPL + q) * 32 + lane of each row
@@ -233,7 +235,7 @@ cudaError_t launch_decode_inst(const __nv_bfloat16* T, const __nv_bfloat16* W0,
                                __nv_bfloat16* o2, int M, int R, int K, float s,
                                cudaStream_t stream, bool pdl) {
   auto kern = k_decode<ACT, MODE, MT>;
-  constexpr int RPW = dec_rpw<MODE>();
+  constexpr int RPW = dec_rpw<MODE, MT>();
   int dev = 0, sms = 148;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -275,8 +277,12 @@ cudaError_t launch_decode_mt(const void* T, const void* W0, const void* W1, void
   auto y = static_cast<__nv_bfloat16*>(out);
   auto y1 = static_cast<__nv_bfloat16*>(o1);
   auto y2 = static_cast<__nv_bfloat16*>(o2);
-  if (M <= 1) return launch_decode_inst<ACT, MODE, 1>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl);
-  return launch_decode_inst<ACT, MODE, 2>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl);
+  switch (M) {
+    case 1: return launch_decode_inst<ACT, MODE, 1>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl);
+    case 2: return launch_decode_inst<ACT, MODE, 2>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl);
+    case 3: return launch_decode_inst<ACT, MODE, 3>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl);
+    default: return launch_decode_inst<ACT, MODE, 4>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl);
+  }
 }
 
 cudaError_t launch_decode_act(const void* x, const void* Wg, const void* Wu, void* a, void* G,

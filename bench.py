@@ -715,7 +715,7 @@ def infer_m_sweep(m, w, g, dev, flush, peaks):
     bf = torch.bfloat16
     wbytes = (3 if w.gated else 2) * w.H * w.I * 2
     rows = []
-    for M in (1, 16, 64, 128, 256, 512):
+    for M in (1, 2, 3, 4, 16, 64, 128, 256, 512):
         prob = m.problem(M, w.H, w.I, w.act, w.gate_mult, w.down_mult)
         x = torch.randn(M, w.H, device=dev).to(bf)
         out = torch.empty(M, w.H, dtype=bf, device=dev)

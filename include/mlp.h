@@ -136,7 +136,7 @@ size_t mlp_workspace_size(const mlp_problem_t* p, int mode);
  *   U_save bf16 [M,I]  out, optional: the up preact x Wu^T (NULL when non-gated)
  * Pass G_save/U_save as NULL for the recompute mode (save only x).  The
  * bf16 values written to `out` are bitwise identical to mlp_fwd_infer's.
- * With one or two tokens (decode; M * max(H, I) * 2 <= 100 KiB), unless a
+ * With one to four tokens (decode; M * max(H, I) * 2 <= 100 KiB), unless a
  * tile policy is set (below), the forward streams the weights on the CUDA
  * cores instead of the tensor cores: each warp reads whole weight rows
  * front to back and accumulates the M dot products in fp32 (two kernels,
@@ -338,7 +338,7 @@ int mlp_fwd_infer_noalloc(const mlp_problem_t* p, const void* x, const void* Wg,
  * 1 = always single-CTA tiles;  2 = always CTA-pair tiles;
  * 3 = as 0, but the gated forward's gate/up and down GEMMs run as two
  *     launches (policy 0 runs them as one; see MLP_KERNEL_FWD_FUSED).
- * Policies 1 and 2 also keep forwards of one or two tokens on the tensor
+ * Policies 1 and 2 also keep forwards of one to four tokens on the tensor
  * cores (policies 0 and 3 stream their weights on the CUDA cores).
  * Process-wide; returns MLP_ERR_INVALID_ARG for other values.  Results of
  * the two tile shapes agree to rounding (same fp32 accumulation order). */

@@ -1,4 +1,4 @@
-"""GPU parity of the decode-sized forward (one or two tokens), which streams
+"""GPU parity of the decode-sized forward (one to four tokens), which streams
 the weights on the CUDA cores, against the fp64 oracle, through the C ABI.
 
 The same guard bands and NaN-filled outputs as the other parity tests; the
@@ -17,11 +17,11 @@ ACTS = ["swiglu", "relu_sq", "gelu_tanh_approx", "relu", "reglu", "geglu", "glu"
 
 
 @pytest.mark.parametrize("act", ACTS)
-@pytest.mark.parametrize("M", [1, 2, 3])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5])
 def test_decode_forward_parity(act, M):
     """K = 1000 (a ragged last load group), I = 1544 rows (a ragged last
     round of rows); the forward saves G/U, the backward then runs on the
-    tensor cores from them.  M = 3 takes the tensor-core forward."""
+    tensor cores from them.  M = 5 takes the tensor-core forward."""
     H, I = 1000, 1544
     t = make_inputs(M, H, I, act, seed=31)
     got, bad, _ = run_gpu(dev_tensors(t), M, H, I, act, 1.125, 2.0, mode="saved")
@@ -30,7 +30,7 @@ def test_decode_forward_parity(act, M):
 
 
 @pytest.mark.parametrize("act", ["swiglu", "relu_sq"])
-@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
 def test_decode_inference_long_k(act, M):
     """Long rows (H = 4096 for gate/up, I = 5504 for the down projection),
     against the oracle and the tensor-core path."""
@@ -88,3 +88,32 @@ def test_decode_path_is_two_kernels_and_graph_capturable():
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("M,path", [(3, ["gate_up_act", "down_proj"]), (4, None)])
+def test_decode_token_rows_must_fit_shared_memory(M, path):
+    """With Llama-3-8B's intermediate size (14336) three token rows of the
+    postact fit a CTA's shared memory and take the weight-streaming kernels;
+    four do not and take the tensor cores (a split-K down projection, then
+    its fp32 -> bf16 pass)."""
+    H, I = 4096, 14336
+    t = make_inputs(M, H, I, "swiglu", seed=34)
+    d = dev_tensors(t)
+    prob = m.problem(M, H, I)
+    out = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    m.mlp_trace_read()
+    m.mlp_trace_enable(True)
+    try:
+        ws = m.mlp_fwd_infer(prob, d["x"], d["Wg"], d["Wu"], d["Wd"], out)
+        torch.cuda.synchronize()
+    finally:
+        m.mlp_trace_enable(False)
+    names = [n for n, _ in m.mlp_trace_read()]
+    if path is not None:
+        assert names == path, names
+    else:
+        assert names == ["gate_up_act", "down_proj", "convert"], names
+    assert m.mlp_device_status(ws) == 0
+    a = {k: to_f64(v) for k, v in t.items() if v is not None}
+    ref = mlp_forward(a["x"], a["Wg"], a["Wu"], a["Wd"], "swiglu")["out"]
+    assert rel_err(to_f64(out), ref) <= 2e-2
