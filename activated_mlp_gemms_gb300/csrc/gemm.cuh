@@ -19,6 +19,9 @@
 // The double-buffered accumulator lets the epilogue of tile t overlap the
 // MMAs of tile t+1.  Every wait is bounded (globaltimer); on expiry the
 // kernel records MLP_ERR_TIMEOUT in the status word and unwinds.
+// EPI_FWD_FUSED runs the gated forward's two GEMMs in one launch: the
+// epilogue warps count their stored gate/up tiles per 256-row block, and the
+// producer of a down-projection unit waits for its block's count.
 //
 // Operand layouts.  A is BM x BK, B is 256 x BK, both bf16 with the
 // 128-byte swizzle.  K-major operands ([rows, K], K contiguous) arrive as
