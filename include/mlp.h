@@ -307,8 +307,8 @@ int mlp_device_status(const void* ws, void* stream);
 /* Library version, e.g. "0.1.0". */
 const char* mlp_version(void);
 
-/* ---- Inference forward without a caller workspace (no counterpart in the
- * paper: an addition of this library) ----
+/* ---- Inference forward without a caller workspace (no counterpart on the
+ * pages: an addition of this library) ----
  * For callers that may not allocate device memory when they run the MLP
  * (for example a C runtime whose device memory is planned once at start-up,
  * or a serving loop that must not call cudaMalloc because it synchronises
