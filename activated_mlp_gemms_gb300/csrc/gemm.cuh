@@ -98,8 +98,10 @@ struct EpiTraits {
   // staged boxes per warp: at most two (a third output reuses the first box
   // once that box's store has read it), so the stage ring keeps 6 stages
   static constexpr int STG_BUFS = NOUT < 2 ? NOUT : 2;
-  // 8-bit outputs: a 32 x 128-byte tile box (+ the bf16 preact's chunk box)
-  static constexpr int STG_WARP = EPI == EPI_ACT_FWD_F8  ? 4096 + 2048
+  // 8-bit outputs: the e4m3 postact's 32 x 64-byte half-tile box (+ the bf16
+  // preact's chunk box; small enough for a sixth pipeline stage), the e5m2
+  // derivative's 32 x 128-byte tile box
+  static constexpr int STG_WARP = EPI == EPI_ACT_FWD_F8  ? 2048 + 2048
                                   : EPI == EPI_DGRAD_F8 ? 4096
                                                         : STG_BUFS * OUT_BYTES;
 };
@@ -483,6 +485,17 @@ __device__ __forceinline__ void stage_f8_chunk(uint32_t buf, int r, int c, const
   st_shared_v4(rb + (((u + 1u) ^ x) << 4), q[4], q[5], q[6], q[7]);
 }
 
+// The same for a 32 x 64-byte box with the 64-byte swizzle (16-byte unit u
+// of row r at unit u ^ ((r / 2) % 4)): lane r writes bytes [32 h, 32 h + 32)
+// of its row for the box's chunk h (0 or 1).
+__device__ __forceinline__ void stage_f8_half(uint32_t buf, int r, int h, const uint32_t (&q)[8]) {
+  const uint32_t rb = buf + static_cast<uint32_t>(r) * 64u;
+  const uint32_t x = (static_cast<uint32_t>(r) >> 1) & 3u;
+  const uint32_t u = 2u * static_cast<uint32_t>(h);
+  st_shared_v4(rb + ((u ^ x) << 4), q[0], q[1], q[2], q[3]);
+  st_shared_v4(rb + (((u + 1u) ^ x) << 4), q[4], q[5], q[6], q[7]);
+}
+
 // Store the staged 8-bit box of output o at (col, row0) as a bulk group.
 __device__ __forceinline__ void store_f8_tile(const EpiUnit& P, const EpiWarp& e, int o,
                                               uint32_t buf, int col) {
@@ -495,10 +508,11 @@ __device__ __forceinline__ void store_f8_tile(const EpiUnit& P, const EpiWarp& e
 }
 
 // e4m3 forward of the ReLU^2 MLP: pre = acc * sx * s1, a = mult * relu(pre)^2,
-// a -> e4m3(a * fp32(1 / s_post)) (map 0, staged per tile at stg) and, if
-// requested, pre in bf16 through a 32 x 32 bf16 box per chunk (map 1, at
-// stg + 4096; for the backward); the largest |a| of the warp's rows goes to
-// *amax (atomic max on the bits of a non-negative float).
+// a -> e4m3(a * fp32(1 / s_post)) (map 0, staged two chunks at a time in a
+// 32 x 64-byte box at stg) and, if requested, pre in bf16 through a 32 x 32
+// bf16 box per chunk (map 1, at stg + 2048; for the backward); the largest
+// |a| of the warp's rows goes to *amax (atomic max on the bits of a
+// non-negative float).
 template <int ACT>
 __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                            uint32_t tb, int col0, int cb, int ce) {
@@ -507,7 +521,7 @@ __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, co
   const float s = P.mult;
   const bool want_pre = P.out[1] != nullptr;
   const bool row_ok = e.row0 + e.lane < P.M;
-  const uint32_t pbuf = e.stg + 4096u;
+  const uint32_t pbuf = e.stg + 2048u;
   float mx = 0.f;
 #pragma unroll 1
   for (int c = cb; c < ce; c += 32) {
@@ -533,16 +547,19 @@ __device__ __forceinline__ void epi_act_f8(const Params& p, const EpiUnit& P, co
       }
       q[j] = w;
     }
-    // the previous chunk's preact box (and the previous tile's code box)
-    // must have been read before they are overwritten
+    // the previous chunk's preact box (and the last stored code box) must
+    // have been read before they are overwritten
     staging_acquire(e);
-    stage_f8_chunk(e.stg, e.lane, (c - cb) >> 5, q);
+    const int k = (c - cb) >> 5;  // chunk of the warp's columns
+    stage_f8_half(e.stg, e.lane, k & 1, q);
     if (want_pre) {
       stage_bf16(pbuf, e.lane, pp);
       store_box(p, P, e, 1, pbuf, col);
     }
+    // a code box goes out once both of its chunks are staged, or after the
+    // warp's last chunk (TMA clips it at the output's edge)
+    if ((k & 1) || c + 32 >= ce || col + 32 >= P.N) store_f8_tile(P, e, 0, e.stg, col - 32 * (k & 1));
   }
-  if (col0 + cb < P.N) store_f8_tile(P, e, 0, e.stg, col0 + cb);
   if (P.amax) {
     if (!row_ok) mx = 0.f;
 #pragma unroll

@@ -256,11 +256,14 @@ struct Gemm {
     return nmaps++;
   }
   // 8-bit epilogue output [rows, cols]: one 32-row x 128-byte box per warp
-  // and tile, 128-byte swizzle.
-  int output_u8(void* ptr, int rows, int cols) {
+  // and tile, 128-byte swizzle; half = true: 32-row x 64-byte boxes, two per
+  // warp and tile, 64-byte swizzle.
+  int output_u8(void* ptr, int rows, int cols, bool half = false) {
     if (!ptr) return -1;
     if (nmaps >= MAX_MAPS) { ok = false; return -1; }
-    if (!make_map(&p.maps[nmaps], ptr, cols, rows, cols, 128, 32, 2)) ok = false;
+    if (!make_map(&p.maps[nmaps], ptr, cols, rows, cols, half ? 64 : 128, 32, 2,
+                  half ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+      ok = false;
     return nmaps++;
   }
   // Epilogue output [rows, cols] (row pitch cols), stored in 32 x 32 boxes;
@@ -1017,7 +1020,7 @@ int mlp_fp8_fwd(const mlp_problem_t* p, const void* x8, const void* W1_8, const 
     Gemm g(*p, c.counter(), c.status, pick_cg(M));
     const int mA = g.kmajor_a_u8(x8, M, H);
     const int mB = g.kmajor_u8(W1_8, I, H, g.b_rows());
-    const int oA = g.output_u8(a8, M, I);
+    const int oA = g.output_u8(a8, M, I, true);  // the fc1 epilogue stores half tiles
     const int oP = g.output(pre_save, M, I);
     Prob& P = g.add(M, I, H, 0, MMA_N, 1, 2 * BK);
     P.mapA0 = mA;
