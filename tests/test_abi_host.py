@@ -182,7 +182,14 @@ def test_kernel_names_and_empty_trace(L):
     assert m.mlp_kernel_name(8) == "rstd"
     assert m.mlp_kernel_name(9) == "rmsnorm_bwd"
     assert m.mlp_kernel_name(10) == "quant_f8"
+    assert m.mlp_kernel_name(11) == "fwd_fused"
     assert m.mlp_kernel_name(99) == "unknown"
+    # every tag the header declares has a name of its own
+    hdr = open(os.path.join(ROOT, "include", "mlp.h")).read()
+    tags = [int(v) for v in re.findall(r"MLP_KERNEL_\w+ = (\d+)", hdr)]
+    assert tags == list(range(len(tags)))
+    names = [m.mlp_kernel_name(t) for t in tags]
+    assert "unknown" not in names and len(set(names)) == len(names)
     assert m.mlp_trace_read() == []  # nothing recorded: no CUDA call is made
 
 
