@@ -26,6 +26,7 @@ __all__ = [
     "Block", "block", "mlp_block_fwd", "mlp_block_bwd", "mlp_fp8_quantize", "mlp_fp8_fwd",
     "MODE_FP8_FWD", "mlp_fp8_bwd", "MODE_FP8_BWD",
     "NOALLOC_SCRATCH_BYTES", "mlp_set_wait_timeout_ms", "mlp_debug_set_flags", "DEBUG_NO_WORK",
+    "mlp_noalloc_status", "mlp_fp8_refresh_scales", "Plan", "mlp_plan", "mlp_debug_hold_sms",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -56,6 +57,16 @@ class Block(ctypes.Structure):
     """mlp_block_t: y = resid_lambda * x + post_lambda * MLP(x / sqrt(mean x^2 + eps))"""
     _fields_ = [("resid_lambda", ctypes.c_float), ("post_lambda", ctypes.c_float),
                 ("eps", ctypes.c_float)]
+
+
+class Plan(ctypes.Structure):
+    """mlp_plan_t: what one call launches (see mlp_plan)."""
+    _fields_ = [("decode", ctypes.c_int), ("fused_forward", ctypes.c_int),
+                ("cta_group", ctypes.c_int), ("out_split", ctypes.c_int),
+                ("wgrad_cta_group", ctypes.c_int), ("wgrad_split", ctypes.c_int)]
+
+    def as_dict(self):
+        return {k: int(getattr(self, k)) for k, _ in self._fields_}
 
 
 _LIB = None
@@ -101,6 +112,15 @@ def lib():
     L.mlp_version.restype = ctypes.c_char_p
     L.mlp_fwd_infer_noalloc.argtypes = [P] + [_VP] * 5 + [_VP]
     L.mlp_fwd_infer_noalloc.restype = ctypes.c_int
+    L.mlp_noalloc_status.argtypes = [_VP]
+    L.mlp_noalloc_status.restype = ctypes.c_int
+    L.mlp_fp8_refresh_scales.argtypes = [_VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                         ctypes.c_float, _VP]
+    L.mlp_fp8_refresh_scales.restype = ctypes.c_int
+    L.mlp_plan.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Plan)]
+    L.mlp_plan.restype = ctypes.c_int
+    L.mlp_debug_hold_sms.argtypes = [ctypes.c_int, ctypes.c_uint, _VP]
+    L.mlp_debug_hold_sms.restype = ctypes.c_int
     L.mlp_set_wait_timeout_ms.argtypes = [ctypes.c_uint]
     L.mlp_set_wait_timeout_ms.restype = ctypes.c_int
     L.mlp_debug_set_flags.argtypes = [ctypes.c_int]
@@ -316,6 +336,34 @@ def mlp_fp8_bwd(prob: Problem, dout, x8, W1_8, W2_8, pre, a8, scales, dx=None, d
     return ws
 
 
+def mlp_fp8_refresh_scales(amax, scale, gain, floor, stream=None) -> None:
+    """The delayed-scale refresh on the device: amax fp32 [n] or [n, width],
+    scale fp32 [n]; scale = max(a * gain, floor) where the slot's amax a is
+    finite and > 0, and the amax is cleared (gpt.py _refresh_delayed_scale)."""
+    n = scale.numel()
+    width = amax.numel() // n if n else 1
+    if n and amax.numel() != n * width:
+        raise ValueError("amax must hold n * width values")
+    rc = lib().mlp_fp8_refresh_scales(_ptr(amax, torch.float32, "amax"),
+                                      _ptr(scale, torch.float32, "scale"), int(n), int(width),
+                                      float(gain), float(floor), _stream(stream))
+    _check(rc, "mlp_fp8_refresh_scales")
+
+
+def mlp_plan(prob: Problem, mode: int, fuse_grad_accum: bool = False) -> dict:
+    """What one call in `mode` launches on the current device (mlp_plan_t as a dict)."""
+    plan = Plan()
+    rc = lib().mlp_plan(ctypes.byref(prob), int(mode), int(bool(fuse_grad_accum)),
+                        ctypes.byref(plan))
+    _check(rc, "mlp_plan")
+    return plan.as_dict()
+
+
+def mlp_debug_hold_sms(ctas: int, us: int, stream=None) -> None:
+    """Testing hook: keep `ctas` SMs busy for `us` microseconds on `stream`."""
+    _check(lib().mlp_debug_hold_sms(int(ctas), int(us), _stream(stream)), "mlp_debug_hold_sms")
+
+
 def mlp_device_status(ws, stream=None) -> int:
     """Synchronises the stream and returns the device status word (0 = OK)."""
     return int(lib().mlp_device_status(ws.data_ptr(), _stream(stream)))
@@ -358,6 +406,12 @@ def mlp_fwd_infer_noalloc(prob: Problem, x, Wg, Wu, Wd, out, stream=None) -> Non
                                      _ptr(Wu, name="Wu"), _ptr(Wd, name="Wd"),
                                      _ptr(out, name="out"), _stream(stream))
     _check(rc, "mlp_fwd_infer_noalloc")
+
+
+def mlp_noalloc_status(stream=None) -> int:
+    """Synchronises the stream and returns the status word of
+    mlp_fwd_infer_noalloc's scratch on the current device (0 = OK)."""
+    return int(lib().mlp_noalloc_status(_stream(stream)))
 
 
 def mlp_set_wait_timeout_ms(ms: int) -> None:

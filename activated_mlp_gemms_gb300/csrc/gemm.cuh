@@ -4,7 +4,8 @@
 // One CTA per SM (320 threads, up to 227 KB shared memory, all 512 TMEM
 // columns):
 //   warp 0     TMA producer and tile scheduler: fetches work units from a
-//              global atomic counter (first unit = blockIdx.x), publishes
+//              global atomic counter (the first one is the cluster id, except
+//              in the one-launch forward), publishes
 //              them through a shared-memory ring, and streams the A/B
 //              k-blocks of each unit into a ring of as many stages as fit
 //              beside the epilogue's staging buffers (six 32 KB stages for
@@ -875,7 +876,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // Work units come from the atomic counter.  A cluster's first unit is its
+  // cluster id, so it starts without the atomic's round trip and a launch of
+  // about one unit per cluster gets one unit to each cluster however late
+  // some start; the units of such launches do not depend on one another.
+  // The fused forward's down units wait for gate/up tiles, so there every
+  // unit, the first included, is claimed from the counter: a cluster that is
+  // not resident yet owns no unit, and a down unit only ever waits for
+  // gate/up tiles that running clusters have claimed.  (The counter was
+  // cleared before the call's first kernel started, so this claim need not
+  // wait for the previous kernel.)
+  constexpr bool CLAIM_ALL = EPI == EPI_FWD_FUSED;
+  int first_unit = static_cast<int>(blockIdx.x) / CG;
   if (warp == 0 && lane == 0) {
+    if (CLAIM_ALL && leader) first_unit = atomicAdd(p.counter, 1);
     for (int i = 0; i < p.nmaps; ++i) prefetch_tmap(&p.maps[i]);
   }
   if (warp == 1) {
@@ -894,7 +908,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
 
   const uint64_t lim = p.timeout_ns;
   const int ncl = gridDim.x / CG;          // clusters (CTA groups) in the grid
-  const int cl = blockIdx.x / CG;          // this CTA group
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -906,7 +919,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       int slot = 0;
       uint32_t sphase = 0;
       int issued = 0;  // k-blocks issued (for the drain on abort)
-      int unit = cl;
+      int unit = first_unit;
       bool ok = true;
       // testing hook: publish no work, so the consumers' bounded waits expire
       const bool publish_nothing = leader && (p.debug_flags & 1);
@@ -941,7 +954,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
           }
           if (unit >= p.total_units) break;
           // the next unit, fetched now and needed when it is published
-          const int next = ncl + atomicAdd(p.counter, 1);
+          const int next = (CLAIM_ALL ? 0 : ncl) + atomicAdd(p.counter, 1);
           bool published = !EARLY_PUB;
           const Work w = decode_unit(p, unit);
           const UnitLoads L = unit_loads<EPI, CG>(p, p.prob[w.prob], w, rank);

@@ -132,6 +132,17 @@ cudaError_t launch_f32_to_bf16(const float* src, void* dst, long long n, cudaStr
 cudaError_t launch_quant_f8(const void* src, long long n, const float* scale, void* dst,
                             float* amax, int fmt, cudaStream_t stream, bool pdl);
 
+// The delayed-scale refresh of n slots (amax fp32 [n, width], scale fp32 [n]):
+// scale = max(a * gain, floor) where a = the slot's finite amax (> 0), amax
+// cleared.
+cudaError_t launch_refresh_scales(float* amax, float* scale, int n, int width, float gain,
+                                  float floor_v, cudaStream_t stream, bool pdl);
+
+// Testing: `ctas` CTAs, each holding HOLD_SMEM_BYTES of shared memory (so no
+// GEMM CTA shares its SM), return after `ns` nanoseconds of the global timer.
+constexpr int HOLD_SMEM_BYTES = 120 * 1024;
+cudaError_t launch_hold(int ctas, unsigned long long ns, cudaStream_t stream);
+
 // Decode-sized forward (M <= DECODE_MAX_M) on the CUDA cores: the gate/up
 // (or fc1) pass with its activation (a, and G/U or P when given), and the
 // down projection out = a Wd^T.  `act` is a device activation (Act).  Each

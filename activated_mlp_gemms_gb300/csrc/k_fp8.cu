@@ -75,6 +75,44 @@ cudaError_t launch_quant_f8(const void* src, long long n, const float* scale, vo
   return cudaLaunchKernelEx(&cfg, k_quant_f8<F8_E4M3>, s, n8, scale, d, amax);
 }
 
+// The delayed-scale refresh of gpt.py (_refresh_delayed_scale): per slot i,
+// a = max of the slot's `width` amax values (a NaN among them makes the
+// max NaN, as torch's amax does), NaN and +-inf read as 0 (nan_to_num), a
+// clamped to at most 1e12; the scale becomes max(a * gain, floor) when
+// a > 0 and keeps its value otherwise; the amax values are cleared.  One
+// thread per slot.
+__global__ void __launch_bounds__(128) k_refresh_scales(float* amax, float* scale, int n,
+                                                        int width, float gain, float floor_v) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float* row = amax + static_cast<long long>(i) * width;
+  float a = row[0];
+  for (int j = 1; j < width; ++j) {
+    const float v = row[j];
+    a = (isnan(a) || isnan(v)) ? __int_as_float(0x7fc00000) : fmaxf(a, v);
+  }
+  if (!isfinite(a)) a = 0.f;
+  a = fminf(a, 1e12f);
+  if (a > 0.f) scale[i] = fmaxf(a * gain, floor_v);
+  for (int j = 0; j < width; ++j) row[j] = 0.f;
+}
+
+cudaError_t launch_refresh_scales(float* amax, float* scale, int n, int width, float gain,
+                                  float floor_v, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((n + 127) / 128), 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_refresh_scales, amax, scale, n, width, gain, floor_v);
+}
+
 template cudaError_t launch_gemm<EPI_ACT_FWD_F8, false, false, 1, ACT_RELU_SQ>(const Params&, int, cudaStream_t, bool);
 template int max_groups<EPI_ACT_FWD_F8, false, false, 1, ACT_RELU_SQ>();
 template cudaError_t launch_gemm<EPI_ACT_FWD_F8, false, false, 2, ACT_RELU_SQ>(const Params&, int, cudaStream_t, bool);

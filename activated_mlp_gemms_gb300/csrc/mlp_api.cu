@@ -550,6 +550,27 @@ int check_ws(const mlp_problem_t* p, int mode, const void* ws, size_t ws_bytes) 
   return MLP_OK;
 }
 
+// Output tiles (256 columns, 128 x cg rows) of a GEMM output [rows, cols].
+long long out_tiles(int rows, int cols, int cg) {
+  return (long long)((rows + BM * cg - 1) / (BM * cg)) * ((cols + MMA_N - 1) / MMA_N);
+}
+
+// Split-K factor of the weight-gradient launch: when its output tiles cannot
+// fill the GPU, the token reduction (K = M) is split so that the work units
+// do, with at least 8 k-blocks per unit (fp32 accumulation only: the
+// partial sums meet through atomic adds in dW).
+int wgrad_split(int M, long long tiles, int cg, int fuse) {
+  if (!fuse || tiles <= 0) return 1;
+  const int slots = num_sms() / cg;
+  const int kb = (M + BK - 1) / BK;
+  int ksplit = 1;
+  if (tiles < slots) {
+    ksplit = (int)(slots / tiles);
+    while (ksplit > 1 && kb / ksplit < 8) --ksplit;
+  }
+  return ksplit;
+}
+
 int begin_call(Call& c, void* ws, void* stream) {
   c.stream = static_cast<cudaStream_t>(stream);
   c.status = static_cast<int*>(ws);
@@ -902,18 +923,8 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     if (dWu) list[n++] = {dU, I, x, H, dWu};
     if (dWd) list[n++] = {dout, H, a, I, dWd};
     long long tiles = 0;
-    for (int i = 0; i < n; ++i)
-      tiles += (long long)((list[i].rows + BM * g.cg - 1) / (BM * g.cg)) *
-               ((list[i].cols + MMA_N - 1) / MMA_N);
-    // split the token reduction when the output tiles cannot fill the GPU
-    // (fp32 accumulation only: partial sums meet through atomic adds)
-    int ksplit = 1;
-    const int slots = num_sms() / g.cg;
-    const int kb = (M + BK - 1) / BK;
-    if (fuse && tiles < slots) {
-      ksplit = (int)(slots / tiles);
-      while (ksplit > 1 && kb / ksplit < 8) --ksplit;
-    }
+    for (int i = 0; i < n; ++i) tiles += out_tiles(list[i].rows, list[i].cols, g.cg);
+    const int ksplit = wgrad_split(M, tiles, g.cg, fuse);
     for (int i = 0; i < n; ++i) {
       const int mA = g.mnmajor(list[i].A, M, list[i].rows);
       const int mB = g.mnmajor(list[i].B, M, list[i].cols);
@@ -1185,6 +1196,47 @@ int mlp_bwd_recompute(const mlp_problem_t* p, const void* dout, const void* x, c
                   ws, ws_bytes, stream, true);
 }
 
+int mlp_fp8_refresh_scales(float* amax, float* scale, int n, int width, float gain,
+                           float floor_v, void* stream) {
+  if (n < 0 || width < 1 || !amax || !scale) return MLP_ERR_INVALID_ARG;
+  if (!std::isfinite(gain) || !std::isfinite(floor_v)) return MLP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(amax) & 3u) || (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return MLP_ERR_ALIGNMENT;
+  if (n == 0) return MLP_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return traced(MLP_KERNEL_REFRESH, s, [&] {
+    return launch_refresh_scales(amax, scale, n, width, gain, floor_v, s, false);
+  });
+}
+
+int mlp_plan(const mlp_problem_t* p, int mode, int fuse_grad_accum, mlp_plan_t* plan) {
+  if (!plan || check_problem(p) != MLP_OK) return MLP_ERR_INVALID_ARG;
+  if (mode < MLP_MODE_FWD || mode > MLP_MODE_FP8_BWD) return MLP_ERR_INVALID_ARG;
+  if (fuse_grad_accum != 0 && fuse_grad_accum != 1) return MLP_ERR_INVALID_ARG;
+  if (num_sms() <= 0) return MLP_ERR_CUDA;
+  std::memset(plan, 0, sizeof(*plan));
+  const bool fp8 = mode == MLP_MODE_FP8_FWD || mode == MLP_MODE_FP8_BWD;
+  const bool fwd = mode == MLP_MODE_FWD || mode == MLP_MODE_INFER;
+  plan->decode = (fwd && decode_path(p)) ? 1 : 0;
+  plan->cta_group = pick_cg(p->M);
+  plan->out_split = (fp8 || plan->decode) ? 1 : bf16_split(p->M, p->H, split_k_of(p, mode));
+  plan->fused_forward = (fwd && !plan->decode && fused_forward(p, plan->out_split)) ? 1 : 0;
+  if (!fwd && mode != MLP_MODE_FP8_FWD) {
+    const int cg = pick_cg(p->H < p->I ? p->H : p->I);
+    long long tiles = out_tiles(p->I, p->H, cg) + out_tiles(p->H, p->I, cg);
+    if (gated(p) && !fp8) tiles += out_tiles(p->I, p->H, cg);
+    plan->wgrad_cta_group = cg;
+    plan->wgrad_split = fp8 ? 1 : wgrad_split(p->M, tiles, cg, fuse_grad_accum);
+  }
+  return MLP_OK;
+}
+
+int mlp_debug_hold_sms(int ctas, unsigned int us, void* stream) {
+  if (ctas < 1 || ctas > 65535) return MLP_ERR_INVALID_ARG;
+  const unsigned long long ns = (us > 10000000u ? 10000000ull : (unsigned long long)us) * 1000ull;
+  return cuda_err(launch_hold(ctas, ns, static_cast<cudaStream_t>(stream)));
+}
+
 const char* mlp_status_string(int s) {
   switch (s) {
     case MLP_OK: return "MLP_OK";
@@ -1269,6 +1321,7 @@ const char* mlp_kernel_name(int tag) {
     case MLP_KERNEL_RMSNORM_BWD: return "rmsnorm_bwd";
     case MLP_KERNEL_QUANT: return "quant_f8";
     case MLP_KERNEL_FWD_FUSED: return "fwd_fused";
+    case MLP_KERNEL_REFRESH: return "refresh_scales";
     default: return "unknown";
   }
 }

@@ -10,11 +10,11 @@
 // The scratch is the file-scope array below, MLP_NOALLOC_SCRATCH_BYTES long.
 // It lives in every device that loads this library, from module load until
 // the process exits.  Host code cannot use the array's name as a device
-// address (in host code it names a host-side shadow), so its device address
-// is fetched with cudaGetSymbolAddress once per device, with that device
-// current, on the first call made on that device, and cached.
-#include <mutex>
-
+// address (in host code it names a host-side shadow), so every call fetches
+// the array's device address on the current device with
+// cudaGetSymbolAddress (cheap once the module is loaded; a cached address
+// would go stale after a device reset).  Its first 4 bytes are the status
+// word that mlp_noalloc_status reads.
 #include "mlp.h"
 
 namespace {
@@ -23,21 +23,11 @@ constexpr size_t kScratchBytes = MLP_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch[kMaxDevices] = {nullptr};
-
 // Device address of the scratch array on the current device (nullptr on error).
 void* scratch_for_current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_scratch[dev] = ptr;
-  }
-  return g_scratch[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+  return ptr;
 }
 
 }  // namespace
@@ -52,4 +42,10 @@ extern "C" int mlp_fwd_infer_noalloc(const mlp_problem_t* p, const void* x, cons
   // mlp_fwd_infer clears the status word and scheduler counters at the start
   // of the scratch on the stream, and overwrites the postact before reading it.
   return mlp_fwd_infer(p, x, Wg, Wu, Wd, out, ws, kScratchBytes, stream);
+}
+
+extern "C" int mlp_noalloc_status(void* stream) {
+  void* ws = scratch_for_current_device();
+  if (!ws) return MLP_ERR_CUDA;
+  return mlp_device_status(ws, stream);
 }

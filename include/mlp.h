@@ -296,6 +296,24 @@ int mlp_fp8_bwd(const mlp_problem_t* p, const void* dout, const void* x8, const 
                 const void* W2_8, const void* pre, const void* a8, const float* scales, void* dx,
                 void* dW1, void* dW2, float* amax_dpre, void* ws, size_t ws_bytes, void* stream);
 
+/* Delayed-scale refresh (modded-nanogpt gpt.py, _refresh_delayed_scale, as
+ * _quantize_mlp_weights_and_scales calls it after every optimizer step): for
+ * each of n slots, a = the largest of the slot's `width` recorded amax values
+ * (amax is fp32 [n, width], row-major; a NaN or an infinity among them makes
+ * a = 0), clamped to at most 1e12; if a > 0 the slot's scale becomes
+ * max(a * gain, floor), else it keeps its value; then the slot's amax values
+ * are set to 0.  The page's two uses, with the amax that mlp_fp8_fwd and
+ * mlp_fp8_bwd record:
+ *   s_post (scales[3]): amax_a,    gain = 1.03 / 448,    floor = 1e-6
+ *   s_dpre (scales[5]): amax_dpre, gain = 1.25 / 57344,  floor = 1e-12
+ * One small kernel on `stream`: a training loop can keep the refresh on the
+ * device (and inside a captured CUDA graph) instead of reading the amax on
+ * the host.  amax and scale: device fp32, 4-byte aligned, not overlapping.
+ * n = 0 enqueues nothing; n < 0, width < 1, a NULL pointer or a non-finite
+ * gain or floor is MLP_ERR_INVALID_ARG. */
+int mlp_fp8_refresh_scales(float* amax, float* scale, int n, int width, float gain, float floor,
+                           void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mlp_status_string(int status);
 
@@ -320,9 +338,11 @@ const char* mlp_version(void);
  *     mlp_workspace_size(p, MLP_MODE_INFER) exceeds
  *     MLP_NOALLOC_SCRATCH_BYTES (about M * I <= 8.3 million elements).
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress, with that device current), so the address stays
+ *     right after a device reset; the first lookup on a device may load the
+ *     library's device code, so make the first call before any stream
+ *     capture.
  *   - All calls share the one array: it keeps the last call's contents, and
  *     each call clears the parts that must start at zero.  Calls whose work
  *     overlaps on the GPU (different streams, or without ordering) race on
@@ -330,6 +350,30 @@ const char* mlp_version(void);
 #define MLP_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 int mlp_fwd_infer_noalloc(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu,
                           const void* Wd, void* out, void* stream);
+
+/* The device status word of mlp_fwd_infer_noalloc's scratch on the current
+ * device, as mlp_device_status reads a workspace's: synchronises `stream`,
+ * then returns MLP_OK, or MLP_ERR_TIMEOUT when a bounded wait of the last
+ * call expired (its output is then incomplete), or MLP_ERR_CUDA.  The word
+ * is cleared at the start of every call. */
+int mlp_noalloc_status(void* stream);
+
+/* ---- Launch plan (introspection; no counterpart on the pages) ----
+ * What one call in `mode` launches for problem `p` on the current device,
+ * with every gradient requested (the backward modes) and the current tile
+ * policy.  The split-K factors depend on the device's SM count. */
+typedef struct {
+  int decode;           /* 1: the forward streams the weights on the CUDA cores (1-4 tokens) */
+  int fused_forward;    /* 1: the gated forward's gate/up and down GEMMs are one launch */
+  int cta_group;        /* CTA-group size (1 or 2) of the GEMMs over token rows */
+  int out_split;        /* split-K factor of the [M,H] output GEMM (down projection, or dx) */
+  int wgrad_cta_group;  /* CTA-group size of the weight-gradient launch */
+  int wgrad_split;      /* split-K factor of the weight-gradient launch (> 1 only when
+                           fuse_grad_accum: the splits meet by fp32 atomic adds in dW) */
+} mlp_plan_t;
+/* Fills *plan; MLP_ERR_INVALID_ARG for an invalid problem, mode or a NULL
+ * plan, MLP_ERR_CUDA when no device can be queried.  Enqueues nothing. */
+int mlp_plan(const mlp_problem_t* p, int mode, int fuse_grad_accum, mlp_plan_t* plan);
 
 /* Tile policy (a tuning and testing knob; no counterpart on the pages):
  * 0 = automatic (default): GEMMs whose output has more than 128 rows use
@@ -358,6 +402,16 @@ int mlp_set_tile_policy(int policy);
 int mlp_set_wait_timeout_ms(unsigned int ms);
 int mlp_debug_set_flags(int flags);
 
+/* Contention hook (testing): enqueues on `stream` one kernel of `ctas` CTAs
+ * that each take enough shared memory to keep any GEMM CTA of this library
+ * off their SM, and return after `us` microseconds (read from the GPU's
+ * global timer; at most 10 s).  Work launched meanwhile on other streams
+ * runs on the SMs left free: this tests that the kernels finish correctly
+ * when only part of their grid is resident.  The kernel reads and writes no
+ * memory and waits on nothing but the timer.  ctas in 1..65535, else
+ * MLP_ERR_INVALID_ARG. */
+int mlp_debug_hold_sms(int ctas, unsigned int us, void* stream);
+
 /* ---- Tracing (timing support; no counterpart on the pages) ----
  * With tracing on, every kernel launch of the calls above is bracketed by
  * a pair of CUDA events recorded on the call's stream (this may keep
@@ -378,9 +432,10 @@ typedef enum {
   MLP_KERNEL_RSTD = 8,          /* the block's per-token RMS-norm scale */
   MLP_KERNEL_RMSNORM_BWD = 9,   /* the block's RMS-norm derivative and residual gradient */
   MLP_KERNEL_QUANT = 10,        /* bf16 -> e4m3 / e5m2 quantisation */
-  MLP_KERNEL_FWD_FUSED = 11     /* the gated forward's gate/up and down GEMMs in one launch
+  MLP_KERNEL_FWD_FUSED = 11,    /* the gated forward's gate/up and down GEMMs in one launch
                                    (CTA-pair tiles, M <= 32768): a down tile starts once the
                                    postact of its 256 rows is stored */
+  MLP_KERNEL_REFRESH = 12       /* the FP8 delayed-scale refresh */
 } mlp_kernel_t;
 
 /* on != 0 starts recording, 0 stops (records already taken are kept). */

@@ -36,7 +36,9 @@ def test_header_declares_the_abi():
                             "mlp_kernel_name", "mlp_set_tile_policy",
                             "mlp_fwd_infer_noalloc", "mlp_set_wait_timeout_ms",
                             "mlp_debug_set_flags", "mlp_block_fwd", "mlp_block_bwd",
-                            "mlp_fp8_quantize", "mlp_fp8_fwd", "mlp_fp8_bwd"])
+                            "mlp_fp8_quantize", "mlp_fp8_fwd", "mlp_fp8_bwd",
+                            "mlp_fp8_refresh_scales", "mlp_plan", "mlp_debug_hold_sms",
+                            "mlp_noalloc_status"])
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -204,3 +206,28 @@ def test_debug_hooks_validate(L):
     assert L.mlp_debug_set_flags(2) == -1
     assert L.mlp_debug_set_flags(0) == 0
     assert L.mlp_set_wait_timeout_ms(0) == 0
+
+
+def test_refresh_scales_validates(L):
+    # rejected before any launch (fake, never-dereferenced pointers)
+    r = L.mlp_fp8_refresh_scales
+    assert r(FAKE, FAKE, -1, 1, 1.0, 0.0, None) == -1
+    assert r(FAKE, FAKE, 1, 0, 1.0, 0.0, None) == -1
+    assert r(None, FAKE, 1, 1, 1.0, 0.0, None) == -1
+    assert r(FAKE, None, 1, 1, 1.0, 0.0, None) == -1
+    assert r(FAKE, FAKE, 1, 1, float("inf"), 0.0, None) == -1
+    assert r(FAKE, FAKE, 1, 1, 1.0, float("nan"), None) == -1
+    assert r(FAKE + 2, FAKE, 1, 1, 1.0, 0.0, None) == -2
+    assert r(FAKE, FAKE, 0, 1, 1.0, 0.0, None) == 0  # nothing to do: nothing enqueued
+    assert m.mlp_kernel_name(12) == "refresh_scales"
+
+
+def test_plan_and_hold_validate(L):
+    plan = m.Plan()
+    p = m.problem(2048, 4096, 11008)
+    assert L.mlp_plan(ctypes.byref(p), m.MODE_FWD, 0, None) == -1
+    assert L.mlp_plan(ctypes.byref(p), 9, 0, ctypes.byref(plan)) == -1
+    assert L.mlp_plan(ctypes.byref(p), m.MODE_BWD, 2, ctypes.byref(plan)) == -1
+    assert L.mlp_plan(ctypes.byref(m.problem(0, 8, 8)), 0, 0, ctypes.byref(plan)) == -1
+    assert L.mlp_debug_hold_sms(0, 10, None) == -1
+    assert L.mlp_debug_hold_sms(70000, 10, None) == -1

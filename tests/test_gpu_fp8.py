@@ -7,6 +7,7 @@ import torch
 
 import activated_mlp_gemms_gb300 as m
 from activated_mlp_gemms_gb300.workloads import make_inputs, to_f64
+from mlp_gpu_helpers import SAMPLE_ROWS, SAMPLE_UNITS, spread_sample
 from oracle import (E4M3_MAX, E5M2_MAX, fp8_relu_sq_backward, fp8_relu_sq_forward, quantize,
                     rel_err)
 
@@ -404,11 +405,8 @@ def test_fp8_full_size_sampled():
     sx = 2.0 ** -4
     s1, s2 = f32(np.max(np.abs(W1d)) / E4M3_MAX), f32(np.max(np.abs(W2d)) / E4M3_MAX)
     xc, W1c, W2c = quantize(xd, sx), quantize(W1d, s1), quantize(W2d, s2)
-    rng = np.random.default_rng(0)
-    rows = np.sort(rng.choice(M, size=48, replace=False))
-    rows[0], rows[-1] = 0, M - 1
-    units = np.sort(rng.choice(I, size=24, replace=False))
-    units[0], units[-1] = 0, I - 1
+    rows = spread_sample(M, SAMPLE_ROWS)
+    units = spread_sample(I, SAMPLE_UNITS)
 
     def round_pre(v):  # the saved preact's bf16 rounding
         return to_f64(torch.tensor(v, dtype=torch.float64).to(torch.bfloat16))
@@ -443,3 +441,112 @@ def test_fp8_full_size_sampled():
     assert all(e <= 2e-2 for e in errs.values()), errs
     for v in (out, dx, dW1, dW2):
         assert torch.isfinite(v.float()).all()
+
+
+def _refresh_host(amax, scale, gain, floor):
+    """gpt.py's _refresh_delayed_scale restated on the host in fp32: the
+    slot's amax (max over its row, NaN propagating), NaN / +-inf -> 0, at
+    most 1e12; scale = max(a * gain, floor) where a > 0, else unchanged."""
+    f = np.float32
+    a = np.max(amax.astype(f), axis=1)
+    a = np.nan_to_num(a, nan=0.0, posinf=0.0, neginf=0.0).astype(f)
+    a = np.minimum(a, f(1e12))
+    new = np.maximum(a * f(gain), f(floor))
+    return np.where(a > 0, new, scale.astype(f)).astype(f)
+
+
+@pytest.mark.parametrize("width", [1, 3])
+def test_refresh_scales_matches_host_restatement(width):
+    inf, nan = float("inf"), float("nan")
+    rows = [[2.5], [0.0], [nan], [inf], [-inf], [-1.0], [3e13], [1e-9], [448.0], [6e-7]]
+    rng = np.random.default_rng(70)
+    amax = np.array([r * width for r in rows], dtype=np.float32)
+    if width > 1:
+        amax[:, 1:] = rng.uniform(0, 4, size=(len(rows), width - 1)).astype(np.float32)
+        amax[2, 2] = nan  # a NaN anywhere in the row
+    scale = rng.uniform(0.5, 2.0, size=len(rows)).astype(np.float32)
+    for gain, floor in ((1.03 / 448.0, 1e-6), (1.25 / 57344.0, 1e-12)):
+        a_d = torch.tensor(amax, device="cuda")
+        s_d = torch.tensor(scale, device="cuda")
+        m.mlp_fp8_refresh_scales(a_d, s_d, gain, floor)
+        torch.cuda.synchronize()
+        want = _refresh_host(amax, scale, gain, floor)
+        got = s_d.cpu().numpy()
+        assert np.array_equal(got.view(np.int32), want.view(np.int32)), (got, want)
+        assert (a_d == 0).all()
+
+
+def test_fp8_training_loop_in_a_graph_needs_no_host_sync():
+    """Three FP8 training steps (forward saving the preact, backward, then the
+    delayed-scale refresh of s_post and s_dpre from the amaxes the kernels
+    recorded) as one captured CUDA graph replayed three times back to back,
+    against the same steps run eagerly with the refresh restated on the
+    host between them: the scales, amaxes and every output agree bit for
+    bit.  The first scales are deliberately off (1.0)."""
+    M, H, I = 512, 256, 512
+    t = make_inputs(M, H, I, "relu_sq", seed=71)
+    xd, W1d, W2d = to_f64(t["x"]), to_f64(t["Wg"]), to_f64(t["Wd"])
+    f32 = lambda v: float(np.float32(v))  # noqa: E731
+    sx = 2.0 ** -4
+    s1, s2 = f32(np.max(np.abs(W1d)) / E4M3_MAX), f32(np.max(np.abs(W2d)) / E4M3_MAX)
+    x8, W1_8, W2_8 = (_f8_bytes(quantize(v, s), torch.float8_e4m3fn)
+                      for v, s in ((xd, sx), (W1d, s1), (W2d, s2)))
+    dout = t["dout"].cuda()
+    prob = m.problem(M, H, I, "relu_sq")
+    bf = torch.bfloat16
+    G_POST, F_POST = 1.03 / E4M3_MAX, 1e-6
+    G_DPRE, F_DPRE = 1.25 / E5M2_MAX, 1e-12
+
+    def state():
+        return {"scales": torch.tensor([sx, s1, s2, 1.0, 2.0 ** -6, 1.0], dtype=torch.float32,
+                                       device="cuda"),
+                "amax_a": torch.zeros(1, dtype=torch.float32, device="cuda"),
+                "amax_d": torch.zeros(1, dtype=torch.float32, device="cuda"),
+                "out": torch.empty(M, H, dtype=bf, device="cuda"),
+                "pre": torch.empty(M, I, dtype=bf, device="cuda"),
+                "a8": torch.empty(M, I, dtype=torch.uint8, device="cuda"),
+                "dx": torch.empty(M, H, dtype=bf, device="cuda"),
+                "dW1": torch.empty(I, H, dtype=bf, device="cuda"),
+                "dW2": torch.empty(H, I, dtype=bf, device="cuda"),
+                "wsf": m.alloc_workspace(prob, m.MODE_FP8_FWD),
+                "wsb": m.alloc_workspace(prob, m.MODE_FP8_BWD)}
+
+    def step(s):
+        m.mlp_fp8_fwd(prob, x8, W1_8, W2_8, s["scales"], s["out"], s["a8"], s["amax_a"],
+                      ws=s["wsf"], pre_save=s["pre"])
+        m.mlp_fp8_bwd(prob, dout, x8, W1_8, W2_8, s["pre"], s["a8"], s["scales"], s["dx"],
+                      s["dW1"], s["dW2"], s["amax_d"], ws=s["wsb"])
+
+    # eager: the refresh on the host after each step
+    e = state()
+    for _ in range(3):
+        step(e)
+        torch.cuda.synchronize()
+        sc = e["scales"].cpu().numpy()
+        sc[3] = _refresh_host(e["amax_a"].cpu().numpy()[None, :], sc[3:4], G_POST, F_POST)[0]
+        sc[5] = _refresh_host(e["amax_d"].cpu().numpy()[None, :], sc[5:6], G_DPRE, F_DPRE)[0]
+        e["scales"].copy_(torch.from_numpy(sc))
+        e["amax_a"].zero_()
+        e["amax_d"].zero_()
+    torch.cuda.synchronize()
+
+    # graph: the whole step including the refresh on the device
+    g = state()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # a direct call first sets up the library's caches
+        step(state())
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(g)
+        m.mlp_fp8_refresh_scales(g["amax_a"], g["scales"][3:4], G_POST, F_POST)
+        m.mlp_fp8_refresh_scales(g["amax_d"], g["scales"][5:6], G_DPRE, F_DPRE)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert float(e["scales"][3]) != 1.0 and float(e["scales"][5]) != 1.0
+    for k in ("scales", "amax_a", "amax_d", "out", "pre", "a8", "dx", "dW1", "dW2"):
+        assert torch.equal(g[k], e[k]), k
+    assert m.mlp_device_status(g["wsb"]) == 0

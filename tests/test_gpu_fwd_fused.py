@@ -5,6 +5,8 @@ launches (tile policy 3) and against the fp64 oracle, through the C ABI.
 Both schedules run the same tile computations in the same accumulation
 order, so their outputs are bitwise equal; the oracle comparison is the
 parity bar of the other tests."""
+import time
+
 import pytest
 import torch
 
@@ -148,3 +150,44 @@ def test_fused_forward_graph_replays():
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
     assert m.mlp_device_status(ws) == 0
+
+
+def test_fused_forward_with_most_sms_held_by_another_stream():
+    """The one-launch forward when only part of its grid is resident: a
+    kernel on another stream keeps all but 40 SMs busy for 400 ms, far longer
+    than the 100 ms bound put on the forward's waits.  Every work unit is
+    claimed from the scheduler's counter, so the down units only wait for
+    gate/up tiles that resident CTA pairs have claimed: the forward completes
+    on the free SMs, with status 0 and the same output as without
+    contention.  (With a unit per pair fixed in advance, the pairs that are
+    not resident would own gate/up tiles the down units wait for, and the
+    waits would expire.)"""
+    M, H, I, act = 2048, 1024, 4096, "swiglu"
+    t = make_inputs(M, H, I, act, seed=44)
+    d = dev_tensors(t)
+    prob = m.problem(M, H, I, act)
+    assert m.mlp_plan(prob, m.MODE_FWD)["fused_forward"] == 1
+    ref = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    m.mlp_fwd_infer(prob, d["x"], d["Wg"], d["Wu"], d["Wd"], ref)
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    hold = torch.cuda.Stream()
+    work = torch.cuda.Stream()
+    out = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = m.alloc_workspace(prob, m.MODE_INFER)
+    torch.cuda.synchronize()
+    try:
+        m.mlp_set_wait_timeout_ms(100)
+        m.mlp_debug_hold_sms(sms - 40, 400_000, stream=hold)
+        time.sleep(0.02)  # the holding CTAs are resident before the forward starts
+        with torch.cuda.stream(work):
+            m.mlp_fwd_infer(prob, d["x"], d["Wg"], d["Wu"], d["Wd"], out, ws=ws, stream=work)
+        work.synchronize()
+        status = m.mlp_device_status(ws, stream=work)
+        hold_busy = not hold.query()  # the holder was still running when the forward ended
+        torch.cuda.synchronize()
+    finally:
+        m.mlp_set_wait_timeout_ms(0)
+    assert hold_busy, "the forward did not overlap the holding kernel"
+    assert status == 0, m.mlp_status_string(status)
+    assert torch.equal(out, ref)

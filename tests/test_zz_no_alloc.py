@@ -4,11 +4,19 @@ is planned once at start-up, or a serving loop that must not call cudaMalloc
 because it synchronises the device).  Its scratch is a fixed array inside the
 library instead of a caller workspace.
 
-Checked through the C ABI against the existing entry point mlp_fwd_infer, on
-two calls in a row (the array keeps the previous call's contents, so the
-second call must still be right), within the bf16 parity tolerance.  This
-file sorts last so that a run stopping at the first failure has already run
-every other test; it also passes alone in a fresh process."""
+Checked through the C ABI against the existing entry point mlp_fwd_infer,
+on two calls in a row with different inputs: the array keeps the previous
+call's contents, so the second call must still be right.  Both entry points
+run the same kernels in the same order of work, so the outputs are bitwise
+equal, except where the down projection splits K (few output tiles, a long
+K): its fp32 partial sums then meet by atomic adds in no fixed order, and
+the two agree to rounding.  The shapes cover the
+tensor-core path (single-CTA and CTA-pair tiles, the one-launch gated
+forward) and the CUDA-core path of one to four tokens.  The status word of
+the array is read with mlp_noalloc_status, including after a bounded wait
+that was made to expire.  This file sorts last so that a run stopping at the
+first failure has already run every other test; it also passes alone in a
+fresh process."""
 import ctypes
 
 import pytest
@@ -16,21 +24,30 @@ import torch
 
 import activated_mlp_gemms_gb300 as m
 from activated_mlp_gemms_gb300.workloads import make_inputs, to_f64
-from oracle import rel_err
+from oracle import mlp_forward, rel_err
 
 pytestmark = pytest.mark.gpu
-
-TOL_BF16 = 2e-2
 
 
 def _dev(t):
     return {k: (v.cuda() if v is not None else None) for k, v in t.items()}
 
 
+def _ptr(v):
+    return None if v is None else v.data_ptr()
+
+
+def _noalloc(L, prob, t, out, stream):
+    return L.mlp_fwd_infer_noalloc(ctypes.byref(prob), _ptr(t["x"]), _ptr(t["Wg"]),
+                                   _ptr(t["Wu"]), _ptr(t["Wd"]), _ptr(out), stream)
+
+
 @pytest.mark.parametrize("act,gm,dm,shape", [
     ("swiglu", 1.0, 1.0, (300, 264, 392)),
     ("swiglu", 1.125, 2.0, (512, 4096, 14336)),
     ("relu_sq", 1.0, 1.0, (257, 768, 3072)),
+    ("swiglu", 1.0, 1.0, (3, 4096, 14336)),   # one to four tokens: the CUDA-core path
+    ("relu_sq", 1.0, 1.0, (1, 768, 3072)),
 ])
 def test_noalloc_matches_workspace_entry_point(act, gm, dm, shape):
     M, H, I = shape
@@ -38,18 +55,21 @@ def test_noalloc_matches_workspace_entry_point(act, gm, dm, shape):
     prob = m.problem(M, H, I, act, gm, dm)
     assert m.mlp_workspace_size(prob, m.MODE_INFER) <= m.NOALLOC_SCRATCH_BYTES
     stream = torch.cuda.current_stream().cuda_stream
+    split = m.mlp_plan(prob, m.MODE_INFER)["out_split"] > 1
     for seed in (11, 12):  # two calls in a row, different inputs
         t = _dev(make_inputs(M, H, I, act, seed=seed))
         ref = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
         m.mlp_fwd_infer(prob, t["x"], t["Wg"], t["Wu"], t["Wd"], ref)
         got = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device="cuda")
-        ptr = lambda v: None if v is None else v.data_ptr()  # noqa: E731
-        rc = L.mlp_fwd_infer_noalloc(ctypes.byref(prob), ptr(t["x"]), ptr(t["Wg"]), ptr(t["Wu"]),
-                                     ptr(t["Wd"]), ptr(got), stream)
+        rc = _noalloc(L, prob, t, got, stream)
         assert rc == 0, m.mlp_status_string(rc)
+        assert m.mlp_noalloc_status() == 0
         torch.cuda.synchronize()
         assert torch.isfinite(got.float()).all()
-        assert rel_err(to_f64(got), to_f64(ref)) <= TOL_BF16
+        if split:
+            assert rel_err(to_f64(got), to_f64(ref)) <= 1e-2
+        else:
+            assert torch.equal(got, ref)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
@@ -60,3 +80,27 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     rc = L.mlp_fwd_infer_noalloc(ctypes.byref(prob), x.data_ptr(), x.data_ptr(), x.data_ptr(),
                                  x.data_ptr(), x.data_ptr(), None)
     assert rc == -4 and m.mlp_status_string(rc) == "MLP_ERR_WORKSPACE_TOO_SMALL"
+
+
+def test_noalloc_reports_an_expired_wait_and_recovers():
+    """A bounded wait that expires inside a no-alloc call (the schedulers
+    publish no work, so no copy or MMA is issued) is reported through
+    mlp_noalloc_status; the next call clears the word and is correct."""
+    M, H, I = 300, 256, 512
+    t = make_inputs(M, H, I, "swiglu", seed=7)
+    g = _dev(t)
+    prob = m.problem(M, H, I)
+    out = torch.zeros(M, H, dtype=torch.bfloat16, device="cuda")
+    try:
+        m.mlp_set_wait_timeout_ms(100)
+        m.mlp_debug_set_flags(m.DEBUG_NO_WORK)
+        m.mlp_fwd_infer_noalloc(prob, g["x"], g["Wg"], g["Wu"], g["Wd"], out)
+        assert m.mlp_noalloc_status() == -6  # MLP_ERR_TIMEOUT
+    finally:
+        m.mlp_debug_set_flags(0)
+        m.mlp_set_wait_timeout_ms(0)
+    m.mlp_fwd_infer_noalloc(prob, g["x"], g["Wg"], g["Wu"], g["Wd"], out)
+    assert m.mlp_noalloc_status() == 0
+    a = {k: to_f64(v) for k, v in t.items() if v is not None}
+    ref = mlp_forward(a["x"], a["Wg"], a["Wu"], a["Wd"], "swiglu")["out"]
+    assert rel_err(to_f64(out), ref) <= 2e-2
