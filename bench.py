@@ -4,9 +4,14 @@
 One step = one training forward (mlp_fwd) plus one backward (mlp_bwd from
 saved preacts, or mlp_bwd_recompute) of the selected workload, on seeded
 synthetic inputs already resident in HBM.  The L2 cache is flushed (a
-512 MiB write) before every timed step, outside the step's events.
+512 MiB write) before every timed step, outside the step's events.  The
+default workload is the largest, the Llama-3-8B-shaped MLP (8192 tokens,
+4096 x 14336, backward recomputing the preacts), with its no-grad inference
+forward beside it; the other four workloads (and, for the ReLU^2 one, the
+FP8 step and the block with its neighbours) are measured for the breakdown
+with a few steps each unless --headline-only is given.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--headline-only]
     python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host cores
 
 Prints one JSON line.  Under torchrun (N > 1) every rank runs an independent
@@ -39,7 +44,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama7b_swiglu")
+    ap.add_argument("--workload", default="llama3_8b_swiglu")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other workloads' breakdown")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-trace", action="store_true")
@@ -248,108 +255,271 @@ class ClockSampler:
 
 # --------------------------------------------------------------------- ours
 
-def run_ours(args, rank, world, local_rank):
+def kernel_bytes(w):
+    """Algorithmic DRAM bytes per launch of each kernel of a step (bf16
+    tensors read or written once; the fused forward reads its postact back
+    from L2), and of each kernel's epilogue alone (the [M,I] intermediates
+    it reads and writes, and the [M,H] outputs of the down projection and
+    dx).  Returns {kernel: (total, epilogue)}."""
+    M, H, I = float(w.M), float(w.H), float(w.I)
+    g = w.gated
+    nw = 2 if g else 1                      # gate/up weights (or fc1)
+    saved = not w.recompute
+    pre = nw * 2 * M * I                    # the stored preacts G, U (or P)
+    a = 2 * M * I                           # the postact
+    gu_pre = pre if (saved or g) else 0.0   # gate/up kernel: forward saving, or recompute stage 0
+    dw_out = (8 if w.fuse_grad_accum else 2) * (nw + 1) * H * I  # fp32 RMW or bf16 store
+    return {
+        "fwd_fused": (2 * M * H + 2 * nw * H * I + a + (pre if saved else 0.0) + 2 * H * I
+                      + 2 * M * H, a + (pre if saved else 0.0) + 2 * M * H),
+        "gate_up_act": (2 * M * H + 2 * nw * H * I + a + gu_pre, a + gu_pre),
+        "down_proj": (a + 2 * H * I + 2 * M * H, 2 * M * H),
+        "dgated": (2 * M * H + 2 * H * I + 2 * pre + (a if saved else 0.0),
+                   2 * pre + (a if saved else 0.0)),
+        "dact_recompute": (4 * M * H + 4 * H * I + 2 * a, 2 * a),
+        "dx": (pre + 2 * nw * H * I + 2 * M * H, 2 * M * H),
+        "wgrad": (pre + a + 2 * nw * M * H + 2 * M * H + dw_out, dw_out),
+    }
+
+
+class StepBuffers:
+    """Device inputs, outputs and workspaces of one fwd + bwd step of a
+    workload, and the step's two library calls."""
+
+    def __init__(self, m, w, dev):
+        import torch
+        from activated_mlp_gemms_gb300.workloads import workload_inputs
+        self.m, self.w, self.dev = m, w, dev
+        t = workload_inputs(w)
+        self.host = t
+        self.g = {k: (v.to(dev) if v is not None else None) for k, v in t.items()}
+        bf = torch.bfloat16
+        M, H, I = w.M, w.H, w.I
+        self.prob = m.problem(M, H, I, w.act, w.gate_mult, w.down_mult)
+        self.out = torch.empty(M, H, dtype=bf, device=dev)
+        self.dx = torch.empty(M, H, dtype=bf, device=dev)
+        wdt = torch.float32 if w.fuse_grad_accum else bf
+        self.dWg = torch.zeros(I, H, dtype=wdt, device=dev)
+        self.dWu = torch.zeros(I, H, dtype=wdt, device=dev) if w.gated else None
+        self.dWd = torch.zeros(H, I, dtype=wdt, device=dev)
+        if w.fuse_grad_accum:
+            self.dWg.copy_(t["dWg_prev"])
+            self.dWd.copy_(t["dWd_prev"])
+            if self.dWu is not None:
+                self.dWu.copy_(t["dWu_prev"])
+        self.saved = not w.recompute
+        self.G = torch.empty(M, I, dtype=bf, device=dev) if self.saved else None
+        self.U = torch.empty(M, I, dtype=bf, device=dev) if (self.saved and w.gated) else None
+        self.ws_f = m.alloc_workspace(self.prob, m.MODE_FWD, dev)
+        self.ws_b = m.alloc_workspace(self.prob, m.MODE_BWD_RECOMPUTE if w.recompute
+                                      else m.MODE_BWD, dev)
+
+    def fwd(self, x=None, out=None):
+        g = self.g
+        self.m.mlp_fwd(self.prob, g["x"] if x is None else x, g["Wg"], g["Wu"], g["Wd"],
+                       self.out if out is None else out, self.G, self.U, ws=self.ws_f)
+
+    def bwd(self, x=None, dout=None, dx=None):
+        g, w = self.g, self.w
+        x = g["x"] if x is None else x
+        dout = g["dout"] if dout is None else dout
+        dx = self.dx if dx is None else dx
+        if self.saved:
+            self.m.mlp_bwd(self.prob, dout, x, g["Wg"], g["Wu"], g["Wd"], self.G, self.U, dx,
+                           self.dWg, self.dWu, self.dWd, fuse_grad_accum=w.fuse_grad_accum,
+                           ws=self.ws_b)
+        else:
+            self.m.mlp_bwd_recompute(self.prob, dout, x, g["Wg"], g["Wu"], g["Wd"], dx, self.dWg,
+                                     self.dWu, self.dWd, fuse_grad_accum=w.fuse_grad_accum,
+                                     ws=self.ws_b)
+
+
+def time_steps(st, K, warmup, flush, world=1, on_region=None):
+    """Times K fwd + bwd steps of StepBuffers `st` with CUDA events on the
+    launching stream, the L2 flushed before every step outside its events.
+    Returns (fwd_ms list, bwd_ms list, wall seconds, device status)."""
     import torch
     import torch.distributed as dist
-
-    import activated_mlp_gemms_gb300 as m
-    from activated_mlp_gemms_gb300.workloads import WORKLOADS, workload_inputs
-
-    w = WORKLOADS[args.workload]
-    if args.tokens > 0:
-        import dataclasses
-        w = dataclasses.replace(w, M=args.tokens)
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    from activated_mlp_gemms_gb300 import _build
-    _build.build()
-
-    t = workload_inputs(w)
-    g = {k: (v.to(dev) if v is not None else None) for k, v in t.items()}
-    bf = torch.bfloat16
-    M, H, I = w.M, w.H, w.I
-    prob = m.problem(M, H, I, w.act, w.gate_mult, w.down_mult)
-    out = torch.empty(M, H, dtype=bf, device=dev)
-    dx = torch.empty(M, H, dtype=bf, device=dev)
-    wdt = torch.float32 if w.fuse_grad_accum else bf
-    dWg = torch.zeros(I, H, dtype=wdt, device=dev)
-    dWu = torch.zeros(I, H, dtype=wdt, device=dev) if w.gated else None
-    dWd = torch.zeros(H, I, dtype=wdt, device=dev)
-    if w.fuse_grad_accum:
-        dWg.copy_(t["dWg_prev"])
-        dWd.copy_(t["dWd_prev"])
-        if dWu is not None:
-            dWu.copy_(t["dWu_prev"])
-    saved = not w.recompute
-    G = torch.empty(M, I, dtype=bf, device=dev) if saved else None
-    U = torch.empty(M, I, dtype=bf, device=dev) if (saved and w.gated) else None
-    ws_f = m.alloc_workspace(prob, m.MODE_FWD, dev)
-    ws_b = m.alloc_workspace(prob, m.MODE_BWD_RECOMPUTE if w.recompute else m.MODE_BWD, dev)
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def fwd():
-        m.mlp_fwd(prob, g["x"], g["Wg"], g["Wu"], g["Wd"], out, G, U, ws=ws_f)
-
-    def bwd():
-        if saved:
-            m.mlp_bwd(prob, g["dout"], g["x"], g["Wg"], g["Wu"], g["Wd"], G, U, dx, dWg, dWu, dWd,
-                      fuse_grad_accum=w.fuse_grad_accum, ws=ws_b)
-        else:
-            m.mlp_bwd_recompute(prob, g["dout"], g["x"], g["Wg"], g["Wu"], g["Wd"], dx, dWg, dWu,
-                                dWd, fuse_grad_accum=w.fuse_grad_accum, ws=ws_b)
-
-    for _ in range(args.warmup):
-        fwd()
-        bwd()
+    m, dev = st.m, st.dev
+    for _ in range(warmup):
+        st.fwd()
+        st.bwd()
     torch.cuda.synchronize(dev)
-    if m.mlp_device_status(ws_b) != 0 or m.mlp_device_status(ws_f) != 0:
+    if m.mlp_device_status(st.ws_b) != 0 or m.mlp_device_status(st.ws_f) != 0:
         raise RuntimeError("device status error during warm-up")
-    if world > 1:
-        dist.barrier()
-
-    K = args.steps
+    stream = torch.cuda.current_stream(dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    trace = not args.no_trace
-    cvd = [c for c in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if c.strip()]
-    sampler = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else local_rank)
-    torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
+    torch.cuda.synchronize(dev)
+    ctx = on_region if on_region is not None else _Null()
     wall0 = time.perf_counter()
-    with sampler:
+    with ctx:
         for i in range(K):
             flush.zero_()
             ev[i][0].record(stream)
-            fwd()
+            st.fwd()
             ev[i][1].record(stream)
-            bwd()
+            st.bwd()
             ev[i][2].record(stream)
         torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
-    status = m.mlp_device_status(ws_b)
+    status = m.mlp_device_status(st.ws_b)
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    return fwd_ms, bwd_ms, wall, status
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def trace_kernels(st, steps, flush, peaks):
+    """Per-kernel device times from a separate traced pass of L2-flushed
+    steps (tracing brackets every launch with events and runs the kernels
+    one after another), with each kernel's TFLOP/s and algorithmic GB/s.
+    Returns (kernels dict, launches per step)."""
+    import torch
+    m, w = st.m, st.w
+    m.mlp_trace_read()
+    m.mlp_trace_enable(True)
+    try:
+        for _ in range(steps):
+            flush.zero_()
+            st.fwd()
+            st.bwd()
+        torch.cuda.synchronize(st.dev)
+    finally:
+        m.mlp_trace_enable(False)
+    recs = m.mlp_trace_read(capacity=64 * (steps + 1))
+    per = {}
+    for name, ms in recs:
+        per.setdefault(name, []).append(ms)
+    kf, kb = kernel_flops(w), kernel_bytes(w)
+    hbm = float(peaks["hbm_gbs"])
+    kernels = {}
+    for name, v in per.items():
+        avg = sum(v) / len(v)
+        fl = kf.get(name)
+        tot, epi = kb.get(name, (None, None))
+        kernels[name] = {
+            "launches": len(v), "avg_ms": avg, "total_ms": sum(v),
+            "tflops": (fl / (avg * 1e-3) / 1e12) if fl else None,
+            "algorithmic_bytes": tot, "gbs": (tot / (avg * 1e-3) / 1e9) if tot else None,
+            "hbm_frac": (tot / (avg * 1e-3) / 1e9 / hbm) if tot else None,
+            "epilogue_bytes": epi, "epilogue_gbs": (epi / (avg * 1e-3) / 1e9) if epi else None}
+    return kernels, len(recs) // max(1, steps)
+
+
+def roofline_of(kernels, w, peaks, peaks_src, exact_workload):
+    """The dominant kernel's tensor roofline (its flops per launch over its
+    average traced duration, against the measured bf16 burst peak), with
+    ncu's DRAM bytes per launch when a capture of the current device code
+    exists; and the epilogue-heavy kernel's HBM figures (the derivative GEMM
+    whose epilogue reads the preacts and writes their gradients)."""
+    if not kernels:
+        return None
+    dom = max(kernels, key=lambda k: kernels[k]["total_ms"])
+    d = kernels[dom]
+    peak = float(peaks["bf16_tflops"])
+    sus = float(peaks.get("bf16_tflops_sustained", 0.0)) or None
+    ach = d["tflops"]
+    traffic = load_traffic(dom, w.name) if exact_workload else None
+    src = "MEASURED_PEAKS.json" if peaks_src == "measured" else "recipe fallback"
+    roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+            "frac": (ach / peak) if ach else None, "traffic": traffic,
+            "peak_sustained": sus, "frac_of_sustained": (ach / sus) if (ach and sus) else None,
+            "peak_source": f"{peaks_src} bf16 burst ({src})"}
+    epi_k = "dact_recompute" if "dact_recompute" in kernels else "dgated"
+    if epi_k in kernels:
+        e = kernels[epi_k]
+        hbm = float(peaks["hbm_gbs"])
+        tr = load_traffic(epi_k, w.name) if exact_workload else None
+        roof["epilogue"] = {
+            "kernel": epi_k, "epilogue_bytes": e["epilogue_bytes"],
+            "achieved_gbs": e["epilogue_gbs"], "peak_gbs": hbm,
+            "frac": e["epilogue_gbs"] / hbm if e["epilogue_gbs"] else None,
+            "kernel_bytes": e["algorithmic_bytes"], "kernel_gbs": e["gbs"],
+            "kernel_frac": e["hbm_frac"], "traffic": tr,
+            "traffic_gbs": (tr / (e["avg_ms"] * 1e-3) / 1e9) if tr else None,
+            "tflops": e["tflops"], "tensor_frac": e["tflops"] / peak if e["tflops"] else None,
+            "peak_source": f"{peaks_src} HBM copy ({src})"}
+    return roof
+
+
+def measure_workload(m, w, dev, flush, steps, warmup, peaks, peaks_src):
+    """A shorter measurement of another workload for the breakdown: its
+    fwd + bwd step timed as the headline is, its per-kernel trace and its
+    roofline."""
+    import torch
+    st = StepBuffers(m, w, dev)
+    fwd_ms, bwd_ms, _, status = time_steps(st, steps, warmup, flush)
+    kernels, per_step = trace_kernels(st, min(steps, 10), flush, peaks)
+    f_fwd, f_bwd = flops_of(w, "fwd"), flops_of(w, mode_of(w))
+    ms = (sum(fwd_ms) + sum(bwd_ms)) / steps
+    peak = float(peaks["bf16_tflops"])
+    res = {"M": w.M, "H": w.H, "I": w.I, "act": w.act, "gate_mult": w.gate_mult,
+           "down_mult": w.down_mult,
+           "backward": "recompute (save only x)" if w.recompute else "saved G/U",
+           "fuse_grad_accum": w.fuse_grad_accum, "steps": steps, "warmup": warmup,
+           "ms_per_step": ms, "tflops": (f_fwd + f_bwd) / (ms * 1e-3) / 1e12,
+           "pct_of_peak": 100.0 * (f_fwd + f_bwd) / (ms * 1e-3) / 1e12 / peak,
+           "model_tflops": (flops_of(w, "fwd") + flops_of(w, "bwd")) / (ms * 1e-3) / 1e12,
+           "fwd_ms": sum(fwd_ms) / steps, "bwd_ms": sum(bwd_ms) / steps,
+           "fwd_tflops": f_fwd / (sum(fwd_ms) / steps * 1e-3) / 1e12,
+           "bwd_tflops": f_bwd / (sum(bwd_ms) / steps * 1e-3) / 1e12,
+           "kernels": kernels, "launches_per_step": per_step, "device_status": status,
+           "roofline": roofline_of(kernels, w, peaks, peaks_src, True)}
+    del st
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import activated_mlp_gemms_gb300 as m
+    from activated_mlp_gemms_gb300.workloads import WORKLOADS, workload_inputs
+
+    w = WORKLOADS[args.workload]
+    exact = True
+    if args.tokens > 0:
+        import dataclasses
+        w = dataclasses.replace(w, M=args.tokens)
+        exact = False
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    from activated_mlp_gemms_gb300 import _build
+    _build.build()
+
+    st = StepBuffers(m, w, dev)
+    g, t = st.g, st.host
+    bf = torch.bfloat16
+    M, H, I = w.M, w.H, w.I
+    prob = st.prob
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    K = args.steps
+    cvd = [c for c in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if c.strip()]
+    sampler = ClockSampler(cvd[local_rank] if local_rank < len(cvd) else local_rank)
+    fwd_ms, bwd_ms, wall, status = time_steps(st, K, args.warmup, flush, world, sampler)
+    peaks, peaks_src = load_peaks()
     # Per-kernel durations from a separate traced pass over the same steps:
     # tracing brackets every launch with events and runs the kernels one after
     # another, so it is kept out of the timed region above.
-    recs = []
     k_tr = min(K, 50)
-    if trace:
-        m.mlp_trace_read()
-        m.mlp_trace_enable(True)
-        for i in range(k_tr):
-            flush.zero_()
-            fwd()
-            bwd()
-        torch.cuda.synchronize(dev)
-        m.mlp_trace_enable(False)
-        recs = m.mlp_trace_read(capacity=64 * (k_tr + 1))
-    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    kernels, per_step = trace_kernels(st, k_tr, flush, peaks) if not args.no_trace else ({}, 0)
     step_ms = [a + b for a, b in zip(fwd_ms, bwd_ms)]
     tot_ms = sum(step_ms)
     if world > 1:
+        import torch.distributed as dist
         tt = torch.tensor([tot_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         tot_ms = float(tt.item())
@@ -358,33 +528,9 @@ def run_ours(args, rank, world, local_rank):
     f_bwd = flops_of(w, mode_of(w))
     f_step = f_fwd + f_bwd
     value = world * f_step / (ms_per_step * 1e-3) / 1e12
-
-    # per-kernel device times from the launch trace of the timed region
-    per = {}
-    for name, ms in recs:
-        per.setdefault(name, []).append(ms)
-    peaks, peaks_src = load_peaks()
-    kf = kernel_flops(w)
-    kernels = {}
-    for name, v in per.items():
-        fl = kf.get(name)
-        # the recompute backward runs the gate/up kernel twice per step
-        kernels[name] = {"launches": len(v), "avg_ms": sum(v) / len(v), "total_ms": sum(v),
-                         "tflops": (fl / (sum(v) / len(v) * 1e-3) / 1e12) if fl else None}
-    roof = None
-    if kernels:
-        dom = max(kernels, key=lambda k: kernels[k]["total_ms"])
-        d = kernels[dom]
-        peak = float(peaks["bf16_tflops"])
-        ach = d["tflops"]
-        traffic = load_traffic(dom, w.name) if w == WORKLOADS[w.name] else None
-        # the burst peak; the sustained one (the power-capped GEMM loop) beside it
-        sus = float(peaks.get("bf16_tflops_sustained", 0.0)) or None
-        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "frac": (ach / peak) if ach else None, "traffic": traffic,
-                "peak_sustained": sus, "frac_of_sustained": (ach / sus) if (ach and sus) else None,
-                "peak_source": f"{peaks_src} bf16 burst ({'MEASURED_PEAKS.json' if peaks_src == 'measured' else 'recipe fallback'})"}
+    roof = roofline_of(kernels, w, peaks, peaks_src, exact)
     clocks = sampler.summary()
+    out, dx = st.out, st.dx
 
     # End to end through the C ABI with host buffers.  Every step copies its
     # inputs x and dout from pinned host memory to the device and reads its
@@ -408,17 +554,6 @@ def run_ours(args, rank, world, local_rank):
         ob = [out, torch.empty_like(out)]
         dxb = [dx, torch.empty_like(dx)]
 
-        def fwd_b(b):
-            m.mlp_fwd(prob, xb[b], g["Wg"], g["Wu"], g["Wd"], ob[b], G, U, ws=ws_f)
-
-        def bwd_b(b):
-            if saved:
-                m.mlp_bwd(prob, db[b], xb[b], g["Wg"], g["Wu"], g["Wd"], G, U, dxb[b], dWg, dWu,
-                          dWd, fuse_grad_accum=w.fuse_grad_accum, ws=ws_b)
-            else:
-                m.mlp_bwd_recompute(prob, db[b], xb[b], g["Wg"], g["Wu"], g["Wd"], dxb[b], dWg,
-                                    dWu, dWd, fuse_grad_accum=w.fuse_grad_accum, ws=ws_b)
-
         def pipelined(nsteps):
             ev_in = [torch.cuda.Event(), torch.cuda.Event()]
             ev_fwd = [torch.cuda.Event(), torch.cuda.Event()]
@@ -438,9 +573,9 @@ def run_ours(args, rank, world, local_rank):
                 stream.wait_event(ev_in[b])
                 if i >= 2:
                     stream.wait_event(ev_out[b])  # step i-2's read-backs of these buffers
-                fwd_b(b)
+                st.fwd(x=xb[b], out=ob[b])
                 ev_fwd[b].record(stream)
-                bwd_b(b)
+                st.bwd(x=xb[b], dout=db[b], dx=dxb[b])
                 ev_bwd[b].record(stream)
                 with torch.cuda.stream(cs):
                     if i + 1 < nsteps:
@@ -477,14 +612,14 @@ def run_ours(args, rank, world, local_rank):
             with torch.cuda.stream(cs):
                 g["dout"].copy_(hd, non_blocking=True)
                 ev_dout.record(cs)
-            fwd()
+            st.fwd()
             ev_fwd.record(stream)
             with torch.cuda.stream(cs):
                 cs.wait_event(ev_fwd)
                 ho.copy_(out, non_blocking=True)
                 ev_out.record(cs)
             stream.wait_event(ev_dout)
-            bwd()
+            st.bwd()
             hdx.copy_(dx, non_blocking=True)
             stream.wait_event(ev_out)
             e1.record(stream)
@@ -493,6 +628,7 @@ def run_ours(args, rank, world, local_rank):
                 tser += e0.elapsed_time(e1)
         tser /= ke
         if world > 1:
+            import torch.distributed as dist
             tt = torch.tensor([tms, tser], device=dev, dtype=torch.float64)
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
             tms, tser = float(tt[0].item()), float(tt[1].item())
@@ -522,11 +658,34 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize(dev)
             ims.append(ei0.elapsed_time(ei1))
         im = sum(ims) / len(ims)
-        infer = {"ms": im, "tflops": flops_of(w, "infer") / (im * 1e-3) / 1e12}
+        infer = {"ms": im, "tflops": flops_of(w, "infer") / (im * 1e-3) / 1e12,
+                 "pct_of_peak": 100.0 * flops_of(w, "infer") / (im * 1e-3) / 1e12
+                 / float(peaks["bf16_tflops"])}
 
     sweep = infer_m_sweep(m, w, g, dev, flush, peaks) if args.sweep_m else None
     block = block_step(m, w, g, dev, flush, K) if args.block else None
     fp8 = fp8_forward(m, w, g, dev, flush, K, peaks) if (args.fp8 and w.act == "relu_sq") else None
+    launches = per_step * K if kernels else None
+    del st, g, out, dx
+    torch.cuda.empty_cache()
+
+    # the other workloads, a few steps each (rank 0 of a single-GPU run only)
+    workloads = None
+    if world == 1 and not args.headline_only:
+        workloads = {}
+        ksub = max(3, min(K, 10))
+        for name, ow in WORKLOADS.items():
+            if name == w.name:
+                continue
+            r = measure_workload(m, ow, dev, flush, ksub, 3, peaks, peaks_src)
+            if ow.act == "relu_sq":
+                og = {k: (v.to(dev) if v is not None else None)
+                      for k, v in workload_inputs(ow).items()}
+                r["fp8"] = fp8_forward(m, ow, og, dev, flush, ksub, peaks)
+                r["block"] = block_step(m, ow, og, dev, flush, ksub)
+                del og
+                torch.cuda.empty_cache()
+            workloads[name] = r
 
     peak = float(peaks["bf16_tflops"])
     res = {
@@ -546,13 +705,17 @@ def run_ours(args, rank, world, local_rank):
                       "fwd_tflops": f_fwd / (sum(fwd_ms) / K * 1e-3) / 1e12,
                       "bwd_tflops": f_bwd / (sum(bwd_ms) / K * 1e-3) / 1e12,
                       "model_flops_per_step": flops_of(w, "fwd") + flops_of(w, "bwd"),
-                      "executed_flops_per_step": f_step, "kernels": kernels,
+                      "executed_flops_per_step": f_step,
+                      "model_tflops": world * (flops_of(w, "fwd") + flops_of(w, "bwd"))
+                      / (ms_per_step * 1e-3) / 1e12,
+                      "kernels": kernels,
                       "kernels_timing": f"separate traced pass of {k_tr} L2-flushed steps, "
                                         "kernels serialised (no side stream, no PDL overlap)",
-                      "infer": infer, "infer_m_sweep": sweep, "block": block, "fp8_forward": fp8},
+                      "infer": infer, "infer_m_sweep": sweep, "block": block, "fp8_forward": fp8,
+                      "workloads": workloads},
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": (len(recs) // k_tr) * K if trace else None,
+        "gpu_launches": launches,
         "clocks": clocks,
         "device_status": status,
         "wall_s_timed_region": wall,
@@ -701,6 +864,7 @@ def block_step(m, w, g, dev, flush, K):
         res[name] = sorted(ts)[len(ts) // 2]
     f = flops_of(w, "fwd") + flops_of(w, "bwd")
     res["block_tflops"] = f / (res["block_ms"] * 1e-3) / 1e12
+    res["plain_tflops"] = f / (res["plain_ms"] * 1e-3) / 1e12
     res["overhead"] = res["block_ms"] / res["plain_ms"] - 1.0
     res["lambdas"] = {"resid_lambda": 1.1 ** 0.5, "post_lambda": 0.8, "eps": 2.0 ** -7}
     return res
