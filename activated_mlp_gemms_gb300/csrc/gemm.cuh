@@ -103,7 +103,7 @@ struct EpiTraits {
   // preact's chunk box; small enough for a sixth pipeline stage), the e5m2
   // derivative's 32 x 128-byte tile box
   static constexpr int STG_WARP = EPI == EPI_ACT_FWD_F8  ? 2048 + 2048
-                                  : EPI == EPI_DGRAD_F8 ? 4096
+                                  : (EPI == EPI_DGRAD_F8 || EPI == EPI_DGRAD_F8_RECOMP) ? 4096
                                                         : STG_BUFS * OUT_BYTES;
 };
 
@@ -165,6 +165,7 @@ struct EpiUnit {
   const float* rstd;          // per-row scale (nullptr: none)
   float alpha;                // residual scale
   float deq;                  // 8-bit epilogues: *sa * *sb (the operands' dequant scales)
+  float deq0;                 // ... EPI_DGRAD_F8_RECOMP: *sp0 * *sp1 (the recomputed preact's)
   float mult;                 // ... the problem's multiplier
   float inv;                  // ... fp32(1 / *sq), the 8-bit output's quantisation factor
   float* amax;                // running max of the 8-bit epilogue's output
@@ -172,7 +173,8 @@ struct EpiUnit {
 
 // deq, inv: the 8-bit epilogues' factors of this problem (read once per kernel)
 template <int EPI>
-__device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P, float deq, float inv) {
+__device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P, float deq, float inv,
+                                            float deq0 = 1.f) {
   EpiUnit U;
 #pragma unroll
   for (int o = 0; o < 3; ++o) U.out[o] = P.mapO[o] >= 0 ? &p.maps[P.mapO[o]] : nullptr;
@@ -187,8 +189,10 @@ __device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P, floa
   U.mult = 1.f;
   U.inv = 1.f;
   U.amax = nullptr;
+  U.deq0 = 1.f;
   if constexpr (is_f8(EPI)) {
     U.deq = deq;
+    U.deq0 = deq0;
     U.mult = P.mult;
     U.inv = inv;
     U.amax = P.amax;
@@ -622,6 +626,73 @@ __device__ __forceinline__ void epi_dgrad_f8(const Params& p, const EpiUnit& P, 
   }
 }
 
+// EPI_DGRAD_F8_RECOMP, phase 1 on accumulator 0 (x8 W1_8^T): this thread's
+// 128 values of dd = 2 relu(deq0 * acc) as packed bf16 pairs (the saved-
+// preact path's 2 relu(bf16(pre)): doubling and relu commute with the
+// rounding), after which the accumulator goes back to the MMAs.
+__device__ __forceinline__ void epi_recomp_f8_p(const EpiUnit& P, uint32_t tb, int col0, int cb,
+                                                uint32_t (&dd)[64]) {
+  const float deq0 = P.deq0;
+#pragma unroll
+  for (int ci = 0; ci < 4; ++ci) {
+    const int c = cb + 32 * ci;
+    if (col0 + c >= P.N) break;  // warp-uniform
+    uint32_t z[32];
+    __syncwarp();
+    tmem_ld32(tb + c, z);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float r0 = fmaxf(deq0 * __uint_as_float(z[2 * j]), 0.f);
+      const float r1 = fmaxf(deq0 * __uint_as_float(z[2 * j + 1]), 0.f);
+      dd[16 * ci + j] = pack_bf16x2(2.f * r0, 2.f * r1);
+    }
+  }
+}
+
+// Phase 2 on accumulator 1 (dout8 W2_8): dpre = mult * deq * acc * dd ->
+// e5m2(dpre * fp32(1 / *sq)) staged per tile as in epi_dgrad_f8; the largest
+// |dpre| of the warp's rows goes to *amax.
+__device__ __forceinline__ void epi_recomp_f8_dh(const EpiUnit& P, const EpiWarp& e, uint32_t tb,
+                                                 int col0, int cb, const uint32_t (&dd)[64]) {
+  const float dq = P.mult * P.deq;
+  const float inv = P.inv;
+  float mx = 0.f;
+#pragma unroll
+  for (int ci = 0; ci < 4; ++ci) {
+    const int col = col0 + cb + 32 * ci;
+    if (col >= P.N) break;
+    uint32_t z[32];
+    __syncwarp();
+    tmem_ld32(tb + cb + 32 * ci, z);
+    tmem_wait_ld();
+    uint32_t q[8];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      q[2 * v] = 0;
+      q[2 * v + 1] = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 g = unpack_bf16x2(dd[16 * ci + 4 * v + j]);
+        const float d0 = dq * __uint_as_float(z[8 * v + 2 * j]) * g.x;
+        const float d1 = dq * __uint_as_float(z[8 * v + 2 * j + 1]) * g.y;
+        mx = fmaxf(mx, fmaxf(fabsf(d0), fabsf(d1)));
+        q[2 * v + (j >> 1)] |= static_cast<uint32_t>(pack_e5m2x2(d0 * inv, d1 * inv))
+                               << (16 * (j & 1));
+      }
+    }
+    if (ci == 0) staging_acquire(e);  // the previous tile's box has been read
+    stage_f8_chunk(e.stg, e.lane, ci, q);
+  }
+  if (col0 + cb < P.N) store_f8_tile(P, e, 0, e.stg, col0 + cb);
+  if (P.amax) {
+    if (e.row0 + e.lane >= P.M) mx = 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (e.lane == 0 && mx > 0.f) atomicMax(reinterpret_cast<int*>(P.amax), __float_as_int(mx));
+  }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epi_plain(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                           uint32_t tb, int col0, int cb, int ce) {
@@ -784,7 +855,8 @@ __device__ __forceinline__ UnitLoads unit_loads(const Params& p, const Prob& P, 
 //   B K-major: one box {64, 256 / CG};      B MN-major: 4 / CG boxes {64 n, 64 k}.
 //   8-bit operands: K-major boxes as above ({128 k, rows}); A MN-major one box
 //   {128 m, 128 k}; B MN-major 2 / CG boxes {128 n, 128 k}.
-//   EPI_DACT_RECOMP: segment 0 B K-major (W1), segment 1 B MN-major (Wd).
+//   EPI_DACT_RECOMP, EPI_DGRAD_F8_RECOMP: segment 0 B K-major (W1), segment 1
+//   B MN-major (Wd, W2_8).
 template <int EPI, bool A_MN, bool B_MN, int CG>
 __device__ __forceinline__ void load_stage(const UnitLoads& L, int seg, int kc, uint32_t sA,
                                            uint32_t sB, uint32_t full, uint64_t pol) {
@@ -806,8 +878,8 @@ __device__ __forceinline__ void load_stage(const UnitLoads& L, int seg, int kc, 
     if constexpr (CG == 1) ld(sB + 16384, L.b1, kc, L.n0);
   } else {
     const CUtensorMap* mB = seg == 0 ? L.b0 : L.b1;
-    // the fused recompute reads W1 (K-major) in segment 0, Wd (MN-major) in 1
-    const bool b_mn = EPI == EPI_DACT_RECOMP ? seg == 1 : B_MN;
+    // the fused recomputes read W1 (K-major) in segment 0, Wd (MN-major) in 1
+    const bool b_mn = is_recomp(EPI) ? seg == 1 : B_MN;
     if (!b_mn) {
       ld(sB, mB, kc, L.n0);
     } else if constexpr (is_f8(EPI)) {
@@ -1053,9 +1125,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
       // 8-bit operands: their formats come with the launch
+      // (the 8-bit fused recompute: segment 0's formats and K-major B, then
+      // segment 1's with B MN-major)
       const uint32_t idesc_8 = idesc_f8(C::TILE_M, MMA_N, p.f8_formats & 7, (p.f8_formats >> 3) & 7,
-                                        A_MN, B_MN);
+                                        A_MN, B_MN || is_recomp(EPI));
+      const uint32_t idesc_8s0 = idesc_f8(C::TILE_M, MMA_N, p.f8_formats0 & 7,
+                                          (p.f8_formats0 >> 3) & 7, A_MN, false);
       (void)idesc_8;
+      (void)idesc_8s0;
       int stage = 0;
       uint32_t phase = 0;
       int slot = 0;
@@ -1072,14 +1149,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
         if (unit < 0) break;
         const Work w = decode_unit(p, unit);
         // the fused recompute's second K segment goes to the other accumulator
-        const int kswitch = EPI == EPI_DACT_RECOMP ? p.prob[w.prob].kb0 : -1;
+        const int kswitch = is_recomp(EPI) ? p.prob[w.prob].kb0 : -1;
         if (!mbar_wait<PAIR>(bar_s(TEMPTY + acc), aphase ^ 1u, lim, abort_flag)) { ok = false; break; }
         tc_fence_after();
         uint32_t d = tmem + acc * MMA_N;
         int kfirst = w.kb_begin;
         bool seg1 = false;
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
-          if (EPI == EPI_DACT_RECOMP && kb == kswitch) {
+          if (is_recomp(EPI) && kb == kswitch) {
             if constexpr (PAIR) tc_commit_pair(bar_s(TFULL + acc), 3);
             else tc_commit(bar_s(TFULL + acc));
             acc ^= 1;
@@ -1106,7 +1183,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
                                      : sdesc_sw128(sA + k * 32, 16, 1024);
             const uint64_t bd = b_mn ? sdesc_sw128(sB + k * MN_STEP, MN_LBO, 1024)
                                      : sdesc_sw128(sB + k * 32, 16, 1024);
-            const uint32_t idesc = F8 ? idesc_8 : b_mn ? IDESC_BMN : IDESC;
+            const uint32_t idesc =
+                F8 ? ((is_recomp(EPI) && !seg1) ? idesc_8s0 : idesc_8) : b_mn ? IDESC_BMN : IDESC;
             const uint32_t accum = (kb > kfirst || k > 0) ? 1u : 0u;
             if constexpr (F8) {
               if constexpr (PAIR) tc_mma_f8_pair(d, ad, bd, idesc, accum);
@@ -1152,6 +1230,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
     // 8-bit epilogues: each problem's dequant factor *sa * *sb and output
     // quantisation factor 1 / *sq (device scalars), read once
     float f8_deq[MAX_PROBS], f8_inv[MAX_PROBS];
+    float f8_deq0 = 1.f;  // EPI_DGRAD_F8_RECOMP (one problem): the recomputed preact's
 #pragma unroll
     for (int i = 0; i < MAX_PROBS; ++i) {
       f8_deq[i] = 1.f;
@@ -1163,6 +1242,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
         }
       }
     }
+    if constexpr (EPI == EPI_DGRAD_F8_RECOMP) f8_deq0 = *p.prob[0].sp0 * *p.prob[0].sp1;
     while (true) {
       if (!mbar_wait<PAIR>(bar_s(SFULL + slot), sphase, lim, abort_flag)) {
         record_timeout(p, abort_flag);
@@ -1180,7 +1260,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       const int pi = w.prob;
       const EpiUnit P = epi_unit<EPI>(p, p.prob[pi],
                                       pi == 0 ? f8_deq[0] : pi == 1 ? f8_deq[1] : f8_deq[2],
-                                      pi == 0 ? f8_inv[0] : pi == 1 ? f8_inv[1] : f8_inv[2]);
+                                      pi == 0 ? f8_inv[0] : pi == 1 ? f8_inv[1] : f8_inv[2],
+                                      f8_deq0);
       e.row0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + q * 32;
       e.rows_ok = e.row0 < P.M;
       e.rs = (P.rstd && e.row0 + lane < P.M) ? P.rstd[e.row0 + lane] : 1.f;
@@ -1188,18 +1269,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       const int cb = half * (tile_n / 2), ce = cb + tile_n / 2;
       const int col0 = w.tn * tile_n;
       uint4 pg[4], pu[4];
-      uint32_t dd[EPI == EPI_DACT_RECOMP ? 64 : 1];  // s*act'(p) between the two phases
+      // s*act'(p) (bf16: dd = 2 relu(pre)) between the two phases
+      uint32_t dd[is_recomp(EPI) ? 64 : 1];
       (void)dd;
-      if constexpr (EPI == EPI_DACT_RECOMP) {
+      if constexpr (is_recomp(EPI)) {
         // phase 1 on the recomputed preact, then its accumulator goes back to the MMAs
         if (!mbar_wait<PAIR>(bar_s(TFULL + acc), aphase, lim, abort_flag)) {
           record_timeout(p, abort_flag);
           break;
         }
         tc_fence_after();
-        if (e.rows_ok)
-          epi_recomp_p<ACT>(p, P, e, tmem + acc * MMA_N + (static_cast<uint32_t>(q * 32) << 16),
-                            col0, cb, dd);
+        if (e.rows_ok) {
+          const uint32_t t0 = tmem + acc * MMA_N + (static_cast<uint32_t>(q * 32) << 16);
+          if constexpr (EPI == EPI_DACT_RECOMP) epi_recomp_p<ACT>(p, P, e, t0, col0, cb, dd);
+          else epi_recomp_f8_p(P, t0, col0, cb, dd);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -1237,6 +1321,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
           epi_act_f8<ACT>(p, P, e, tb, col0, cb, ce);
         } else if constexpr (EPI == EPI_DGRAD_F8) {
           epi_dgrad_f8(p, P, e, tb, col0, cb, ce, pg);
+        } else if constexpr (EPI == EPI_DGRAD_F8_RECOMP) {
+          epi_recomp_f8_dh(P, e, tb, col0, cb, dd);
         } else {
           epi_plain<EPI>(p, P, e, tb, col0, cb, ce);
         }

@@ -43,11 +43,26 @@ enum Epi : int {
   // EPI_STORE_BF16 epilogue, reading problem 0's postact.  A down unit of a
   // 256-row block starts once every gate/up tile of that block is stored
   // (Params::dep), so the down tiles fill the SMs the gate/up tail leaves idle.
-  EPI_FWD_FUSED = 10
+  EPI_FWD_FUSED = 10,
+  // The 8-bit derivative with the preact recomputed in the same tile
+  // (nothing saved by the forward): segment 0 acc = x8 W1_8^T (accumulator
+  // 0, both e4m3, B K-major), segment 1 acc = dout8 W2_8 (accumulator 1,
+  // e5m2 x e4m3, B MN-major).  dd = bf16(2 relu(deq0 * acc0)) is held per
+  // thread between the two, then dpre = mult * deq * acc1 * dd ->
+  // e5m2(dpre / *sq) (map 0), amax|dpre| -> *amax.  dd is the value the
+  // saved-preact path forms from the preact it stores in bf16, so both give
+  // the same codes.
+  EPI_DGRAD_F8_RECOMP = 11
 };
 
 __host__ __device__ constexpr bool is_f8(int epi) {
-  return epi == EPI_ACT_FWD_F8 || epi == EPI_STORE_BF16_F8 || epi == EPI_DGRAD_F8;
+  return epi == EPI_ACT_FWD_F8 || epi == EPI_STORE_BF16_F8 || epi == EPI_DGRAD_F8 ||
+         epi == EPI_DGRAD_F8_RECOMP;
+}
+// Epilogues whose tiles accumulate two K segments into the two accumulators
+// (segment 0's B K-major, segment 1's B MN-major).
+__host__ __device__ constexpr bool is_recomp(int epi) {
+  return epi == EPI_DACT_RECOMP || epi == EPI_DGRAD_F8_RECOMP;
 }
 // 8-bit operand formats of Params::f8_formats (the kind::f8f6f4 type codes)
 constexpr int F8_E4M3 = 0, F8_E5M2 = 1;
@@ -85,6 +100,9 @@ struct Prob {
   const float* sq;
   float mult;
   float* amax;            // running max of |the quantised output| (atomic; may be null)
+  // EPI_DGRAD_F8_RECOMP: the recomputed preact's dequant scales (sx, s1)
+  const float* sp0;
+  const float* sp1;
 };
 
 struct Params {  // 64-byte aligned through CUtensorMap
@@ -96,6 +114,7 @@ struct Params {  // 64-byte aligned through CUtensorMap
   int group_m;            // L2 raster: tiles are visited in groups of group_m tile rows
   float scale;            // gate_mult * down_mult (activation epilogues)
   int f8_formats;         // 8-bit MMAs: A's format (bits 0-2) and B's (bits 3-5), F8_*
+  int f8_formats0;        // EPI_DGRAD_F8_RECOMP: the formats of K segment 0 (f8_formats: segment 1)
   int debug_flags;        // MLP_DEBUG_* (testing only; 0 in normal use)
   int a_tx_bytes;         // bytes one CTA's A boxes bring per k-block (K-major A: rows x 128 B)
   int nmaps;              // tensor maps in use

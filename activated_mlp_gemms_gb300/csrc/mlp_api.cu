@@ -1074,7 +1074,11 @@ int mlp_fp8_bwd(const mlp_problem_t* p, const void* dout, const void* x8, const 
   const bool need_dpre = dx || dW1;
   if (need_dpre) {
     MLP_TRY(need(W2_8));
-    MLP_TRY(need(pre));
+    MLP_TRY(opt(pre));
+    if (!pre) {  // the derivative GEMM recomputes the preact from the forward's operands
+      MLP_TRY(need(x8));
+      MLP_TRY(need(W1_8));
+    }
   }
   if (dx) MLP_TRY(need(W1_8));
   if (dW1) MLP_TRY(need(x8));
@@ -1097,7 +1101,34 @@ int mlp_fp8_bwd(const mlp_problem_t* p, const void* dout, const void* x8, const 
                              pdl);
     }));
   }
-  if (need_dpre) {
+  if (need_dpre && !pre) {
+    // the same derivative with the preact recomputed in each output tile:
+    // segment 0 accumulates x8 W1_8^T (both e4m3, B K-major), segment 1
+    // dout8 W2_8 (e5m2 x e4m3, B MN-major); dpre = gate_mult * down_mult * sg
+    // * s2 * acc1 * 2 relu(sx * s1 * acc0), to e5m2 with s_dpre
+    Gemm g(*p, c.counter(), c.status, pick_cg(M));
+    g.p.f8_formats = fmts;
+    g.p.f8_formats0 = F8_E4M3 | (F8_E4M3 << 3);
+    const int mA0 = g.kmajor_a_u8(x8, M, H);
+    const int mB0 = g.kmajor_u8(W1_8, I, H, g.b_rows());
+    const int mA1 = g.kmajor_a_u8(dout8, M, H);
+    const int mB1 = g.mnmajor_u8(W2_8, H, I);
+    const int oP = g.output_u8(dP8, M, I);
+    Prob& P = g.add(M, I, H, H, MMA_N, 1, 2 * BK);
+    P.mapA0 = mA0;
+    P.mapB0 = mB0;
+    P.mapA1 = mA1;
+    P.mapB1 = mB1;
+    P.mapO[0] = oP;
+    P.sa = scales + 4;   // sg
+    P.sb = scales + 2;   // s2
+    P.sq = scales + 5;   // s_dpre
+    P.sp0 = scales + 0;  // sx
+    P.sp1 = scales + 1;  // s1
+    P.mult = p->gate_mult * p->down_mult;
+    P.amax = amax_dpre;
+    MLP_TRY((run<EPI_DGRAD_F8_RECOMP, false, false>(g, c, MLP_KERNEL_DGATED)));
+  } else if (need_dpre) {
     // dpre = gate_mult * down_mult * sg * s2 * (dout8 W2_8) * 2 relu(pre), to
     // e5m2 with the delayed scale s_dpre; W2_8 [H,I]: B(n=i, k=h) is N-contiguous
     Gemm g(*p, c.counter(), c.status, pick_cg(M));

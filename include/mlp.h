@@ -282,7 +282,12 @@ int mlp_fp8_fwd(const mlp_problem_t* p, const void* x8, const void* W1_8, const 
  *   dx    = (dP8 W1_8) * s_dpre * s1                          (bf16 [M,H])
  *   dW1   = (dP8^T x8) * s_dpre * sx                          (bf16 [I,H])
  *   dW2   = down_mult * (dout8^T a8) * sg * s_post            (bf16 [H,I])
- *   dout: bf16 [M,H];  pre: the forward's pre_save (bf16 [M,I]);  a8: its e4m3 postact
+ *   dout: bf16 [M,H];  pre: the forward's pre_save (bf16 [M,I]), or NULL: then the
+ *         derivative GEMM recomputes the preact in each output tile from x8 and
+ *         W1_8 (a second accumulator, the forward's own fp32 sums) and forms
+ *         2 relu(pre) from it rounded to bf16 as the saved path does, so the
+ *         codes, dx, dW1 and dW2 are the same as with the forward's pre_save
+ *         (the forward then need not write it);  a8: the forward's e4m3 postact
  *   x8, W1_8, W2_8: the forward's e4m3 codes
  *   scales: device fp32 {sx, s1, s2, s_post, sg, s_dpre}
  *   dx, dW1, dW2: outputs, each NULL when not wanted (then its operands may be NULL)

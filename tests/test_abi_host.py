@@ -169,7 +169,9 @@ def test_fp8_backward_validation_and_workspace(L):
     assert b(W1=None) == -1                       # dx needs W1_8
     assert b(x8=None) == -1                       # dW1 needs x8
     assert b(a8=None) == -1                       # dW2 needs a8
-    assert b(pre=None) == -1                      # the derivative needs the preact
+    # without the saved preact the derivative recomputes it: x8 and W1_8 are then needed
+    assert b(pre=None, x8=None, dW1=None) == -1
+    assert b(pre=None, W1=None, dx=None) == -1
     assert b(W2=None) == -1                       # ... and W2_8
     assert b(ws_bytes=need - 1) == -4
     # nothing requested: returns before any CUDA call; absent operands of

@@ -550,3 +550,45 @@ def test_fp8_training_loop_in_a_graph_needs_no_host_sync():
     for k in ("scales", "amax_a", "amax_d", "out", "pre", "a8", "dx", "dW1", "dW2"):
         assert torch.equal(g[k], e[k]), k
     assert m.mlp_device_status(g["wsb"]) == 0
+
+
+@pytest.mark.parametrize("tile_policy", [1, 2], indirect=True)
+@pytest.mark.parametrize("M,H,I", [(7, 256, 400), (300, 256, 400), (1000, 768, 3072)])
+def test_fp8_backward_recomputing_the_preact_equals_the_saved_path(M, H, I, tile_policy):
+    """mlp_fp8_bwd without a saved preact recomputes it in the derivative
+    GEMM's tile from x8 and W1_8 (the forward's own fp32 sums) and rounds
+    2 relu(pre) to bf16 as the saved path does: the e5m2 derivative codes,
+    their amax, dx, dW1 and dW2 are bitwise those of the saved path."""
+    t = make_inputs(M, H, I, "relu_sq", seed=72)
+    xd, W1d, W2d = to_f64(t["x"]), to_f64(t["Wg"]), to_f64(t["Wd"])
+    f32 = lambda v: float(np.float32(v))  # noqa: E731
+    sx = 2.0 ** -4
+    s1, s2 = f32(np.max(np.abs(W1d)) / E4M3_MAX), f32(np.max(np.abs(W2d)) / E4M3_MAX)
+    x8, W1_8, W2_8 = (_f8_bytes(quantize(v, sc), torch.float8_e4m3fn)
+                      for v, sc in ((xd, sx), (W1d, s1), (W2d, s2)))
+    prob = m.problem(M, H, I, "relu_sq", 1.125, 2.0)
+    bf = torch.bfloat16
+    pre = (xd[:64] @ W1d.T).clip(min=0) ** 2
+    s_post = f32(np.max(pre) * 1.125 * 1.03 / E4M3_MAX)
+    scales = torch.tensor([sx, s1, s2, s_post, 2.0 ** -6, 2.0 ** -10], dtype=torch.float32,
+                          device="cuda")
+    out = torch.empty(M, H, dtype=bf, device="cuda")
+    a8 = torch.empty(M, I, dtype=torch.uint8, device="cuda")
+    pre_s = torch.empty(M, I, dtype=bf, device="cuda")
+    m.mlp_fp8_fwd(prob, x8, W1_8, W2_8, scales, out, a8, pre_save=pre_s)
+    dout = t["dout"].cuda()
+    res = {}
+    for name, p_in in (("saved", pre_s), ("recompute", None)):
+        dx = torch.full((M, H), float("nan"), dtype=bf, device="cuda")
+        dW1 = torch.full((I, H), float("nan"), dtype=bf, device="cuda")
+        dW2 = torch.full((H, I), float("nan"), dtype=bf, device="cuda")
+        amax = torch.zeros(1, dtype=torch.float32, device="cuda")
+        ws = m.mlp_fp8_bwd(prob, dout, x8, W1_8, W2_8, p_in, a8, scales, dx, dW1, dW2, amax)
+        torch.cuda.synchronize()
+        assert m.mlp_device_status(ws) == 0
+        off = 1024 + (M * H + 255) // 256 * 256
+        res[name] = {"dx": dx, "dW1": dW1, "dW2": dW2, "amax": amax,
+                     "dP8": ws[off:off + M * I].clone()}
+    for k in res["saved"]:
+        assert torch.isfinite(res["recompute"][k].float()).all() if k != "dP8" else True
+        assert torch.equal(res["saved"][k], res["recompute"][k]), k
