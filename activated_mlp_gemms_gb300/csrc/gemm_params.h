@@ -168,7 +168,9 @@ cudaError_t launch_hold(int ctas, unsigned long long ns, cudaStream_t stream);
 // CTA stages the M token rows of its K (H, then I) whole in shared memory:
 // M * K * 2 <= DECODE_MAX_TOKEN_BYTES.
 constexpr int DECODE_MAX_M = 4;
-constexpr int DECODE_MAX_TOKEN_BYTES = 100 * 1024;
+// (112 KiB: four token rows of a 14336-wide intermediate; two such CTAs,
+// with the 1 KiB each reserves, fit an SM's 228 KiB of shared memory)
+constexpr int DECODE_MAX_TOKEN_BYTES = 112 * 1024;
 cudaError_t launch_decode_act(const void* x, const void* Wg, const void* Wu, void* a, void* G,
                               void* U, int M, int H, int I, int act, bool gated, float s,
                               cudaStream_t stream, bool pdl);

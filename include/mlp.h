@@ -136,7 +136,7 @@ size_t mlp_workspace_size(const mlp_problem_t* p, int mode);
  *   U_save bf16 [M,I]  out, optional: the up preact x Wu^T (NULL when non-gated)
  * Pass G_save/U_save as NULL for the recompute mode (save only x).  The
  * bf16 values written to `out` are bitwise identical to mlp_fwd_infer's.
- * With one to four tokens (decode; M * max(H, I) * 2 <= 100 KiB), unless a
+ * With one to four tokens (decode; M * max(H, I) * 2 <= 112 KiB), unless a
  * tile policy is set (below), the forward streams the weights on the CUDA
  * cores instead of the tensor cores: each warp reads whole weight rows
  * front to back and accumulates the M dot products in fp32 (two kernels,

@@ -90,13 +90,15 @@ def test_decode_path_is_two_kernels_and_graph_capturable():
         assert torch.equal(out, ref)
 
 
-@pytest.mark.parametrize("M,path", [(3, ["gate_up_act", "down_proj"]), (4, None)])
-def test_decode_token_rows_must_fit_shared_memory(M, path):
-    """With Llama-3-8B's intermediate size (14336) three token rows of the
-    postact fit a CTA's shared memory and take the weight-streaming kernels;
-    four do not and take the tensor cores (a split-K down projection, then
-    its fp32 -> bf16 pass)."""
-    H, I = 4096, 14336
+@pytest.mark.parametrize("M,I,path", [(3, 14336, ["gate_up_act", "down_proj"]),
+                                      (4, 14336, ["gate_up_act", "down_proj"]),
+                                      (4, 16384, None)])
+def test_decode_token_rows_must_fit_shared_memory(M, I, path):
+    """With Llama-3-8B's intermediate size (14336) up to four token rows of
+    the postact (112 KiB) fit a CTA's shared memory and take the
+    weight-streaming kernels; four rows of 16384 do not and take the tensor
+    cores (a split-K down projection, then its fp32 -> bf16 pass)."""
+    H = 4096
     t = make_inputs(M, H, I, "swiglu", seed=34)
     d = dev_tensors(t)
     prob = m.problem(M, H, I)
@@ -117,3 +119,23 @@ def test_decode_token_rows_must_fit_shared_memory(M, path):
     a = {k: to_f64(v) for k, v in t.items() if v is not None}
     ref = mlp_forward(a["x"], a["Wg"], a["Wu"], a["Wd"], "swiglu")["out"]
     assert rel_err(to_f64(out), ref) <= 2e-2
+
+
+def test_decode_four_tokens_of_a_wide_intermediate():
+    """Four tokens with I = 14336 (the Llama-3-8B width): 112 KiB of staged
+    token rows for the down projection, still on the CUDA cores, against the
+    oracle and bitwise against a second call."""
+    M, H, I = 4, 1024, 14336
+    t = make_inputs(M, H, I, "swiglu", seed=33)
+    d = dev_tensors(t)
+    prob = m.problem(M, H, I)
+    assert m.mlp_plan(prob, m.MODE_INFER)["decode"] == 1
+    out = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+    out2 = torch.empty_like(out)
+    m.mlp_fwd_infer(prob, d["x"], d["Wg"], d["Wu"], d["Wd"], out)
+    m.mlp_fwd_infer(prob, d["x"], d["Wg"], d["Wu"], d["Wd"], out2)
+    torch.cuda.synchronize()
+    a = {k: to_f64(v) for k, v in t.items() if v is not None}
+    ref = mlp_forward(a["x"], a["Wg"], a["Wu"], a["Wd"], "swiglu")["out"]
+    assert rel_err(to_f64(out), ref) <= 2e-2
+    assert torch.equal(out, out2)
