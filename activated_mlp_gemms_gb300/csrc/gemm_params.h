@@ -177,6 +177,17 @@ cudaError_t launch_decode_act(const void* x, const void* Wg, const void* Wu, voi
 cudaError_t launch_decode_down(const void* a, const void* Wd, void* out, int M, int H, int I,
                                cudaStream_t stream, bool pdl);
 
+// Decode-sized forward (M <= DECODE_MMA_MAX_M) on the warp-level MMA: the
+// same two passes and epilogues as above, the dot products as mma.sync
+// m16n8k16 (bf16 in, fp32 accumulate) fed straight from 16-byte loads; the
+// token rows are read through the caches, so K is not limited.
+constexpr int DECODE_MMA_MAX_M = 16;
+cudaError_t launch_decode_mma_act(const void* x, const void* Wg, const void* Wu, void* a, void* G,
+                                  void* U, int M, int H, int I, int act, bool gated, float s,
+                                  cudaStream_t stream, bool pdl);
+cudaError_t launch_decode_mma_down(const void* a, const void* Wd, void* out, int M, int H, int I,
+                                   cudaStream_t stream, bool pdl);
+
 // Per-token RMS-norm scale rstd[m] = 1 / sqrt(mean_h x^2 + eps), x bf16 [M, H].
 cudaError_t launch_rstd(const void* x, float* rstd, int M, int H, float eps, cudaStream_t stream,
                         bool pdl);

@@ -173,14 +173,18 @@ int device_act(int act) {
 // forward's two GEMMs as separate launches
 std::atomic<int> g_tile_policy{0};
 
-// The forward of at most DECODE_MAX_M tokens runs on the CUDA cores (a
-// weight stream) unless a tile policy forces the tensor-core path, or its
-// token rows do not fit a CTA's shared memory.
-bool decode_path(const mlp_problem_t* p) {
-  const long long k = p->H > p->I ? p->H : p->I;
+// Which kernels a forward of few tokens streams its weights with (unless a
+// tile policy forces the tensor-core GEMMs): 2, the warp-MMA weight stream,
+// for at most DECODE_MMA_MAX_M tokens; 1, the CUDA-core one, only when
+// MLP_DEBUG_DECODE_FMA asks for it and its token rows fit a CTA's shared
+// memory; 0, the tensor-core GEMMs.
+int decode_kernel(const mlp_problem_t* p) {
   const int pol = g_tile_policy.load();
-  return p->M <= DECODE_MAX_M && (long long)p->M * k * 2 <= DECODE_MAX_TOKEN_BYTES &&
-         (pol == 0 || pol == 3);
+  if ((pol != 0 && pol != 3) || p->M > DECODE_MMA_MAX_M) return 0;
+  const long long k = p->H > p->I ? p->H : p->I;
+  const bool fma_fits = p->M <= DECODE_MAX_M && (long long)p->M * k * 2 <= DECODE_MAX_TOKEN_BYTES;
+  if (fma_fits && (g_debug_flags.load() & MLP_DEBUG_DECODE_FMA)) return 1;
+  return 2;
 }
 
 // CTA-group size for a GEMM whose output has `rows` rows: pairs (256-row
@@ -739,16 +743,22 @@ int forward(const mlp_problem_t* p, const void* x, const void* Wg, const void* W
   Call c;
   MLP_TRY(begin_call(c, ws, stream));
   void* a = static_cast<char*>(ws) + CTRL_BYTES;
-  if (!blk && decode_path(p)) {
-    // a few tokens: two weight-streaming passes on the CUDA cores
+  const int dk = blk ? 0 : decode_kernel(p);
+  if (dk != 0) {
+    // a few tokens: two weight-streaming passes (warp-level MMA, or CUDA cores)
     const bool pdl0 = c.pdl();
     MLP_TRY(traced(MLP_KERNEL_GATE_UP, c.stream, [&] {
-      return launch_decode_act(x, Wg, Wu, a, G_save, U_save, p->M, p->H, p->I, device_act(p->act),
-                               gated(p), p->gate_mult * p->down_mult, c.stream, pdl0);
+      return dk == 2 ? launch_decode_mma_act(x, Wg, Wu, a, G_save, U_save, p->M, p->H, p->I,
+                                             device_act(p->act), gated(p),
+                                             p->gate_mult * p->down_mult, c.stream, pdl0)
+                     : launch_decode_act(x, Wg, Wu, a, G_save, U_save, p->M, p->H, p->I,
+                                         device_act(p->act), gated(p),
+                                         p->gate_mult * p->down_mult, c.stream, pdl0);
     }));
     const bool pdl1 = c.pdl();
     return traced(MLP_KERNEL_DOWN, c.stream, [&] {
-      return launch_decode_down(a, Wd, out, p->M, p->H, p->I, c.stream, pdl1);
+      return dk == 2 ? launch_decode_mma_down(a, Wd, out, p->M, p->H, p->I, c.stream, pdl1)
+                     : launch_decode_down(a, Wd, out, p->M, p->H, p->I, c.stream, pdl1);
     });
   }
   const int split = bf16_split(p->M, p->H, split_k_of(p, mode));
@@ -1248,7 +1258,7 @@ int mlp_plan(const mlp_problem_t* p, int mode, int fuse_grad_accum, mlp_plan_t* 
   std::memset(plan, 0, sizeof(*plan));
   const bool fp8 = mode == MLP_MODE_FP8_FWD || mode == MLP_MODE_FP8_BWD;
   const bool fwd = mode == MLP_MODE_FWD || mode == MLP_MODE_INFER;
-  plan->decode = (fwd && decode_path(p)) ? 1 : 0;
+  plan->decode = fwd ? decode_kernel(p) : 0;
   plan->cta_group = pick_cg(p->M);
   plan->out_split = (fp8 || plan->decode) ? 1 : bf16_split(p->M, p->H, split_k_of(p, mode));
   plan->fused_forward = (fwd && !plan->decode && fused_forward(p, plan->out_split)) ? 1 : 0;
@@ -1305,7 +1315,7 @@ int mlp_set_wait_timeout_ms(unsigned int ms) {
 }
 
 int mlp_debug_set_flags(int flags) {
-  if (flags & ~MLP_DEBUG_NO_WORK) return MLP_ERR_INVALID_ARG;
+  if (flags & ~(MLP_DEBUG_NO_WORK | MLP_DEBUG_DECODE_FMA)) return MLP_ERR_INVALID_ARG;
   g_debug_flags.store(flags);
   return MLP_OK;
 }

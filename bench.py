@@ -888,7 +888,7 @@ def infer_m_sweep(m, w, g, dev, flush, peaks):
     bf = torch.bfloat16
     wbytes = (3 if w.gated else 2) * w.H * w.I * 2
     rows = []
-    for M in (1, 2, 3, 4, 16, 64, 128, 256, 512):
+    for M in (1, 2, 3, 4, 8, 16, 17, 32, 64, 128, 256, 512):
         prob = m.problem(M, w.H, w.I, w.act, w.gate_mult, w.down_mult)
         x = torch.randn(M, w.H, device=dev).to(bf)
         out = torch.empty(M, w.H, dtype=bf, device=dev)
@@ -916,7 +916,34 @@ def infer_m_sweep(m, w, g, dev, flush, peaks):
                 ts.append(e0.elapsed_time(e1))
             res[name] = sorted(ts)[len(ts) // 2] * 1e3  # median, us
         best = min(res.values())
-        rows.append({"M": M, "direct_us": res["direct"], "graph_us": res["graph"],
+        path = ("warp_mma_stream", "cuda_core_stream", "tensor_core_gemm")[
+            [2, 1, 0].index(m.mlp_plan(prob, m.MODE_INFER)["decode"])]
+        # the CUDA-core weight stream on the same call, where it applies
+        fma_us = None
+        m.mlp_debug_set_flags(m.DEBUG_DECODE_FMA)
+        try:
+            if m.mlp_plan(prob, m.MODE_INFER)["decode"] == 1:
+                for _ in range(3):
+                    call()
+                torch.cuda.synchronize(dev)
+                g2 = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g2):
+                    call()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                ts = []
+                for _ in range(20):
+                    flush.zero_()
+                    e0.record()
+                    g2.replay()
+                    e1.record()
+                    torch.cuda.synchronize(dev)
+                    ts.append(e0.elapsed_time(e1))
+                fma_us = sorted(ts)[len(ts) // 2] * 1e3
+        finally:
+            m.mlp_debug_set_flags(0)
+        rows.append({"M": M, "path": path, "direct_us": res["direct"], "graph_us": res["graph"],
+                     "cuda_core_graph_us": fma_us,
                      "tflops": (6 if w.gated else 4) * M * w.H * w.I / (best * 1e-6) / 1e12,
                      "weight_gbs": wbytes / (best * 1e-6) / 1e9,
                      "hbm_frac": wbytes / (best * 1e-6) / 1e9 / float(peaks["hbm_gbs"])})

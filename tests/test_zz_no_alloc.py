@@ -12,7 +12,7 @@ equal, except where the down projection splits K (few output tiles, a long
 K): its fp32 partial sums then meet by atomic adds in no fixed order, and
 the two agree to rounding.  The shapes cover the
 tensor-core path (single-CTA and CTA-pair tiles, the one-launch gated
-forward) and the CUDA-core path of one to four tokens.  The status word of
+forward) and the weight-streaming path of one to sixteen tokens.  The status word of
 the array is read with mlp_noalloc_status, including after a bounded wait
 that was made to expire.  This file sorts last so that a run stopping at the
 first failure has already run every other test; it also passes alone in a
@@ -46,7 +46,8 @@ def _noalloc(L, prob, t, out, stream):
     ("swiglu", 1.0, 1.0, (300, 264, 392)),
     ("swiglu", 1.125, 2.0, (512, 4096, 14336)),
     ("relu_sq", 1.0, 1.0, (257, 768, 3072)),
-    ("swiglu", 1.0, 1.0, (3, 4096, 14336)),   # one to four tokens: the CUDA-core path
+    ("swiglu", 1.0, 1.0, (3, 4096, 14336)),   # one to sixteen tokens: the weight stream
+    ("swiglu", 1.0, 1.0, (16, 4096, 14336)),
     ("relu_sq", 1.0, 1.0, (1, 768, 3072)),
 ])
 def test_noalloc_matches_workspace_entry_point(act, gm, dm, shape):
