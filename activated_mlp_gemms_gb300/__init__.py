@@ -26,6 +26,7 @@ __all__ = [
     "Block", "block", "mlp_block_fwd", "mlp_block_bwd", "mlp_fp8_quantize", "mlp_fp8_fwd",
     "MODE_FP8_FWD", "mlp_fp8_bwd", "MODE_FP8_BWD",
     "NOALLOC_SCRATCH_BYTES", "mlp_set_wait_timeout_ms", "mlp_debug_set_flags", "DEBUG_NO_WORK", "DEBUG_DECODE_FMA",
+    "DEBUG_DECODE_MMA",
     "mlp_noalloc_status", "mlp_fp8_refresh_scales", "Plan", "mlp_plan", "mlp_debug_hold_sms",
 ]
 
@@ -39,6 +40,7 @@ MODE_FWD, MODE_INFER, MODE_BWD, MODE_BWD_RECOMPUTE, MODE_FP8_FWD, MODE_FP8_BWD =
 NOALLOC_SCRATCH_BYTES = 16 << 20  # MLP_NOALLOC_SCRATCH_BYTES
 DEBUG_NO_WORK = 1  # MLP_DEBUG_NO_WORK
 DEBUG_DECODE_FMA = 2  # MLP_DEBUG_DECODE_FMA
+DEBUG_DECODE_MMA = 4  # MLP_DEBUG_DECODE_MMA
 
 
 class MlpError(RuntimeError):
@@ -422,6 +424,6 @@ def mlp_set_wait_timeout_ms(ms: int) -> None:
 
 def mlp_debug_set_flags(flags: int) -> None:
     """Testing hooks: DEBUG_NO_WORK makes later calls time out on purpose;
-    DEBUG_DECODE_FMA sends forwards of one to four tokens to the CUDA-core
-    weight stream instead of the warp-MMA one."""
+    DEBUG_DECODE_FMA / DEBUG_DECODE_MMA force the decode-sized forward onto
+    the CUDA-core or the warp-MMA weight stream."""
     _check(lib().mlp_debug_set_flags(int(flags)), "mlp_debug_set_flags")

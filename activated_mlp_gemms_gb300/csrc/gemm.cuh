@@ -1025,10 +1025,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
             }
           }
           if (unit >= p.total_units) break;
-          // the next unit, fetched now and needed when it is published
-          const int next = (CLAIM_ALL ? 0 : ncl) + atomicAdd(p.counter, 1);
-          bool published = !EARLY_PUB;
           const Work w = decode_unit(p, unit);
+          // The next unit, fetched now and needed when it is published.  A
+          // down unit of the fused forward (K = I, several times a gate/up
+          // unit's length) fetches it only when it publishes it, half-way
+          // through: fetched at its start, the last down units of the queue
+          // went two to a pair while other pairs found the queue empty, and
+          // a forward of a few hundred tokens took one down unit longer.
+          const bool late_claim = CLAIM_ALL && w.prob == 1;
+          int next = late_claim ? -1 : (CLAIM_ALL ? 0 : ncl) + atomicAdd(p.counter, 1);
+          auto claim = [&] {
+            if (late_claim) next = atomicAdd(p.counter, 1);
+          };
+          bool published = !EARLY_PUB;
           const UnitLoads L = unit_loads<EPI, CG>(p, p.prob[w.prob], w, rank);
           if constexpr (EpiTraits<EPI>::DACT) {
             // the epilogue reads this tile's saved inputs a tile or two later
@@ -1058,6 +1067,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
             ++issued;
             if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
             if (!published && kb == w.kb_begin + (w.kb_end - w.kb_begin) / 2) {
+              claim();
               if (!publish(next < p.total_units ? next : -1)) {
                 ok = false;
                 break;
@@ -1065,7 +1075,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
               published = true;
             }
           }
-          if (ok && !published && !publish(next < p.total_units ? next : -1)) ok = false;
+          if (ok && !published) {
+            claim();
+            if (!publish(next < p.total_units ? next : -1)) ok = false;
+          }
           unit = next;
         } else {
           // peer of a pair: take units from the ring the leader fills

@@ -174,16 +174,20 @@ int device_act(int act) {
 std::atomic<int> g_tile_policy{0};
 
 // Which kernels a forward of few tokens streams its weights with (unless a
-// tile policy forces the tensor-core GEMMs): 2, the warp-MMA weight stream,
-// for at most DECODE_MMA_MAX_M tokens; 1, the CUDA-core one, only when
-// MLP_DEBUG_DECODE_FMA asks for it and its token rows fit a CTA's shared
-// memory; 0, the tensor-core GEMMs.
+// tile policy forces the tensor-core GEMMs): 1, the CUDA-core stream, for
+// one or two tokens whose rows fit a CTA's shared memory (measured 3-6 %
+// faster than the warp-MMA stream there); 2, the warp-MMA stream, for the
+// others up to DECODE_MMA_MAX_M tokens; 0, the tensor-core GEMMs.  The
+// testing flags force one stream: MLP_DEBUG_DECODE_FMA the CUDA-core one
+// (up to four tokens that fit), MLP_DEBUG_DECODE_MMA the warp-MMA one.
 int decode_kernel(const mlp_problem_t* p) {
   const int pol = g_tile_policy.load();
   if ((pol != 0 && pol != 3) || p->M > DECODE_MMA_MAX_M) return 0;
+  const int flags = g_debug_flags.load();
+  if (flags & MLP_DEBUG_DECODE_MMA) return 2;
   const long long k = p->H > p->I ? p->H : p->I;
   const bool fma_fits = p->M <= DECODE_MAX_M && (long long)p->M * k * 2 <= DECODE_MAX_TOKEN_BYTES;
-  if (fma_fits && (g_debug_flags.load() & MLP_DEBUG_DECODE_FMA)) return 1;
+  if (fma_fits && (p->M <= 2 || (flags & MLP_DEBUG_DECODE_FMA))) return 1;
   return 2;
 }
 
@@ -1315,7 +1319,8 @@ int mlp_set_wait_timeout_ms(unsigned int ms) {
 }
 
 int mlp_debug_set_flags(int flags) {
-  if (flags & ~(MLP_DEBUG_NO_WORK | MLP_DEBUG_DECODE_FMA)) return MLP_ERR_INVALID_ARG;
+  if (flags & ~(MLP_DEBUG_NO_WORK | MLP_DEBUG_DECODE_FMA | MLP_DEBUG_DECODE_MMA))
+    return MLP_ERR_INVALID_ARG;
   g_debug_flags.store(flags);
   return MLP_OK;
 }

@@ -9,7 +9,8 @@ default workload is the largest, the Llama-3-8B-shaped MLP (8192 tokens,
 4096 x 14336, backward recomputing the preacts), with its no-grad inference
 forward beside it; the other four workloads (and, for the ReLU^2 one, the
 FP8 step and the block with its neighbours) are measured for the breakdown
-with a few steps each unless --headline-only is given.
+with a few steps each, and the inference forward of 1 to 512 tokens with the
+same weights (decode sizes), unless --headline-only is given.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--headline-only]
     python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host cores
@@ -55,7 +56,8 @@ def parse():
     ap.add_argument("--block", action="store_true",
                     help="also time the MLP block with its fused RMS norm and residual add")
     ap.add_argument("--sweep-m", action="store_true",
-                    help="also time the inference forward at decode-sized token counts")
+                    help="time the inference forward at decode-sized token counts even with "
+                         "--headline-only (the default run includes it)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count M (small cases for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -662,7 +664,9 @@ def run_ours(args, rank, world, local_rank):
                  "pct_of_peak": 100.0 * flops_of(w, "infer") / (im * 1e-3) / 1e12
                  / float(peaks["bf16_tflops"])}
 
-    sweep = infer_m_sweep(m, w, g, dev, flush, peaks) if args.sweep_m else None
+    # the decode-sized inference forward: part of the default single-GPU run
+    do_sweep = args.sweep_m or (world == 1 and not args.headline_only)
+    sweep = infer_m_sweep(m, w, g, dev, flush, peaks) if do_sweep else None
     block = block_step(m, w, g, dev, flush, K) if args.block else None
     fp8 = fp8_forward(m, w, g, dev, flush, K, peaks) if (args.fp8 and w.act == "relu_sq") else None
     launches = per_step * K if kernels else None
@@ -918,32 +922,36 @@ def infer_m_sweep(m, w, g, dev, flush, peaks):
         best = min(res.values())
         path = ("warp_mma_stream", "cuda_core_stream", "tensor_core_gemm")[
             [2, 1, 0].index(m.mlp_plan(prob, m.MODE_INFER)["decode"])]
-        # the CUDA-core weight stream on the same call, where it applies
-        fma_us = None
-        m.mlp_debug_set_flags(m.DEBUG_DECODE_FMA)
-        try:
-            if m.mlp_plan(prob, m.MODE_INFER)["decode"] == 1:
-                for _ in range(3):
-                    call()
-                torch.cuda.synchronize(dev)
-                g2 = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g2):
-                    call()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                ts = []
-                for _ in range(20):
-                    flush.zero_()
-                    e0.record()
-                    g2.replay()
-                    e1.record()
+        # the other weight stream on the same call, where both apply (1-4 tokens)
+        alt_path, alt_us = None, None
+        if path != "tensor_core_gemm" and M <= 4:
+            alt = "cuda_core_stream" if path == "warp_mma_stream" else "warp_mma_stream"
+            m.mlp_debug_set_flags(m.DEBUG_DECODE_FMA if alt == "cuda_core_stream"
+                                  else m.DEBUG_DECODE_MMA)
+            try:
+                if m.mlp_plan(prob, m.MODE_INFER)["decode"] == (1 if alt == "cuda_core_stream" else 2):
+                    alt_path = alt
+                    for _ in range(3):
+                        call()
                     torch.cuda.synchronize(dev)
-                    ts.append(e0.elapsed_time(e1))
-                fma_us = sorted(ts)[len(ts) // 2] * 1e3
-        finally:
-            m.mlp_debug_set_flags(0)
+                    g2 = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g2):
+                        call()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    ts = []
+                    for _ in range(20):
+                        flush.zero_()
+                        e0.record()
+                        g2.replay()
+                        e1.record()
+                        torch.cuda.synchronize(dev)
+                        ts.append(e0.elapsed_time(e1))
+                    alt_us = sorted(ts)[len(ts) // 2] * 1e3
+            finally:
+                m.mlp_debug_set_flags(0)
         rows.append({"M": M, "path": path, "direct_us": res["direct"], "graph_us": res["graph"],
-                     "cuda_core_graph_us": fma_us,
+                     "alt_path": alt_path, "alt_graph_us": alt_us,
                      "tflops": (6 if w.gated else 4) * M * w.H * w.I / (best * 1e-6) / 1e12,
                      "weight_gbs": wbytes / (best * 1e-6) / 1e9,
                      "hbm_frac": wbytes / (best * 1e-6) / 1e9 / float(peaks["hbm_gbs"])})

@@ -138,10 +138,13 @@ size_t mlp_workspace_size(const mlp_problem_t* p, int mode);
  * bf16 values written to `out` are bitwise identical to mlp_fwd_infer's.
  * With one to sixteen tokens (decode), unless a tile policy is set (below),
  * the forward streams the weights instead of running tensor-core GEMM
- * tiles: each CTA owns 16 weight rows, its warps read them in 128-byte
+ * tiles (two kernels, no split-K region used): with three to sixteen
+ * tokens each CTA owns 16 weight rows, its warps read them in 128-byte
  * pieces per row and accumulate the M dot products with the warp-level MMA
- * (mma.sync, bf16 in, fp32 accumulate) straight from the loaded registers
- * (two kernels, no split-K region used). */
+ * (mma.sync, bf16 in, fp32 accumulate) straight from the loaded registers;
+ * with one or two tokens (M * max(H, I) * 2 <= 112 KiB) each warp reads
+ * whole weight rows front to back and accumulates with fp32 fused
+ * multiply-adds on the CUDA cores. */
 int mlp_fwd(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu,
             const void* Wd, void* out, void* G_save, void* U_save,
             void* ws, size_t ws_bytes, void* stream);
@@ -370,7 +373,7 @@ int mlp_noalloc_status(void* stream);
  * policy.  The split-K factors depend on the device's SM count. */
 typedef struct {
   int decode;           /* the forward streams the weights (1-16 tokens): 2 with the warp-level
-                           MMA, 1 on the CUDA cores (MLP_DEBUG_DECODE_FMA); 0: GEMM tiles */
+                           MMA, 1 on the CUDA cores; 0: GEMM tiles */
   int fused_forward;    /* 1: the gated forward's gate/up and down GEMMs are one launch */
   int cta_group;        /* CTA-group size (1 or 2) of the GEMMs over token rows */
   int out_split;        /* split-K factor of the [M,H] output GEMM (down projection, or dx) */
@@ -404,13 +407,15 @@ int mlp_set_tile_policy(int policy);
  * mlp_debug_set_flags(MLP_DEBUG_NO_WORK) makes the kernels' tile schedulers
  * publish no work, so the bounded waits of every later call expire (a test
  * of the timeout path that issues no copy and no MMA); 0 restores normal
- * operation.  MLP_DEBUG_DECODE_FMA sends forwards of one to four tokens
- * whose token rows fit a CTA's shared memory (M * max(H, I) * 2 <= 112 KiB)
- * to the CUDA-core weight stream (each warp reads whole weight rows and
- * accumulates with fp32 fused multiply-adds) instead of the warp-MMA one.
- * Flags may be combined; both settings are process-wide. */
+ * operation.  The decode flags pick one of the two weight streams of the
+ * decode-sized forward (mlp_fwd): MLP_DEBUG_DECODE_FMA the CUDA-core one for
+ * one to four tokens whose token rows fit a CTA's shared memory
+ * (M * max(H, I) * 2 <= 112 KiB), MLP_DEBUG_DECODE_MMA the warp-MMA one for
+ * one to sixteen tokens (it wins when both are set).  Flags may be
+ * combined; both settings are process-wide. */
 #define MLP_DEBUG_NO_WORK 1
 #define MLP_DEBUG_DECODE_FMA 2
+#define MLP_DEBUG_DECODE_MMA 4
 int mlp_set_wait_timeout_ms(unsigned int ms);
 int mlp_debug_set_flags(int flags);
 

@@ -205,9 +205,10 @@ def test_tile_policy_values(L):
 
 
 def test_debug_hooks_validate(L):
-    assert L.mlp_debug_set_flags(4) == -1
+    assert L.mlp_debug_set_flags(8) == -1
     assert L.mlp_debug_set_flags(-1) == -1
     assert L.mlp_debug_set_flags(2) == 0  # MLP_DEBUG_DECODE_FMA
+    assert L.mlp_debug_set_flags(4) == 0  # MLP_DEBUG_DECODE_MMA
     assert L.mlp_debug_set_flags(0) == 0
     assert L.mlp_set_wait_timeout_ms(0) == 0
 

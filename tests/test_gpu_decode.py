@@ -2,9 +2,9 @@
 streams the weights instead of running GEMM tiles, against the fp64 oracle,
 through the C ABI.
 
-Two weight streams: the warp-MMA one (the default, up to sixteen tokens)
-and the CUDA-core one (MLP_DEBUG_DECODE_FMA, up to four tokens whose rows
-fit shared memory).  The same guard bands and NaN-filled outputs as the
+Two weight streams: the warp-MMA one (three to sixteen tokens by default)
+and the CUDA-core one (one or two tokens by default, up to four whose rows
+fit shared memory when forced); the debug flags force either.  The same guard bands and NaN-filled outputs as the
 other parity tests; the training forward's saved preacts (G, U) come from
 the same kernels."""
 import contextlib
@@ -24,8 +24,8 @@ PLAN_MMA, PLAN_FMA, PLAN_TC = 2, 1, 0
 
 @contextlib.contextmanager
 def decode_kernel(kind):
-    """kind "mma" (default) or "fma" (the CUDA-core stream)."""
-    m.mlp_debug_set_flags(m.DEBUG_DECODE_FMA if kind == "fma" else 0)
+    """kind "mma" or "fma": force that weight stream; others: the default choice."""
+    m.mlp_debug_set_flags({"fma": m.DEBUG_DECODE_FMA, "mma": m.DEBUG_DECODE_MMA}.get(kind, 0))
     try:
         yield
     finally:
@@ -117,6 +117,23 @@ def test_decode_path_is_two_kernels_and_graph_capturable(M, kind):
             g.replay()
             torch.cuda.synchronize()
             assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("M,I,plan", [(1, 14336, PLAN_FMA), (2, 14336, PLAN_FMA),
+                                      (2, 32768, PLAN_MMA), (3, 14336, PLAN_MMA),
+                                      (16, 14336, PLAN_MMA), (17, 14336, PLAN_TC)])
+def test_default_decode_stream(M, I, plan):
+    """Without a flag: the CUDA-core stream for one or two tokens whose rows
+    fit shared memory, the warp-MMA one for the others up to sixteen, then
+    the tensor-core GEMMs; a tile policy keeps every size on the GEMMs."""
+    prob = m.problem(M, 4096, I)
+    assert m.mlp_plan(prob, m.MODE_INFER)["decode"] == plan
+    assert m.mlp_plan(prob, m.MODE_FWD)["decode"] == plan
+    m.mlp_set_tile_policy(1)
+    try:
+        assert m.mlp_plan(prob, m.MODE_INFER)["decode"] == PLAN_TC
+    finally:
+        m.mlp_set_tile_policy(0)
 
 
 @pytest.mark.parametrize("M,I,plan", [(3, 14336, PLAN_FMA), (4, 14336, PLAN_FMA),
