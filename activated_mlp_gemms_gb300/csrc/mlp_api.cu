@@ -480,19 +480,45 @@ bool gated(const mlp_problem_t* p) {
 size_t inter_bytes(const mlp_problem_t* p) { return round256((size_t)p->M * p->I * 2); }
 
 // Split-K factor of a bf16-output GEMM [rows, cols] x K whose output tiles
-// cannot fill the GPU (decode-sized token counts): the splits' fp32 partial
-// sums meet in a zeroed region of the workspace (TMA reduce-add) and one
-// elementwise pass converts it to bf16.  It depends on the shape only, so
-// the workspace size does too.  Aims at ~128 work units with at least 8
-// k-blocks each.
-int bf16_split(int rows, int cols, int K) {
+// cannot fill the GPU: the splits' fp32 partial sums meet in a zeroed region
+// of the workspace (TMA reduce-add) and one elementwise pass converts it to
+// bf16.  It depends on the shape only (a nominal 152 SMs), so the workspace
+// size does too.
+//  - Decode-sized token counts (at most 32 tiles of 128 x 256): about 128
+//    work units with at least 8 k-blocks each.
+//  - `fill` (the forward's down projection): when its 256 x 256 tiles (CTA
+//    pairs) would occupy at most half of the 76 pairs, the smallest split
+//    whose units fill at least 80 % of their last wave, again with at least
+//    8 k-blocks a unit.  (A 512-token Llama-3-8B down projection is 32 such
+//    tiles.)  Measured against the unsplit forward (the gated forward then
+//    runs as one launch): 9-13 % faster at 384 and 512 tokens of the
+//    4096-wide shapes, 3-10 % at 640-1024 tokens of a 2048-wide one; with
+//    more tiles, splitting until the units filled their waves lost to the
+//    one-launch forward.  The backward's dx is left whole: its last wave
+//    shares the GPU with the weight gradients on the second stream.
+constexpr int SPLIT_NOMINAL_SMS = 152;
+int bf16_split(int rows, int cols, int K, bool fill) {
   const long long tiles =
       (long long)((rows + BM - 1) / BM) * (long long)((cols + MMA_N - 1) / MMA_N);
   const int kb = (K + BK - 1) / BK;
-  if (tiles > 32 || kb < 16) return 1;
-  int split = static_cast<int>(128 / tiles);
-  if (split > kb / 8) split = kb / 8;
-  return split < 2 ? 1 : split;
+  if (kb < 16) return 1;
+  if (tiles <= 32) {
+    int split = static_cast<int>(128 / tiles);
+    if (split > kb / 8) split = kb / 8;
+    return split < 2 ? 1 : split;
+  }
+  if (!fill) return 1;
+  // 256 x 256 tiles on CTA pairs (rows > 128 take pairs)
+  const int pairs = SPLIT_NOMINAL_SMS / 2;
+  const long long ptiles =
+      (long long)((rows + 2 * BM - 1) / (2 * BM)) * (long long)((cols + MMA_N - 1) / MMA_N);
+  if (2 * ptiles > pairs) return 1;
+  for (int s = 2; s <= 8 && kb / s >= 8; ++s) {
+    const long long units = ptiles * s;
+    const long long waves = (units + pairs - 1) / pairs;
+    if (units * 5 >= waves * pairs * 4) return s;
+  }
+  return 1;
 }
 
 // K of the bf16-output GEMM of a mode: the down projection (forward) or dx.
@@ -501,8 +527,14 @@ int split_k_of(const mlp_problem_t* p, int mode) {
   return gated(p) ? 2 * p->I : p->I;
 }
 
+// The split-K factor of a mode's [M,H] output GEMM.
+int out_split_of(const mlp_problem_t* p, int mode) {
+  const bool fwd = mode == MLP_MODE_FWD || mode == MLP_MODE_INFER;
+  return bf16_split(p->M, p->H, split_k_of(p, mode), fwd);
+}
+
 size_t split_bytes(const mlp_problem_t* p, int mode) {
-  return bf16_split(p->M, p->H, split_k_of(p, mode)) > 1 ? round256((size_t)p->M * p->H * 4) : 0;
+  return out_split_of(p, mode) > 1 ? round256((size_t)p->M * p->H * 4) : 0;
 }
 
 size_t ws_size(const mlp_problem_t* p, int mode) {
@@ -765,7 +797,7 @@ int forward(const mlp_problem_t* p, const void* x, const void* Wg, const void* W
                      : launch_decode_down(a, Wd, out, p->M, p->H, p->I, c.stream, pdl1);
     });
   }
-  const int split = bf16_split(p->M, p->H, split_k_of(p, mode));
+  const int split = out_split_of(p, mode);
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + split_offset(p, mode));
   if (split > 1)
     MLP_TRY(cuda_err(cudaMemsetAsync(part, 0, (size_t)p->M * p->H * 4, c.stream)));
@@ -814,7 +846,7 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
   Call c;
   MLP_TRY(begin_call(c, ws, stream));
   char* base = static_cast<char*>(ws) + CTRL_BYTES;
-  const int dx_split = dx ? bf16_split(p->M, p->H, split_k_of(p, mode)) : 1;
+  const int dx_split = dx ? out_split_of(p, mode) : 1;
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + split_offset(p, mode));
   if (dx_split > 1)
     MLP_TRY(cuda_err(cudaMemsetAsync(part, 0, (size_t)p->M * p->H * 4, c.stream)));
@@ -1264,7 +1296,7 @@ int mlp_plan(const mlp_problem_t* p, int mode, int fuse_grad_accum, mlp_plan_t* 
   const bool fwd = mode == MLP_MODE_FWD || mode == MLP_MODE_INFER;
   plan->decode = fwd ? decode_kernel(p) : 0;
   plan->cta_group = pick_cg(p->M);
-  plan->out_split = (fp8 || plan->decode) ? 1 : bf16_split(p->M, p->H, split_k_of(p, mode));
+  plan->out_split = (fp8 || plan->decode) ? 1 : out_split_of(p, mode);
   plan->fused_forward = (fwd && !plan->decode && fused_forward(p, plan->out_split)) ? 1 : 0;
   if (!fwd && mode != MLP_MODE_FP8_FWD) {
     const int cg = pick_cg(p->H < p->I ? p->H : p->I);

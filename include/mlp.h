@@ -119,10 +119,13 @@ typedef enum {
  * arguments).  FWD/INFER/BWD: the control block plus one bf16 [M,I] buffer
  * (the postact); BWD_RECOMPUTE: plus the recomputed preacts, two bf16
  * [M,I] buffers when gated, one when not.  When the [M,H] output GEMM (the
- * down projection, or dx) has too few output tiles to fill the GPU
- * (decode-sized M: at most 32 tiles of 128 x 256 and K >= 1024), the GEMM
- * splits K and the workspace also holds one fp32 [M,H] partial-sum region.
- * The size depends on the problem and mode only. */
+ * down projection, or dx) has too few output tiles to fill the GPU, the GEMM
+ * splits K and the workspace also holds one fp32 [M,H] partial-sum region:
+ * decode-sized M (at most 32 tiles of 128 x 256 and K >= 1024), and for the
+ * forward's down projection also at most 38 tiles of 256 x 256 (half of 76
+ * CTA pairs: e.g. 384 or 512 tokens of a 4096-wide model), split so that
+ * the units fill at least 80 % of their last wave.  The size depends on the
+ * problem and mode only. */
 size_t mlp_workspace_size(const mlp_problem_t* p, int mode);
 
 /* Training forward (flash-swiglu-mlp README "Design notes", forward fusion;

@@ -68,6 +68,16 @@ def test_workspace_sizes(L):
     r256 = lambda n: (n + 255) // 256 * 256  # noqa: E731
     assert m.mlp_workspace_size(d, m.MODE_INFER) == 1024 + r256(16 * 14336 * 2) + 16 * 4096 * 4
     assert m.mlp_workspace_size(d, m.MODE_BWD) == 1024 + r256(16 * 14336 * 2) + 16 * 4096 * 4
+    # a partial wave of down-projection tiles (512 tokens: 32 tiles of 256 x 256
+    # on 76 CTA pairs): the forward splits K and needs the fp32 region, the
+    # backward's dx does not
+    e = m.problem(512, 4096, 14336)
+    assert m.mlp_workspace_size(e, m.MODE_INFER) == 1024 + 512 * 14336 * 2 + 512 * 4096 * 4
+    assert m.mlp_workspace_size(e, m.MODE_FWD) == 1024 + 512 * 14336 * 2 + 512 * 4096 * 4
+    assert m.mlp_workspace_size(e, m.MODE_BWD) == 1024 + 512 * 14336 * 2
+    # more than half the pairs (1024 tokens: 64 tiles) is left whole
+    f = m.problem(1024, 4096, 14336)
+    assert m.mlp_workspace_size(f, m.MODE_INFER) == 1024 + 1024 * 14336 * 2
     assert m.mlp_workspace_size(m.problem(64, 128, 352), m.MODE_INFER) == 1024 + 64 * 352 * 2
     assert m.mlp_workspace_size(m.problem(0, 8, 8), 0) == 0
     assert m.mlp_workspace_size(m.problem(8, 12, 8), 0) == 0  # H % 8 != 0

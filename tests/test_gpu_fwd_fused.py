@@ -42,12 +42,13 @@ def _forward(prob, d, M, H, I, save, policy):
 
 
 @pytest.mark.parametrize("act", GATED)
-@pytest.mark.parametrize("M,H,I", [(300, 200, 392), (1000, 2056, 1544), (2048 + 77, 520, 1160)])
+@pytest.mark.parametrize("M,H,I", [(300, 200, 392), (1000, 2568, 1544), (2048 + 77, 520, 1160)])
 def test_fused_forward_equals_two_launches_and_the_oracle(act, M, H, I):
     """Ragged token blocks (M not a multiple of 256), a ragged last gate/up
     tile (I not a multiple of 128) and a ragged last down tile (H not a
-    multiple of 256).  (Shapes whose down projection would split K, with few
-    output tiles and a long K, keep the two launches.)"""
+    multiple of 256).  (Shapes whose down projection would split K keep the
+    two launches: few output tiles and a long K, or at most 38 output tiles
+    of 256 x 256, half the GPU's CTA pairs.)"""
     t = make_inputs(M, H, I, act, seed=41)
     d = dev_tensors(t)
     prob = m.problem(M, H, I, act, 1.125, 2.0)
@@ -95,7 +96,7 @@ def test_fused_inference_forward(M, I):
 def test_fused_block_forward():
     """The block's forward: the RMS norm's scale on the gate/up tiles and the
     residual add in the down tiles, fused the same way."""
-    M, H, I = 1000, 2048, 1408
+    M, H, I = 1000, 2560, 1408
     kw = dict(resid_lambda=1.1 ** 0.5, post_lambda=0.8, eps=2.0 ** -7)
     t = make_inputs(M, H, I, "swiglu", seed=43)
     d = dev_tensors(t)
@@ -127,7 +128,7 @@ def test_fused_forward_graph_replays():
     """Captured in a CUDA graph, replays of the fused forward (its block
     counts reset by each call's control-block clear) give the direct call's
     result bitwise."""
-    M, H, I = 2048, 1024, 2816
+    M, H, I = 2048, 1280, 2816
     d = dev_tensors(make_inputs(M, H, I, "swiglu", seed=44))
     prob = m.problem(M, H, I)
     ws = m.alloc_workspace(prob, m.MODE_FWD)
@@ -162,7 +163,7 @@ def test_fused_forward_with_most_sms_held_by_another_stream():
     contention.  (With a unit per pair fixed in advance, the pairs that are
     not resident would own gate/up tiles the down units wait for, and the
     waits would expire.)"""
-    M, H, I, act = 2048, 1024, 4096, "swiglu"
+    M, H, I, act = 2048, 1280, 4096, "swiglu"
     t = make_inputs(M, H, I, act, seed=44)
     d = dev_tensors(t)
     prob = m.problem(M, H, I, act)

@@ -313,7 +313,8 @@ def test_dwd_only_postact_kernel(act):
 @pytest.mark.parametrize("M", [1, 16, 64, 200])
 def test_small_m_split_k(act, M):
     """Few tokens: the down projection (and dx) split K so that their few
-    output tiles still use the whole GPU; the partial sums meet in fp32."""
+    output tiles still use the whole GPU; the partial sums meet in fp32.
+    (1 and 16 tokens take the weight-streaming forward, then the split dx.)"""
     H, I = 512, 2048  # 2 output tiles per 128 rows, K = 2048 (forward), 4096 (gated dx)
     t = make_inputs(M, H, I, act, seed=12)
     got, bad, _ = run_gpu(dev_tensors(t), M, H, I, act, 1.125, 2.0, mode="recompute")
@@ -325,6 +326,25 @@ def test_small_m_split_k(act, M):
     m.mlp_fwd_infer(m.problem(M, H, I, act, 1.125, 2.0), d["x"], d["Wg"], d["Wu"], d["Wd"], o2)
     torch.cuda.synchronize()
     assert rel_err(to_f64(o2), to_f64(got["out"])) < 1e-2
+
+
+@pytest.mark.parametrize("act", ["swiglu", "relu_sq"])
+def test_forward_split_k_fills_a_partial_wave(act):
+    """640 tokens with H = 2048: the down projection's 24 output tiles of
+    256 x 256 would occupy a third of the 76 CTA pairs, so the forward splits
+    K three ways (72 units, 95 % of one wave) and runs as two launches; the
+    backward's dx stays whole.  Against the oracle, the training forward with
+    its saved preacts and the backward from them."""
+    M, H, I = 640, 2048, 4096
+    prob = m.problem(M, H, I, act, 1.125, 2.0)
+    assert m.mlp_plan(prob, m.MODE_INFER)["out_split"] == 3
+    assert m.mlp_plan(prob, m.MODE_FWD)["out_split"] == 3
+    assert m.mlp_plan(prob, m.MODE_BWD)["out_split"] == 1
+    assert m.mlp_plan(prob, m.MODE_FWD)["fused_forward"] == 0
+    t = make_inputs(M, H, I, act, seed=14)
+    got, bad, _ = run_gpu(dev_tensors(t), M, H, I, act, 1.125, 2.0, mode="saved")
+    assert not bad
+    compare_full(got, oracle_full(t, act, 1.125, 2.0), fuse=False)
 
 
 def test_inference_forward_in_a_cuda_graph():

@@ -44,7 +44,8 @@ def _noalloc(L, prob, t, out, stream):
 
 @pytest.mark.parametrize("act,gm,dm,shape", [
     ("swiglu", 1.0, 1.0, (300, 264, 392)),
-    ("swiglu", 1.125, 2.0, (512, 4096, 14336)),
+    ("swiglu", 1.125, 2.0, (1024, 4096, 4096)),  # the one-launch gated forward
+    ("swiglu", 1.0, 1.0, (200, 1024, 4096)),      # a split-K down projection
     ("relu_sq", 1.0, 1.0, (257, 768, 3072)),
     ("swiglu", 1.0, 1.0, (3, 4096, 14336)),   # one to sixteen tokens: the weight stream
     ("swiglu", 1.0, 1.0, (16, 4096, 14336)),
