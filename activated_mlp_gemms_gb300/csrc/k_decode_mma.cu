@@ -4,12 +4,13 @@
 //
 // With M <= 16 tokens the forward reads every weight once and does M
 // multiply-adds per weight element, so it is bound by HBM, not by any
-// arithmetic unit.  On the CUDA cores the multiply-adds (plus the bf16 ->
-// fp32 conversions) cost about 19 instructions per weight element per
-// token, which at four tokens already outruns the instruction issue.  The
-// warp-level MMA takes a 16-row x 16-k weight fragment and a 16-k x 8-token
-// fragment straight from registers: one 16-byte weight load per lane feeds
-// two MMAs, and the kernel issues about 12 instructions per 2 KB of weights.
+// arithmetic unit.  On the CUDA cores every weight element costs a bf16 ->
+// fp32 conversion and, per token, a token conversion and a fused
+// multiply-add; at four tokens that already outruns the instruction issue.
+// The warp-level MMA takes a 16-row x 16-k weight fragment and a 16-k x
+// 8-token fragment straight from registers: one 16-byte weight load per lane
+// feeds two MMAs, and the kernel issues about 12 instructions per 2 KB of
+// weights.
 //
 // Fragments without shuffles.  The MMA's k index is a summation index, so
 // any permutation of k that A and B share gives the same dot products.  Lane
@@ -23,7 +24,8 @@
 // Work.  A CTA owns 16 consecutive weight rows (of Wg and Wu for the gated
 // pass) and all of K; its S warps take the 64-wide k groups round-robin
 // (warp w: groups w, w + S, ...), with two groups in flight per warp
-// (registers double-buffered).  The warps' partial sums meet in shared
+// (registers double-buffered).  S is the most warps with which the whole
+// grid is resident at once (md_warps).  The warps' partial sums meet in shared
 // memory; the CTA's first warp applies the epilogue.  The token rows are
 // read through L1/L2 (they are small and every CTA reads them); the weights
 // with no L1 allocation (each is read once).  The weights do not depend on
@@ -31,9 +33,9 @@
 // waiting for it.
 //
 // Epilogues (MODE, as the CUDA-core decode kernel's):
-//   DEC_GATED    y0 = x Wg^T, y1 = x Wu^T:  a = s*act(y0)*y1 (+ G = y0, U = y1)
-//   DEC_NONGATED y0 = x W1^T:               a = s*act(y0)    (+ P = y0)
-//   DEC_STORE    y0 = a Wd^T:               out = y0
+//   MD_GATED    y0 = x Wg^T, y1 = x Wu^T:  a = s*act(y0)*y1 (+ G = y0, U = y1)
+//   MD_NONGATED y0 = x W1^T:               a = s*act(y0)    (+ P = y0)
+//   MD_STORE    y0 = a Wd^T:               out = y0
 #include <atomic>
 
 #include "act.cuh"
