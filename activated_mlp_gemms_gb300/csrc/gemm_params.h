@@ -166,14 +166,15 @@ cudaError_t launch_hold(int ctas, unsigned long long ns, cudaStream_t stream);
 // (or fc1) pass with its activation (a, and G/U or P when given), and the
 // down projection out = a Wd^T.  `act` is a device activation (Act).  Each
 // CTA stages the M token rows of its K (H, then I) whole in shared memory:
-// M * K * 2 <= DECODE_MAX_TOKEN_BYTES.
+// M * K * 2 <= DECODE_MAX_TOKEN_BYTES.  The gate/up pass, the first kernel
+// of its call, also clears the call's status word (`status`, may be null).
 constexpr int DECODE_MAX_M = 4;
 // (112 KiB: four token rows of a 14336-wide intermediate; two such CTAs,
 // with the 1 KiB each reserves, fit an SM's 228 KiB of shared memory)
 constexpr int DECODE_MAX_TOKEN_BYTES = 112 * 1024;
 cudaError_t launch_decode_act(const void* x, const void* Wg, const void* Wu, void* a, void* G,
                               void* U, int M, int H, int I, int act, bool gated, float s,
-                              cudaStream_t stream, bool pdl);
+                              cudaStream_t stream, bool pdl, int* status);
 cudaError_t launch_decode_down(const void* a, const void* Wd, void* out, int M, int H, int I,
                                cudaStream_t stream, bool pdl);
 
@@ -184,7 +185,7 @@ cudaError_t launch_decode_down(const void* a, const void* Wd, void* out, int M, 
 constexpr int DECODE_MMA_MAX_M = 16;
 cudaError_t launch_decode_mma_act(const void* x, const void* Wg, const void* Wu, void* a, void* G,
                                   void* U, int M, int H, int I, int act, bool gated, float s,
-                                  cudaStream_t stream, bool pdl);
+                                  cudaStream_t stream, bool pdl, int* status);
 cudaError_t launch_decode_mma_down(const void* a, const void* Wd, void* out, int M, int H, int I,
                                    cudaStream_t stream, bool pdl);
 

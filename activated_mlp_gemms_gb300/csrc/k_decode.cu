@@ -125,9 +125,11 @@ __global__ void __launch_bounds__(DEC_THREADS, dec_ctas<MODE>()) k_decode(
     const __nv_bfloat16* __restrict__ T, const __nv_bfloat16* __restrict__ W0,
     const __nv_bfloat16* __restrict__ W1, __nv_bfloat16* __restrict__ out,
     __nv_bfloat16* __restrict__ o1, __nv_bfloat16* __restrict__ o2, int M, int R, int K, float s,
-    int passes) {
+    int passes, int* status) {
   using G = DecGroup<MODE, MT>;
   constexpr int NMAT = G::NMAT;
+  // the call's status word (the first kernel of the call clears it)
+  if (status != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
   constexpr int RPW = G::RPW;
   extern __shared__ uint4 tok[];  // [MT][K / 8], token rows m >= M as zeros
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -233,7 +235,7 @@ template <int ACT, int MODE, int MT>
 cudaError_t launch_decode_inst(const __nv_bfloat16* T, const __nv_bfloat16* W0,
                                const __nv_bfloat16* W1, __nv_bfloat16* out, __nv_bfloat16* o1,
                                __nv_bfloat16* o2, int M, int R, int K, float s,
-                               cudaStream_t stream, bool pdl) {
+                               cudaStream_t stream, bool pdl, int* status) {
   auto kern = k_decode<ACT, MODE, MT>;
   constexpr int RPW = dec_rpw<MODE, MT>();
   int dev = 0, sms = 148;
@@ -264,13 +266,13 @@ cudaError_t launch_decode_inst(const __nv_bfloat16* T, const __nv_bfloat16* W0,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, T, W0, W1, out, o1, o2, M, R, K, s, passes);
+  return cudaLaunchKernelEx(&cfg, kern, T, W0, W1, out, o1, o2, M, R, K, s, passes, status);
 }
 
 template <int ACT, int MODE>
 cudaError_t launch_decode_mt(const void* T, const void* W0, const void* W1, void* out, void* o1,
                              void* o2, int M, int R, int K, float s, cudaStream_t stream,
-                             bool pdl) {
+                             bool pdl, int* status) {
   auto t = static_cast<const __nv_bfloat16*>(T);
   auto w0 = static_cast<const __nv_bfloat16*>(W0);
   auto w1 = static_cast<const __nv_bfloat16*>(W1);
@@ -278,35 +280,35 @@ cudaError_t launch_decode_mt(const void* T, const void* W0, const void* W1, void
   auto y1 = static_cast<__nv_bfloat16*>(o1);
   auto y2 = static_cast<__nv_bfloat16*>(o2);
   switch (M) {
-    case 1: return launch_decode_inst<ACT, MODE, 1>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl);
-    case 2: return launch_decode_inst<ACT, MODE, 2>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl);
-    case 3: return launch_decode_inst<ACT, MODE, 3>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl);
-    default: return launch_decode_inst<ACT, MODE, 4>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl);
+    case 1: return launch_decode_inst<ACT, MODE, 1>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl, status);
+    case 2: return launch_decode_inst<ACT, MODE, 2>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl, status);
+    case 3: return launch_decode_inst<ACT, MODE, 3>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl, status);
+    default: return launch_decode_inst<ACT, MODE, 4>(t, w0, w1, y, y1, y2, M, R, K, s, stream, pdl, status);
   }
 }
 
 cudaError_t launch_decode_act(const void* x, const void* Wg, const void* Wu, void* a, void* G,
                               void* U, int M, int H, int I, int act, bool gated, float s,
-                              cudaStream_t stream, bool pdl) {
+                              cudaStream_t stream, bool pdl, int* status) {
   if (gated) {
     switch (act) {
-      case ACT_RELU: return launch_decode_mt<ACT_RELU, DEC_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl);
-      case ACT_GELU_TANH: return launch_decode_mt<ACT_GELU_TANH, DEC_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl);
-      case ACT_SIGMOID: return launch_decode_mt<ACT_SIGMOID, DEC_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl);
-      default: return launch_decode_mt<ACT_SILU, DEC_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl);
+      case ACT_RELU: return launch_decode_mt<ACT_RELU, DEC_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl, status);
+      case ACT_GELU_TANH: return launch_decode_mt<ACT_GELU_TANH, DEC_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl, status);
+      case ACT_SIGMOID: return launch_decode_mt<ACT_SIGMOID, DEC_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl, status);
+      default: return launch_decode_mt<ACT_SILU, DEC_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl, status);
     }
   }
   switch (act) {
-    case ACT_RELU: return launch_decode_mt<ACT_RELU, DEC_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl);
-    case ACT_GELU_TANH: return launch_decode_mt<ACT_GELU_TANH, DEC_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl);
-    default: return launch_decode_mt<ACT_RELU_SQ, DEC_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl);
+    case ACT_RELU: return launch_decode_mt<ACT_RELU, DEC_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl, status);
+    case ACT_GELU_TANH: return launch_decode_mt<ACT_GELU_TANH, DEC_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl, status);
+    default: return launch_decode_mt<ACT_RELU_SQ, DEC_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl, status);
   }
 }
 
 cudaError_t launch_decode_down(const void* a, const void* Wd, void* out, int M, int H, int I,
                                cudaStream_t stream, bool pdl) {
   return launch_decode_mt<0, DEC_STORE>(a, Wd, nullptr, out, nullptr, nullptr, M, H, I, 1.f,
-                                        stream, pdl);
+                                        stream, pdl, nullptr);
 }
 
 }  // namespace mlpk

@@ -143,8 +143,11 @@ template <int ACT, int MODE, int NT>
 __global__ void __launch_bounds__(md_max_threads<MODE>()) k_decode_mma(
     const __nv_bfloat16* __restrict__ T, const __nv_bfloat16* __restrict__ W0,
     const __nv_bfloat16* __restrict__ W1, __nv_bfloat16* __restrict__ out,
-    __nv_bfloat16* __restrict__ o1, __nv_bfloat16* __restrict__ o2, int M, int R, int K, float s) {
+    __nv_bfloat16* __restrict__ o1, __nv_bfloat16* __restrict__ o2, int M, int R, int K, float s,
+    int* status) {
   using G = MdGroup<MODE, NT>;
+  // the call's status word (the first kernel of the call clears it)
+  if (status != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
   constexpr int NMAT = G::NMAT, NTB = G::NTB;
   constexpr int DEPTH = 2;  // load groups in flight per warp (deeper: no faster, more registers)
   // the warps' partial sums, [warp][matrix][token block][lane] x 4 floats
@@ -273,7 +276,7 @@ int md_warps(int blocks, int ngroups) {
 
 template <int ACT, int MODE, int NT>
 cudaError_t launch_md(const void* T, const void* W0, const void* W1, void* out, void* o1, void* o2,
-                      int M, int R, int K, float s, cudaStream_t stream, bool pdl) {
+                      int M, int R, int K, float s, cudaStream_t stream, bool pdl, int* status) {
   const int blocks = (R + MD_ROWS - 1) / MD_ROWS;
   const int ngroups = (K + MD_KG - 1) / MD_KG;
   const int warps = md_warps<ACT, MODE, NT>(blocks, ngroups);
@@ -292,34 +295,36 @@ cudaError_t launch_md(const void* T, const void* W0, const void* W1, void* out, 
                             static_cast<const __nv_bfloat16*>(W0),
                             static_cast<const __nv_bfloat16*>(W1), static_cast<__nv_bfloat16*>(out),
                             static_cast<__nv_bfloat16*>(o1), static_cast<__nv_bfloat16*>(o2), M, R,
-                            K, s);
+                            K, s, status);
 }
 
 template <int ACT, int MODE>
 cudaError_t launch_md_nt(const void* T, const void* W0, const void* W1, void* out, void* o1,
-                         void* o2, int M, int R, int K, float s, cudaStream_t stream, bool pdl) {
-  if (M <= 8) return launch_md<ACT, MODE, 8>(T, W0, W1, out, o1, o2, M, R, K, s, stream, pdl);
-  return launch_md<ACT, MODE, 16>(T, W0, W1, out, o1, o2, M, R, K, s, stream, pdl);
+                         void* o2, int M, int R, int K, float s, cudaStream_t stream, bool pdl,
+                         int* status) {
+  if (M <= 8)
+    return launch_md<ACT, MODE, 8>(T, W0, W1, out, o1, o2, M, R, K, s, stream, pdl, status);
+  return launch_md<ACT, MODE, 16>(T, W0, W1, out, o1, o2, M, R, K, s, stream, pdl, status);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_mma_act(const void* x, const void* Wg, const void* Wu, void* a, void* G,
                                   void* U, int M, int H, int I, int act, bool gated, float s,
-                                  cudaStream_t stream, bool pdl) {
+                                  cudaStream_t stream, bool pdl, int* status) {
   if (M < 1 || M > DECODE_MMA_MAX_M) return cudaErrorInvalidValue;
   if (gated) {
     switch (act) {
-      case ACT_RELU: return launch_md_nt<ACT_RELU, MD_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl);
-      case ACT_GELU_TANH: return launch_md_nt<ACT_GELU_TANH, MD_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl);
-      case ACT_SIGMOID: return launch_md_nt<ACT_SIGMOID, MD_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl);
-      default: return launch_md_nt<ACT_SILU, MD_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl);
+      case ACT_RELU: return launch_md_nt<ACT_RELU, MD_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl, status);
+      case ACT_GELU_TANH: return launch_md_nt<ACT_GELU_TANH, MD_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl, status);
+      case ACT_SIGMOID: return launch_md_nt<ACT_SIGMOID, MD_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl, status);
+      default: return launch_md_nt<ACT_SILU, MD_GATED>(x, Wg, Wu, a, G, U, M, I, H, s, stream, pdl, status);
     }
   }
   switch (act) {
-    case ACT_RELU: return launch_md_nt<ACT_RELU, MD_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl);
-    case ACT_GELU_TANH: return launch_md_nt<ACT_GELU_TANH, MD_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl);
-    default: return launch_md_nt<ACT_RELU_SQ, MD_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl);
+    case ACT_RELU: return launch_md_nt<ACT_RELU, MD_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl, status);
+    case ACT_GELU_TANH: return launch_md_nt<ACT_GELU_TANH, MD_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl, status);
+    default: return launch_md_nt<ACT_RELU_SQ, MD_NONGATED>(x, Wg, nullptr, a, G, nullptr, M, I, H, s, stream, pdl, status);
   }
 }
 
@@ -327,7 +332,7 @@ cudaError_t launch_decode_mma_down(const void* a, const void* Wd, void* out, int
                                    cudaStream_t stream, bool pdl) {
   if (M < 1 || M > DECODE_MMA_MAX_M) return cudaErrorInvalidValue;
   return launch_md_nt<0, MD_STORE>(a, Wd, nullptr, out, nullptr, nullptr, M, H, I, 1.f, stream,
-                                   pdl);
+                                   pdl, nullptr);
 }
 
 }  // namespace mlpk

@@ -317,7 +317,7 @@ struct Call {
   int next_counter = 0;
   int launches = 0;
   int* counter() { return counters + (next_counter++ % MAX_COUNTERS); }
-  bool pdl() { return launches++ > 0; }  // the first kernel follows the control-block memset
+  bool pdl() { return launches++ > 0; }  // the first kernel follows the memset or the caller's work
 };
 
 int cuda_err(cudaError_t e) { return e == cudaSuccess ? MLP_OK : MLP_ERR_CUDA; }
@@ -611,11 +611,14 @@ int wgrad_split(int M, long long tiles, int cg, int fuse) {
   return ksplit;
 }
 
-int begin_call(Call& c, void* ws, void* stream) {
+// clear = false: the call's first kernel clears the status word itself (the
+// decode weight streams, which use no counter of the control block), so the
+// call enqueues no memset.
+int begin_call(Call& c, void* ws, void* stream, bool clear = true) {
   c.stream = static_cast<cudaStream_t>(stream);
   c.status = static_cast<int*>(ws);
   c.counters = static_cast<int*>(ws) + COUNTER_BASE;
-  return cuda_err(cudaMemsetAsync(ws, 0, CTRL_BYTES, c.stream));
+  return clear ? cuda_err(cudaMemsetAsync(ws, 0, CTRL_BYTES, c.stream)) : MLP_OK;
 }
 
 // The MLP block's neighbours (mlp_block_fwd / mlp_block_bwd); nullptr for
@@ -776,20 +779,22 @@ int forward(const mlp_problem_t* p, const void* x, const void* Wg, const void* W
   MLP_TRY(opt(U_save));
   if (!gated(p) && U_save) return MLP_ERR_INVALID_ARG;
   MLP_TRY(check_ws(p, mode, ws, ws_bytes));
-  Call c;
-  MLP_TRY(begin_call(c, ws, stream));
-  void* a = static_cast<char*>(ws) + CTRL_BYTES;
   const int dk = blk ? 0 : decode_kernel(p);
+  Call c;
+  MLP_TRY(begin_call(c, ws, stream, dk == 0));
+  void* a = static_cast<char*>(ws) + CTRL_BYTES;
   if (dk != 0) {
-    // a few tokens: two weight-streaming passes (warp-level MMA, or CUDA cores)
+    // a few tokens: two weight-streaming passes (warp-level MMA, or CUDA
+    // cores); the first, launched after everything before it on the stream,
+    // clears the status word in place of the control block's memset
     const bool pdl0 = c.pdl();
     MLP_TRY(traced(MLP_KERNEL_GATE_UP, c.stream, [&] {
       return dk == 2 ? launch_decode_mma_act(x, Wg, Wu, a, G_save, U_save, p->M, p->H, p->I,
                                              device_act(p->act), gated(p),
-                                             p->gate_mult * p->down_mult, c.stream, pdl0)
+                                             p->gate_mult * p->down_mult, c.stream, pdl0, c.status)
                      : launch_decode_act(x, Wg, Wu, a, G_save, U_save, p->M, p->H, p->I,
                                          device_act(p->act), gated(p),
-                                         p->gate_mult * p->down_mult, c.stream, pdl0);
+                                         p->gate_mult * p->down_mult, c.stream, pdl0, c.status);
     }));
     const bool pdl1 = c.pdl();
     return traced(MLP_KERNEL_DOWN, c.stream, [&] {
