@@ -1,4 +1,7 @@
-// Decode-sized forward (one to four tokens) on the CUDA cores.
+// Decode-sized forward (one to four tokens) on the CUDA cores.  The
+// library takes it for one or two tokens, where it streams the weights a
+// few per cent faster than the warp-MMA stream (k_decode_mma.cu); from three
+// tokens on its fused multiply-adds outrun the instruction issue.
 //
 // With a few tokens every weight element is used a few times: the forward
 // is a weight stream, bound by HBM.  The tensor-core path reads its
