@@ -134,6 +134,12 @@ struct EpiWarp {
   bool rows_ok;  // any of the 32 rows inside the output
   uint32_t box;  // EPI_DACT_RECOMP: which of the two boxes the next chunk fills
   float rs;      // this lane's row scale (the block's RMS norm; 1 without it)
+  // EPI_DGRAD_F8 with TMA-loaded preact boxes: the two halves of the staging
+  // box each have a barrier (ebar, ebar + 8); ephase holds their parities,
+  // epend the halves with a load in flight (bit per half)
+  uint32_t ebar;
+  uint32_t ephase;
+  uint32_t epend;
 };
 
 // Stage this lane's 32 bf16 (16 packed words) into a 64B-swizzled 32x32 box.
@@ -169,6 +175,7 @@ struct EpiUnit {
   float mult;                 // ... the problem's multiplier
   float inv;                  // ... fp32(1 / *sq), the 8-bit output's quantisation factor
   float* amax;                // running max of the 8-bit epilogue's output
+  const CUtensorMap* ein;     // EPI_DGRAD_F8: in0's 32 x 32 boxes for TMA loads (nullptr: none)
 };
 
 // deq, inv: the 8-bit epilogues' factors of this problem (read once per kernel)
@@ -189,6 +196,7 @@ __device__ __forceinline__ EpiUnit epi_unit(const Params& p, const Prob& P, floa
   U.mult = 1.f;
   U.inv = 1.f;
   U.amax = nullptr;
+  U.ein = P.mapE >= 0 ? &p.maps[P.mapE] : nullptr;
   U.deq0 = 1.f;
   if constexpr (is_f8(EPI)) {
     U.deq = deq;
@@ -626,6 +634,113 @@ __device__ __forceinline__ void epi_dgrad_f8(const Params& p, const EpiUnit& P, 
   }
 }
 
+// EPI_DGRAD_F8 with the saved preact loaded by TMA (P.ein).  Loading P row
+// by row (each lane its own row's 64 bytes a chunk) costs a warp 32 L1
+// wavefronts per 16-byte load and was the largest part of this epilogue.
+// Instead the warp's 4 KB staging box serves as two 2 KB buffers, X (stg)
+// and Y (stg + 2048), that take P's 32 x 32 bf16 boxes (64-byte swizzle):
+// chunks 0 and 2 in X, 1 and 3 in Y, each with its own barrier.  The e5m2
+// codes of a chunk stay in registers (8 a lane) until the tile's last chunk
+// is done; the box then stages them for the one TMA store per tile.
+//
+// dgrad_f8_issue: the loads of chunks 0 and 1 of a tile, issued before the
+// wait for the accumulator (the previous tile's store must have read the
+// box first).
+__device__ __forceinline__ void dgrad_f8_issue(const EpiUnit& P, EpiWarp& e, int col, int half,
+                                               uint64_t pol) {
+  if (col >= P.N) return;  // warp-uniform
+  e.epend |= 1u << half;
+  if (e.lane == 0) {
+    const uint32_t bar = e.ebar + 8u * static_cast<uint32_t>(half);
+    mbar_expect_tx(bar, 2048);
+    tma_load_2d(e.stg + 2048u * static_cast<uint32_t>(half), P.ein, col, e.row0, bar, pol);
+  }
+}
+
+// After an expired wait: let the loads still in flight land (bounded)
+// before the kernel unwinds and its shared memory is released.
+__device__ __forceinline__ void dgrad_f8_drain(EpiWarp& e) {
+  volatile int never = 0;
+#pragma unroll
+  for (uint32_t h = 0; h < 2; ++h) {
+    if (e.epend & (1u << h)) {
+      mbar_wait(e.ebar + 8u * h, (e.ephase >> h) & 1u, 10000000ull, &never);
+      e.ephase ^= 1u << h;
+    }
+  }
+  e.epend = 0;
+}
+
+// The tile's epilogue; false when a bounded wait expired (loads drained).
+__device__ __forceinline__ bool epi_dgrad_f8_tma(const EpiUnit& P, EpiWarp& e, uint32_t tb,
+                                                 int col0, int cb, uint64_t lim,
+                                                 volatile int* abort_flag, uint64_t pol) {
+  const float dq2 = 2.f * P.mult * P.deq;
+  const float inv = P.inv;
+  const int row = e.row0 + e.lane;
+  const uint32_t rb = static_cast<uint32_t>(e.lane) * 64u;
+  const uint32_t x = (static_cast<uint32_t>(e.lane) >> 1) & 3u;
+  uint32_t qq[4][8];
+  float mx = 0.f;
+  int nch = 0;
+#pragma unroll
+  for (int ci = 0; ci < 4; ++ci) {
+    const int col = col0 + cb + 32 * ci;
+    if (col >= P.N) break;  // warp-uniform
+    const uint32_t h = static_cast<uint32_t>(ci & 1);
+    const uint32_t buf = e.stg + 2048u * h;
+    if (!mbar_wait(e.ebar + 8u * h, (e.ephase >> h) & 1u, lim, abort_flag)) {
+      dgrad_f8_drain(e);
+      return false;
+    }
+    e.ephase ^= 1u << h;
+    e.epend &= ~(1u << h);
+    // this lane's row of the chunk (16-byte unit u sits at u ^ ((r / 2) % 4))
+    uint4 pv[4];
+#pragma unroll
+    for (uint32_t v = 0; v < 4; ++v) pv[v] = ld_shared_v4(buf + rb + ((v ^ x) << 4));
+    uint32_t z[32];
+    __syncwarp();
+    tmem_ld32(tb + cb + 32 * ci, z);
+    tmem_wait_ld();
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint32_t gw[4] = {pv[v].x, pv[v].y, pv[v].z, pv[v].w};
+      qq[ci][2 * v] = 0;
+      qq[ci][2 * v + 1] = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 pp = unpack_bf16x2(gw[j]);
+        const float d0 = dq2 * __uint_as_float(z[8 * v + 2 * j]) * fmaxf(pp.x, 0.f);
+        const float d1 = dq2 * __uint_as_float(z[8 * v + 2 * j + 1]) * fmaxf(pp.y, 0.f);
+        mx = fmaxf(mx, fmaxf(fabsf(d0), fabsf(d1)));
+        qq[ci][2 * v + (j >> 1)] |= static_cast<uint32_t>(pack_e5m2x2(d0 * inv, d1 * inv))
+                                    << (16 * (j & 1));
+      }
+    }
+    nch = ci + 1;
+    // every lane has used its row of the buffer (the codes above depend on
+    // it): chunk ci + 2 may go there
+    __syncwarp();
+    if (ci < 2) {
+      if (e.lane == 0) fence_proxy_async_smem();
+      dgrad_f8_issue(P, e, col + 64, static_cast<int>(h), pol);
+    }
+  }
+  // every load issued for this tile has been waited for: the box is free
+#pragma unroll
+  for (int ci = 0; ci < 4; ++ci)
+    if (ci < nch) stage_f8_chunk(e.stg, e.lane, ci, qq[ci]);
+  if (nch > 0) store_f8_tile(P, e, 0, e.stg, col0 + cb);
+  if (P.amax) {
+    if (row >= P.M) mx = 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (e.lane == 0 && mx > 0.f) atomicMax(reinterpret_cast<int*>(P.amax), __float_as_int(mx));
+  }
+  return true;
+}
+
 // EPI_DGRAD_F8_RECOMP, phase 1 on accumulator 0 (x8 W1_8^T): this thread's
 // 128 values of dd = 2 relu(deq0 * acc) as packed bf16 pairs (the saved-
 // preact path's 2 relu(bf16(pre)): doubling and relu commute with the
@@ -916,7 +1031,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
   constexpr int FULL = 0, EMPTY = C::STAGES, TFULL = 2 * C::STAGES, TEMPTY = 2 * C::STAGES + 2,
                 SFULL = 2 * C::STAGES + 4, SEMPTY = 2 * C::STAGES + 4 + SCHED_SLOTS,
                 DRAIN = 2 * C::STAGES + 4 + 2 * SCHED_SLOTS;
-  constexpr int NBAR = DRAIN + 1;
+  // EPI_DGRAD_F8: two barriers per epilogue warp for its TMA-loaded preact boxes
+  constexpr int EBAR = DRAIN + 1;
+  constexpr int NBAR = EBAR + 2 * NUM_EPI_WARPS;
   int* sched = reinterpret_cast<int*>(ctrl + 8 * NBAR);
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sched + SCHED_SLOTS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
@@ -945,6 +1062,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
       mbar_init(bar_s(SEMPTY + i), 1 + CG * NUM_EPI_WARPS + (CG - 1));
     }
     mbar_init(bar_s(DRAIN), 1);
+    if constexpr (EPI == EPI_DGRAD_F8)
+      for (int i = 0; i < 2 * NUM_EPI_WARPS; ++i) mbar_init(bar_s(EBAR + i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1236,6 +1355,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
     e.stg = stg_s + static_cast<uint32_t>(warp - 2) * EpiTraits<EPI>::STG_WARP;
     e.lane = lane;
     e.box = 0;
+    e.ebar = bar_s(EBAR + 2 * (warp - 2));
+    e.ephase = 0;
+    e.epend = 0;
+    const uint64_t epol = policy_evict_normal();  // the epilogue's TMA loads
     int slot = 0;
     uint32_t sphase = 0;
     int acc = 0;
@@ -1307,11 +1430,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
         if (acc == 0) aphase ^= 1u;
       }
       if constexpr (EpiTraits<EPI>::DACT) {
-        // the saved preacts do not depend on the MMAs: fetch the first chunk now
-        if (e.rows_ok) dact_load<EPI == EPI_DGATED>(P, e.row0 + lane, col0 + cb, pg, pu);
+        // the saved preacts do not depend on the MMAs: fetch the first chunk(s) now
+        if (EPI == EPI_DGRAD_F8 && P.ein != nullptr) {
+          if (e.rows_ok) {
+            staging_acquire(e);  // the previous tile's store has read the box
+            dgrad_f8_issue(P, e, col0 + cb, 0, epol);
+            dgrad_f8_issue(P, e, col0 + cb + 32, 1, epol);
+          }
+        } else if (e.rows_ok) {
+          dact_load<EPI == EPI_DGATED>(P, e.row0 + lane, col0 + cb, pg, pu);
+        }
       }
       if (!mbar_wait<PAIR>(bar_s(TFULL + acc), aphase, lim, abort_flag)) {
         record_timeout(p, abort_flag);
+        if constexpr (EPI == EPI_DGRAD_F8) dgrad_f8_drain(e);
         break;
       }
       tc_fence_after();
@@ -1333,7 +1465,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
         } else if constexpr (EPI == EPI_ACT_FWD_F8) {
           epi_act_f8<ACT>(p, P, e, tb, col0, cb, ce);
         } else if constexpr (EPI == EPI_DGRAD_F8) {
-          epi_dgrad_f8(p, P, e, tb, col0, cb, ce, pg);
+          if (P.ein == nullptr) {
+            epi_dgrad_f8(p, P, e, tb, col0, cb, ce, pg);
+          } else if (!epi_dgrad_f8_tma(P, e, tb, col0, cb, lim, abort_flag, epol)) {
+            record_timeout(p, abort_flag);
+            break;
+          }
         } else if constexpr (EPI == EPI_DGRAD_F8_RECOMP) {
           epi_recomp_f8_dh(P, e, tb, col0, cb, dd);
         } else {

@@ -83,6 +83,8 @@ struct Prob {
   int ld;                 // row pitch (elements) of the epilogue's outputs and inputs
   int mapI0, mapI1;       // derivative epilogues: maps of in0 / in1 with boxes {256, 128}
                           // whose tiles the producer prefetches into L2 (-1: none)
+  int mapE;               // EPI_DGRAD_F8: map of in0 with the epilogue warps' 32 x 32 bf16
+                          // boxes (64-byte swizzle), loaded by TMA (-1: plain loads)
   int mapO[3];            // tensor maps of the epilogue's outputs (-1: output not written)
   void* out0;
   void* out1;

@@ -304,6 +304,7 @@ struct Gemm {
     P.ld = N;
     P.mapO[0] = P.mapO[1] = P.mapO[2] = -1;
     P.mapI0 = P.mapI1 = -1;
+    P.mapE = -1;
     return P;
   }
   // B rows per K-major box: a CTA stages 256 / cg of the 256 B rows
@@ -1188,12 +1189,14 @@ int mlp_fp8_bwd(const mlp_problem_t* p, const void* dout, const void* x8, const 
     const int mB = g.mnmajor_u8(W2_8, H, I);
     const int oP = g.output_u8(dP8, M, I);
     const int iP = g.prefetch_map(pre, M, I);
+    const int eP = g.output(const_cast<void*>(pre), M, I);  // the epilogue's preact boxes
     Prob& P = g.add(M, I, H, 0, MMA_N, 1, 2 * BK);
     P.mapA0 = mA;
     P.mapB0 = mB;
     P.mapO[0] = oP;
     P.in0 = pre;
     P.mapI0 = iP;
+    P.mapE = eP;
     P.sa = scales + 4;  // sg
     P.sb = scales + 2;  // s2
     P.sq = scales + 5;  // s_dpre
