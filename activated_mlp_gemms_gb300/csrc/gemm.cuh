@@ -930,6 +930,7 @@ struct UnitLoads {
   const CUtensorMap* i0;  // nullptr: none
   const CUtensorMap* i1;
   int icol;               // the tile's first column
+  int l2a, l2b;           // the operands' L2 policies (Prob::l2a, l2b)
 };
 
 template <int EPI, int CG>
@@ -940,6 +941,8 @@ __device__ __forceinline__ UnitLoads unit_loads(const Params& p, const Prob& P, 
   L.a1 = &p.maps[P.mapA1];
   L.m0 = w.tm * (BM * CG) + static_cast<int>(rank) * BM;
   L.kb0 = P.kb0;
+  L.l2a = P.l2a;
+  L.l2b = P.l2b;
   if (gated_unit<EPI>(w.prob)) {
     // CG=1: both weights' rows; CG=2: the leader stages the gate rows, the peer the up rows
     L.b0 = &p.maps[(CG == 2 && rank != 0) ? P.mapB1 : P.mapB0];
@@ -974,7 +977,9 @@ __device__ __forceinline__ UnitLoads unit_loads(const Params& p, const Prob& P, 
 //   B MN-major (Wd, W2_8).
 template <int EPI, bool A_MN, bool B_MN, int CG>
 __device__ __forceinline__ void load_stage(const UnitLoads& L, int seg, int kc, uint32_t sA,
-                                           uint32_t sB, uint32_t full, uint64_t pol) {
+                                           uint32_t sB, uint32_t full, uint64_t polA,
+                                           uint64_t polB) {
+  uint64_t pol = polA;
   auto ld = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
     if constexpr (CG == 2) tma_load_2d_pair(dst, m, c0, c1, full, pol);
     else tma_load_2d(dst, m, c0, c1, full, pol);
@@ -988,6 +993,7 @@ __device__ __forceinline__ void load_stage(const UnitLoads& L, int seg, int kc, 
     ld(sA, mA, L.m0, kc);
     ld(sA + 8192, mA, L.m0 + 64, kc);
   }
+  pol = polB;
   if constexpr (EPI == EPI_GATED_FWD) {
     ld(sB, L.b0, kc, L.n0);
     if constexpr (CG == 1) ld(sB + 16384, L.b1, kc, L.n0);
@@ -1103,7 +1109,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_normal();
+      const uint64_t pol_n = policy_evict_normal(), pol_l = policy_evict_last(),
+                     pol_f = policy_evict_first();
+      auto pol_of = [&](int k) { return k == 1 ? pol_l : (k == 2 ? pol_f : pol_n); };
       const uint32_t tx_bytes = CG * (p.a_tx_bytes + C::B_BYTES);
       int stage = 0;
       uint32_t phase = 0;
@@ -1182,7 +1190,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
             const int seg = kb < L.kb0 ? 0 : 1;
             const int kc = (seg == 0 ? kb : kb - L.kb0) * KE;
             const uint32_t sA = base_s + stage * C::STAGE;
-            load_stage<EPI, A_MN, B_MN, CG>(L, seg, kc, sA, sA + C::A_BYTES, full, pol);
+            load_stage<EPI, A_MN, B_MN, CG>(L, seg, kc, sA, sA + C::A_BYTES, full,
+                                            pol_of(L.l2a), pol_of(L.l2b));
             ++issued;
             if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
             if (!published && kb == w.kb_begin + (w.kb_end - w.kb_begin) / 2) {
@@ -1231,7 +1240,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
             const int kc = (seg == 0 ? kb : kb - L.kb0) * KE;
             const uint32_t sA = base_s + stage * C::STAGE;
             load_stage<EPI, A_MN, B_MN, CG>(L, seg, kc, sA, sA + C::A_BYTES,
-                                            full_lead + 8u * stage, pol);
+                                            full_lead + 8u * stage, pol_of(L.l2a),
+                                            pol_of(L.l2b));
             ++issued;
             if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
           }

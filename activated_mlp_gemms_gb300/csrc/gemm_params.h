@@ -17,6 +17,12 @@ constexpr int NUM_EPI_WARPS = 8;                // two per TMEM lane quadrant (c
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;  // producer, MMA, epilogue warps
 constexpr int TMEM_COLS = 512;                  // two 256-column accumulators
 constexpr int MAX_PROBS = 3;
+
+// L2 cache policies of the operand loads (Prob::l2a, l2b).  The launches
+// mark the operand that many tiles re-read evict-last and, where the other
+// streams past once per tile column, that one evict-first: same-call A/B on
+// the bf16 training steps, 2.3-3.0 % faster (SwiGLU shapes), 0.6 % (ReLU^2).
+enum L2Policy : int { L2_NORMAL = 0, L2_EVICT_LAST = 1, L2_EVICT_FIRST = 2 };
 constexpr int MAX_MAPS = 12;
 
 // What the epilogue does with the accumulator tile.
@@ -96,6 +102,7 @@ struct Prob {
                           // dG, dU / dP (derivative epilogues) are multiplied by rstd[row]
   float alpha;            // EPI_STORE_BF16 with in0 = residual [M, ld]: D = alpha*in0 + acc
   int group_m;            // L2 raster group of this problem (0: Params::group_m)
+  int l2a, l2b;           // L2 policy of the A / B operand loads (L2Policy)
   // 8-bit epilogues: dequant factor mult * *sa * *sb; *sq the scale of an 8-bit output
   const float* sa;
   const float* sb;

@@ -305,6 +305,7 @@ struct Gemm {
     P.mapO[0] = P.mapO[1] = P.mapO[2] = -1;
     P.mapI0 = P.mapI1 = -1;
     P.mapE = -1;
+    P.l2a = P.l2b = 0;
     return P;
   }
   // B rows per K-major box: a CTA stages 256 / cg of the 256 B rows
@@ -631,6 +632,7 @@ struct Block {
   const float* rstd;  // the per-token scale the GEMM epilogues apply
 };
 
+
 // gate/up (or fc1) GEMM with the activation epilogue.
 //   a_out: postact (may be null), G_out/U_out: preact stores (may be null)
 //   rstd: per-row scale of the accumulators (the block's RMS norm; may be null)
@@ -645,6 +647,8 @@ int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* W
     const int oG = g.output(G_out, p->M, p->I);
     const int oU = g.output(U_out, p->M, p->I);
     Prob& P = g.add(p->M, p->I, p->H, 0, 128);
+    P.l2a = L2_EVICT_LAST;   // x: every tile column re-reads it
+    P.l2b = L2_EVICT_FIRST;  // the weights: a panel's reuse is by consecutive row tiles
     P.mapA0 = mA;
     P.mapB0 = mG;
     P.mapB1 = mU;
@@ -750,6 +754,7 @@ int launch_fwd_fused(const mlp_problem_t* p, Call& c, const void* x, const void*
   const int mD = g.kmajor(Wd, p->H, p->I, g.b_rows());
   const int oO = g.output(out, p->M, p->H);
   Prob& P0 = g.add(p->M, p->I, p->H, 0, 128);
+  P0.l2b = L2_EVICT_LAST;  // Wg, Wu: walked again by every group of 16 row tiles
   P0.mapA0 = mX;
   P0.mapB0 = mG;
   P0.mapB1 = mU;
@@ -885,6 +890,7 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     // (no L2 prefetch of G/U here: with the long K of these GEMMs the
     // epilogue keeps up, and the prefetch made the kernel 5-7 % slower)
     Prob& P = g.add(M, I, H, 0, MMA_N);
+    P.l2a = L2_EVICT_LAST;  // dout: re-read by every tile column
     P.mapA0 = mA;
     P.mapB0 = mB;
     P.in0 = G;
@@ -938,6 +944,8 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
     }
     const int oX = dx_split > 1 ? g.output(part, M, H, true) : g.output(dx, M, H);
     Prob& P = g.add(M, H, I, gated(p) ? I : 0, MMA_N, dx_split);
+    P.l2a = L2_EVICT_LAST;   // dG, dU: re-read by every tile column
+    P.l2b = L2_EVICT_FIRST;  // Wg, Wu
     P.mapA0 = mA0;
     P.mapB0 = mB0;
     P.mapA1 = mA1;
@@ -982,6 +990,7 @@ int backward(const mlp_problem_t* p, const void* dout, const void* x, const void
       const int mB = g.mnmajor(list[i].B, M, list[i].cols);
       const int oW = g.output(list[i].out, list[i].rows, list[i].cols, fuse != 0);
       Prob& P = g.add(list[i].rows, list[i].cols, M, 0, MMA_N, ksplit);
+      P.l2b = L2_EVICT_LAST;  // x, or the postact: shared by the three problems' tile rows
       P.mapA0 = mA;
       P.mapB0 = mB;
       P.mapO[0] = oW;
