@@ -633,6 +633,7 @@ struct Block {
 };
 
 
+
 // gate/up (or fc1) GEMM with the activation epilogue.
 //   a_out: postact (may be null), G_out/U_out: preact stores (may be null)
 //   rstd: per-row scale of the accumulators (the block's RMS norm; may be null)
@@ -662,6 +663,7 @@ int launch_fwd_act(const mlp_problem_t* p, Call& c, const void* x, const void* W
   const int oA = g.output(a_out, p->M, p->I);
   const int oP = g.output(G_out, p->M, p->I);
   Prob& P = g.add(p->M, p->I, p->H, 0, MMA_N);
+  P.l2b = L2_EVICT_LAST;  // W1: walked again by every group of row tiles
   P.mapA0 = mA;
   P.mapB0 = mW;
   P.mapO[0] = oA;
@@ -684,6 +686,7 @@ int launch_dact_recomp(const mlp_problem_t* p, Call& c, const void* x, const voi
   const int oP = g.output(dP, p->M, p->I);
   const int oA = g.output(a_out, p->M, p->I);
   Prob& P = g.add(p->M, p->I, p->H, p->H, MMA_N);
+  P.l2b = L2_EVICT_LAST;  // W1 and Wd: walked again by every group of row tiles
   P.mapA0 = mA0;
   P.mapB0 = mB0;
   P.mapA1 = mA1;
@@ -712,6 +715,8 @@ int launch_down(const mlp_problem_t* p, Call& c, const void* a, const void* Wd, 
   if (split > 1) {
     const int oP = g.output(part, p->M, p->H, true);
     Prob& P = g.add(p->M, p->H, p->I, 0, MMA_N, split);
+    P.l2a = L2_EVICT_LAST;   // the postact: re-read by every tile column
+    P.l2b = L2_EVICT_FIRST;  // Wd
     P.mapA0 = mA;
     P.mapB0 = mB;
     P.mapO[0] = oP;
@@ -720,6 +725,8 @@ int launch_down(const mlp_problem_t* p, Call& c, const void* a, const void* Wd, 
   }
   const int oO = g.output(out, p->M, p->H);
   Prob& P = g.add(p->M, p->H, p->I, 0, MMA_N);
+  P.l2a = L2_EVICT_LAST;   // the postact: re-read by every tile column
+  P.l2b = L2_EVICT_FIRST;  // Wd
   P.mapA0 = mA;
   P.mapB0 = mB;
   P.mapO[0] = oO;
