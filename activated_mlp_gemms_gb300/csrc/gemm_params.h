@@ -192,6 +192,10 @@ cudaError_t launch_decode_down(const void* a, const void* Wd, void* out, int M, 
 // m16n8k16 (bf16 in, fp32 accumulate) fed straight from 16-byte loads; the
 // token rows are read through the caches, so K is not limited.
 constexpr int DECODE_MMA_MAX_M = 16;
+// Tokens up to which the library takes the warp-MMA stream by itself: with
+// 9-16 tokens (two 8-token blocks) the tensor-core GEMMs measured faster
+// (73-75 against 81-83 us on Llama-3-8B's weights)
+constexpr int DECODE_MMA_AUTO_M = 8;
 cudaError_t launch_decode_mma_act(const void* x, const void* Wg, const void* Wu, void* a, void* G,
                                   void* U, int M, int H, int I, int act, bool gated, float s,
                                   cudaStream_t stream, bool pdl, int* status);

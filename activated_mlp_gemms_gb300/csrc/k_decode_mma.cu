@@ -1,6 +1,8 @@
 // Decode-sized forward (up to sixteen tokens): a weight stream whose dot
 // products run on the warp-level MMA (mma.sync m16n8k16, bf16 in, fp32
-// accumulate).
+// accumulate).  The library takes it for three to eight tokens; with 9-16
+// (two 8-token blocks, twice the token loads) the tensor-core GEMMs are
+// faster, and the 16-token instances run only when a test forces them.
 //
 // With M <= 16 tokens the forward reads every weight once and does M
 // multiply-adds per weight element, so it is bound by HBM, not by any

@@ -177,9 +177,10 @@ std::atomic<int> g_tile_policy{0};
 // tile policy forces the tensor-core GEMMs): 1, the CUDA-core stream, for
 // one or two tokens whose rows fit a CTA's shared memory (measured 3-6 %
 // faster than the warp-MMA stream there); 2, the warp-MMA stream, for the
-// others up to DECODE_MMA_MAX_M tokens; 0, the tensor-core GEMMs.  The
+// others up to DECODE_MMA_AUTO_M tokens; 0, the tensor-core GEMMs.  The
 // testing flags force one stream: MLP_DEBUG_DECODE_FMA the CUDA-core one
-// (up to four tokens that fit), MLP_DEBUG_DECODE_MMA the warp-MMA one.
+// (up to four tokens that fit), MLP_DEBUG_DECODE_MMA the warp-MMA one (up to
+// DECODE_MMA_MAX_M tokens).
 int decode_kernel(const mlp_problem_t* p) {
   const int pol = g_tile_policy.load();
   if ((pol != 0 && pol != 3) || p->M > DECODE_MMA_MAX_M) return 0;
@@ -188,7 +189,7 @@ int decode_kernel(const mlp_problem_t* p) {
   const long long k = p->H > p->I ? p->H : p->I;
   const bool fma_fits = p->M <= DECODE_MAX_M && (long long)p->M * k * 2 <= DECODE_MAX_TOKEN_BYTES;
   if (fma_fits && (p->M <= 2 || (flags & MLP_DEBUG_DECODE_FMA))) return 1;
-  return 2;
+  return p->M <= DECODE_MMA_AUTO_M ? 2 : 0;
 }
 
 // CTA-group size for a GEMM whose output has `rows` rows: pairs (256-row

@@ -139,15 +139,15 @@ size_t mlp_workspace_size(const mlp_problem_t* p, int mode);
  *   U_save bf16 [M,I]  out, optional: the up preact x Wu^T (NULL when non-gated)
  * Pass G_save/U_save as NULL for the recompute mode (save only x).  The
  * bf16 values written to `out` are bitwise identical to mlp_fwd_infer's.
- * With one to sixteen tokens (decode), unless a tile policy is set (below),
+ * With one to eight tokens (decode), unless a tile policy is set (below),
  * the forward streams the weights instead of running tensor-core GEMM
- * tiles (two kernels, no split-K region used): with three to sixteen
- * tokens each CTA owns 16 weight rows, its warps read them in 128-byte
- * pieces per row and accumulate the M dot products with the warp-level MMA
- * (mma.sync, bf16 in, fp32 accumulate) straight from the loaded registers;
- * with one or two tokens (M * max(H, I) * 2 <= 112 KiB) each warp reads
- * whole weight rows front to back and accumulates with fp32 fused
- * multiply-adds on the CUDA cores. */
+ * tiles (two kernels, no split-K region used): with three to eight tokens
+ * each CTA owns 16 weight rows, its warps read them in 128-byte pieces per
+ * row and accumulate the M dot products with the warp-level MMA (mma.sync,
+ * bf16 in, fp32 accumulate) straight from the loaded registers; with one or
+ * two tokens (M * max(H, I) * 2 <= 112 KiB) each warp reads whole weight
+ * rows front to back and accumulates with fp32 fused multiply-adds on the
+ * CUDA cores.  From nine tokens on, the tensor-core GEMMs with split-K. */
 int mlp_fwd(const mlp_problem_t* p, const void* x, const void* Wg, const void* Wu,
             const void* Wd, void* out, void* G_save, void* U_save,
             void* ws, size_t ws_bytes, void* stream);
@@ -375,8 +375,8 @@ int mlp_noalloc_status(void* stream);
  * with every gradient requested (the backward modes) and the current tile
  * policy.  The split-K factors depend on the device's SM count. */
 typedef struct {
-  int decode;           /* the forward streams the weights (1-16 tokens): 2 with the warp-level
-                           MMA, 1 on the CUDA cores; 0: GEMM tiles */
+  int decode;           /* the forward streams the weights (1-8 tokens; up to 16 when forced):
+                           2 with the warp-level MMA, 1 on the CUDA cores; 0: GEMM tiles */
   int fused_forward;    /* 1: the gated forward's gate/up and down GEMMs are one launch */
   int cta_group;        /* CTA-group size (1 or 2) of the GEMMs over token rows */
   int out_split;        /* split-K factor of the [M,H] output GEMM (down projection, or dx) */
@@ -395,7 +395,7 @@ int mlp_plan(const mlp_problem_t* p, int mode, int fuse_grad_accum, mlp_plan_t* 
  * 1 = always single-CTA tiles;  2 = always CTA-pair tiles;
  * 3 = as 0, but the gated forward's gate/up and down GEMMs run as two
  *     launches (policy 0 runs them as one; see MLP_KERNEL_FWD_FUSED).
- * Policies 1 and 2 also keep forwards of one to sixteen tokens on the
+ * Policies 1 and 2 also keep forwards of one to eight tokens on the
  * tensor-core GEMMs (policies 0 and 3 stream their weights, above).
  * Process-wide; returns MLP_ERR_INVALID_ARG for other values.  Results of
  * the two tile shapes agree to rounding (same fp32 accumulation order). */

@@ -2,9 +2,10 @@
 streams the weights instead of running GEMM tiles, against the fp64 oracle,
 through the C ABI.
 
-Two weight streams: the warp-MMA one (three to sixteen tokens by default)
-and the CUDA-core one (one or two tokens by default, up to four whose rows
-fit shared memory when forced); the debug flags force either.  The same guard bands and NaN-filled outputs as the
+Two weight streams: the warp-MMA one (three to eight tokens by default, up
+to sixteen when forced) and the CUDA-core one (one or two tokens by default,
+up to four whose rows fit shared memory when forced); the debug flags force
+either.  From nine tokens on the library takes the tensor-core GEMMs.  The same guard bands and NaN-filled outputs as the
 other parity tests; the training forward's saved preacts (G, U) come from
 the same kernels."""
 import contextlib
@@ -37,13 +38,13 @@ ACTS = ["swiglu", "relu_sq", "gelu_tanh_approx", "relu", "reglu", "geglu", "glu"
 
 @pytest.mark.parametrize("act", ACTS)
 @pytest.mark.parametrize("M,kind", [(1, "mma"), (2, "mma"), (3, "mma"), (4, "mma"), (5, "mma"),
-                                    (8, "mma"), (9, "mma"), (16, "mma"), (17, "tc"),
+                                    (8, "mma"), (9, "mma"), (16, "mma"), (9, "tc"), (17, "tc"),
                                     (1, "fma"), (2, "fma"), (3, "fma"), (4, "fma")])
 def test_decode_forward_parity(act, M, kind):
     """K = 1000 (a ragged last load group), I = 1544 rows (a ragged last
     16-row block; the down pass: K = 1544, 1000 rows); the forward saves
-    G/U, the backward then runs on the tensor cores from them.  M = 17
-    takes the tensor-core GEMMs."""
+    G/U, the backward then runs on the tensor cores from them.  Without a
+    flag M = 9 and M = 17 take the tensor-core GEMMs."""
     H, I = 1000, 1544
     t = make_inputs(M, H, I, act, seed=31)
     with decode_kernel(kind):
@@ -121,11 +122,12 @@ def test_decode_path_is_two_kernels_and_graph_capturable(M, kind):
 
 @pytest.mark.parametrize("M,I,plan", [(1, 14336, PLAN_FMA), (2, 14336, PLAN_FMA),
                                       (2, 32768, PLAN_MMA), (3, 14336, PLAN_MMA),
-                                      (16, 14336, PLAN_MMA), (17, 14336, PLAN_TC)])
+                                      (8, 14336, PLAN_MMA), (9, 14336, PLAN_TC),
+                                      (16, 14336, PLAN_TC), (17, 14336, PLAN_TC)])
 def test_default_decode_stream(M, I, plan):
     """Without a flag: the CUDA-core stream for one or two tokens whose rows
-    fit shared memory, the warp-MMA one for the others up to sixteen, then
-    the tensor-core GEMMs; a tile policy keeps every size on the GEMMs."""
+    fit shared memory, the warp-MMA one for the others up to eight, then the
+    tensor-core GEMMs; a tile policy keeps every size on the GEMMs."""
     prob = m.problem(M, 4096, I)
     assert m.mlp_plan(prob, m.MODE_INFER)["decode"] == plan
     assert m.mlp_plan(prob, m.MODE_FWD)["decode"] == plan
@@ -168,8 +170,8 @@ def test_cuda_core_stream_needs_its_token_rows_in_shared_memory(M, I, plan):
 def test_decode_at_llama3_8b_width(M, kind):
     """Llama-3-8B's gate/up and down shapes (H = 4096, I = 14336): four
     tokens on the CUDA-core stream (112 KiB of staged token rows), sixteen on
-    the warp-MMA stream, against the oracle and bitwise against a second
-    call; every output row checked."""
+    the warp-MMA stream (forced: two 8-token blocks), against the oracle and
+    bitwise against a second call; every output row checked."""
     H, I = 4096, 14336
     t = make_inputs(M, H, I, "swiglu", seed=35)
     d = dev_tensors(t)

@@ -314,7 +314,7 @@ def test_dwd_only_postact_kernel(act):
 def test_small_m_split_k(act, M):
     """Few tokens: the down projection (and dx) split K so that their few
     output tiles still use the whole GPU; the partial sums meet in fp32.
-    (1 and 16 tokens take the weight-streaming forward, then the split dx.)"""
+    (1 token takes the weight-streaming forward, then the split dx.)"""
     H, I = 512, 2048  # 2 output tiles per 128 rows, K = 2048 (forward), 4096 (gated dx)
     t = make_inputs(M, H, I, act, seed=12)
     got, bad, _ = run_gpu(dev_tensors(t), M, H, I, act, 1.125, 2.0, mode="recompute")

@@ -3,7 +3,7 @@ training forward and the backward (saved or recomputed preacts, bf16 or
 fp32-accumulated weight gradients), every activation.
 
 The launch plan makes size-dependent choices: the weight-streaming forward
-for 1-16 tokens (CUDA-core or warp-MMA stream), split-K for [M,H] outputs
+for 1-8 tokens (CUDA-core or warp-MMA stream), split-K for [M,H] outputs
 with few tiles, the one-launch gated forward, single-CTA or CTA-pair tiles.
 Hand-picked test shapes sit where their authors expected the boundaries;
 these are drawn at random (with a fixed seed) from ranges that straddle
