@@ -193,8 +193,9 @@ cudaError_t launch_decode_down(const void* a, const void* Wd, void* out, int M, 
 // token rows are read through the caches, so K is not limited.
 constexpr int DECODE_MMA_MAX_M = 16;
 // Tokens up to which the library takes the warp-MMA stream by itself: with
-// 9-16 tokens (two 8-token blocks) the tensor-core GEMMs measured faster
-// (73-75 against 81-83 us on Llama-3-8B's weights)
+// 9-16 tokens (two 8-token blocks) the stream measured no faster than the
+// tensor-core GEMMs (74.9-75.9 against 74.0-75.9 us on Llama-3-8B's
+// weights; 81-83 us before its down pass took two row tiles per warp)
 constexpr int DECODE_MMA_AUTO_M = 8;
 cudaError_t launch_decode_mma_act(const void* x, const void* Wg, const void* Wu, void* a, void* G,
                                   void* U, int M, int H, int I, int act, bool gated, float s,

@@ -1,8 +1,9 @@
 // Decode-sized forward (up to sixteen tokens): a weight stream whose dot
 // products run on the warp-level MMA (mma.sync m16n8k16, bf16 in, fp32
 // accumulate).  The library takes it for three to eight tokens; with 9-16
-// (two 8-token blocks, twice the token loads) the tensor-core GEMMs are
-// faster, and the 16-token instances run only when a test forces them.
+// (two 8-token blocks, twice the token loads) it is no faster than the
+// tensor-core GEMMs, and the 16-token instances run only when a test forces
+// them.
 //
 // With M <= 16 tokens the forward reads every weight once and does M
 // multiply-adds per weight element, so it is bound by HBM, not by any
@@ -24,11 +25,13 @@
 // 16 rows.
 //
 // Work.  A CTA owns 16 consecutive weight rows (of Wg and Wu for the gated
-// pass) and all of K; its S warps take the 64-wide k groups round-robin
-// (warp w: groups w, w + S, ...), with two groups in flight per warp
-// (registers double-buffered).  S is the most warps with which the whole
-// grid is resident at once (md_warps).  The warps' partial sums meet in shared
-// memory; the CTA's first warp applies the epilogue.  The token rows are
+// pass; 32, two 16-row tiles per warp, for the down pass with 16 tokens, so
+// that each token fragment feeds twice the weights: 36 -> 30 us for
+// Llama-3-8B's Wd) and all of K; its S warps take the 64-wide k groups
+// round-robin (warp w: groups w, w + S, ...), with two groups in flight per
+// warp (registers double-buffered).  S is the most warps with which the
+// whole grid is resident at once (md_warps).  The warps' partial sums meet
+// in shared memory; the CTA's first warp applies the epilogue.  The token rows are
 // read through L1/L2 (they are small and every CTA reads them); the weights
 // with no L1 allocation (each is read once).  The weights do not depend on
 // the previous kernel, so the first group's weights are requested before
@@ -55,7 +58,11 @@ constexpr int MD_MAX_WARPS = 16;
 // pass 8 (its two weight matrices need more than 128 with 16 tokens)
 template <int MODE>
 __host__ __device__ constexpr int md_max_threads() { return MODE == MD_GATED ? 256 : 512; }
-constexpr int MD_ROWS = 16;  // weight rows per CTA (the MMA's M)
+constexpr int MD_ROWS = 16;  // weight rows of one MMA tile (the MMA's M)
+// 16-row tiles per warp: two for the down pass with 16 tokens, so that each
+// token fragment it loads feeds twice the weights
+template <int MODE, int NT>
+__host__ __device__ constexpr int md_row_tiles() { return (MODE == MD_STORE && NT == 16) ? 2 : 1; }
 constexpr int MD_KG = 64;    // k per load group (two k-steps of 32)
 
 __device__ __forceinline__ uint4 ld_weights_v4(const void* p) {
@@ -85,11 +92,11 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int MODE, int NT>
+template <int MODE, int NT, int RT>
 struct MdGroup {
   static constexpr int NMAT = MODE == MD_GATED ? 2 : 1;
   static constexpr int NTB = NT / 8;  // 8-token blocks
-  uint4 w[NMAT][2][2];                // [matrix][row g, g + 8][k-step]
+  uint4 w[NMAT][RT][2][2];            // [matrix][16-row tile][row g, g + 8][k-step]
   uint4 t[NTB][2];                    // [token block][k-step]
 
   // the weights of the group starting at k0 (zeros past the rows or K)
@@ -102,11 +109,14 @@ struct MdGroup {
 #pragma unroll
       for (int a = 0; a < NMAT; ++a)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = row0 + g + 8 * h;
-          w[a][h][s] = (k < K && r < R) ? ld_weights_v4(W[a] + static_cast<size_t>(r) * K + k)
-                                        : make_uint4(0, 0, 0, 0);
-        }
+        for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int r = row0 + 16 * rt + g + 8 * h;
+            w[a][rt][h][s] = (k < K && r < R)
+                                 ? ld_weights_v4(W[a] + static_cast<size_t>(r) * K + k)
+                                 : make_uint4(0, 0, 0, 0);
+          }
     }
   }
 
@@ -125,19 +135,23 @@ struct MdGroup {
     }
   }
 
-  // acc[a][b] += the group's part of rows (g, g + 8) of matrix a times tokens of block b
-  __device__ __forceinline__ void mma(float (&acc)[NMAT][NTB][4]) const {
+  // acc[a][rt][b] += the group's part of rows (g, g + 8) of tile rt of
+  // matrix a times tokens of block b
+  __device__ __forceinline__ void mma(float (&acc)[NMAT][RT][NTB][4]) const {
 #pragma unroll
     for (int s = 0; s < 2; ++s)
 #pragma unroll
       for (int a = 0; a < NMAT; ++a)
 #pragma unroll
-        for (int b = 0; b < NTB; ++b) {
-          mma_16816(acc[a][b], w[a][0][s].x, w[a][1][s].x, w[a][0][s].y, w[a][1][s].y, t[b][s].x,
-                    t[b][s].y);
-          mma_16816(acc[a][b], w[a][0][s].z, w[a][1][s].z, w[a][0][s].w, w[a][1][s].w, t[b][s].z,
-                    t[b][s].w);
-        }
+        for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+          for (int b = 0; b < NTB; ++b) {
+            const uint4(&x)[2][2] = w[a][rt];
+            mma_16816(acc[a][rt][b], x[0][s].x, x[1][s].x, x[0][s].y, x[1][s].y, t[b][s].x,
+                      t[b][s].y);
+            mma_16816(acc[a][rt][b], x[0][s].z, x[1][s].z, x[0][s].w, x[1][s].w, t[b][s].z,
+                      t[b][s].w);
+          }
   }
 };
 
@@ -147,26 +161,29 @@ __global__ void __launch_bounds__(md_max_threads<MODE>()) k_decode_mma(
     const __nv_bfloat16* __restrict__ W1, __nv_bfloat16* __restrict__ out,
     __nv_bfloat16* __restrict__ o1, __nv_bfloat16* __restrict__ o2, int M, int R, int K, float s,
     int* status) {
-  using G = MdGroup<MODE, NT>;
+  constexpr int RT = md_row_tiles<MODE, NT>();
+  using G = MdGroup<MODE, NT, RT>;
   // the call's status word (the first kernel of the call clears it)
   if (status != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
   constexpr int NMAT = G::NMAT, NTB = G::NTB;
   constexpr int DEPTH = 2;  // load groups in flight per warp (deeper: no faster, more registers)
   // the warps' partial sums, [warp][matrix][token block][lane] x 4 floats
-  __shared__ float4 part[md_max_threads<MODE>() / 32][NMAT][NTB][32];
+  __shared__ float4 part[md_max_threads<MODE>() / 32][NMAT][RT][NTB][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  const int row0 = blockIdx.x * MD_ROWS;
+  const int row0 = blockIdx.x * MD_ROWS * RT;
   const __nv_bfloat16* const W[2] = {W0, W1};
   const int ngroups = (K + MD_KG - 1) / MD_KG;
 
-  float acc[NMAT][NTB][4];
+  float acc[NMAT][RT][NTB][4];
 #pragma unroll
   for (int a = 0; a < NMAT; ++a)
 #pragma unroll
-    for (int b = 0; b < NTB; ++b)
+    for (int rt = 0; rt < RT; ++rt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[a][b][e] = 0.f;
+      for (int b = 0; b < NTB; ++b)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[a][rt][b][e] = 0.f;
 
   // groups warp, warp + nwarps, ... in a ring of DEPTH register buffers
   G buf[DEPTH];
@@ -201,53 +218,59 @@ __global__ void __launch_bounds__(md_max_threads<MODE>()) k_decode_mma(
 #pragma unroll
   for (int a = 0; a < NMAT; ++a)
 #pragma unroll
-    for (int b = 0; b < NTB; ++b)
-      part[warp][a][b][lane] = make_float4(acc[a][b][0], acc[a][b][1], acc[a][b][2], acc[a][b][3]);
+    for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+      for (int b = 0; b < NTB; ++b)
+        part[warp][a][rt][b][lane] = make_float4(acc[a][rt][b][0], acc[a][rt][b][1],
+                                                 acc[a][rt][b][2], acc[a][rt][b][3]);
   __syncthreads();
   if (warp != 0) return;
   // the CTA's sums, in the accumulator layout: element (h, e) of lane
-  // (g, q) is row g + 8h, token 2q + e of the block
-  float y[NMAT][NTB][4];
-#pragma unroll
-  for (int a = 0; a < NMAT; ++a)
-#pragma unroll
-    for (int b = 0; b < NTB; ++b) {
-      float4 v = part[0][a][b][lane];
-      for (int w2 = 1; w2 < nwarps; ++w2) {
-        const float4 u = part[w2][a][b][lane];
-        v.x += u.x;
-        v.y += u.y;
-        v.z += u.z;
-        v.w += u.w;
-      }
-      y[a][b][0] = v.x;
-      y[a][b][1] = v.y;
-      y[a][b][2] = v.z;
-      y[a][b][3] = v.w;
-    }
+  // (g, q) is row 16 rt + g + 8h, token 2q + e of the block
   const int g = lane >> 2, q = lane & 3;
 #pragma unroll
-  for (int b = 0; b < NTB; ++b)
+  for (int rt = 0; rt < RT; ++rt) {
+    float y[NMAT][NTB][4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int a = 0; a < NMAT; ++a)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int r = row0 + g + 8 * h, m = 8 * b + 2 * q + e;
-        if (r >= R || m >= M) continue;
-        const size_t o = static_cast<size_t>(m) * R + r;
-        const float y0 = y[0][b][2 * h + e];
-        if constexpr (MODE == MD_STORE) {
-          out[o] = __float2bfloat16_rn(y0);
-        } else if constexpr (MODE == MD_GATED) {
-          const float y1 = y[NMAT - 1][b][2 * h + e];
-          out[o] = __float2bfloat16_rn(s * act_f<ACT>(y0) * y1);
-          if (o1) o1[o] = __float2bfloat16_rn(y0);
-          if (o2) o2[o] = __float2bfloat16_rn(y1);
-        } else {
-          out[o] = __float2bfloat16_rn(s * act_f<ACT>(y0));
-          if (o1) o1[o] = __float2bfloat16_rn(y0);
+      for (int b = 0; b < NTB; ++b) {
+        float4 v = part[0][a][rt][b][lane];
+        for (int w2 = 1; w2 < nwarps; ++w2) {
+          const float4 u = part[w2][a][rt][b][lane];
+          v.x += u.x;
+          v.y += u.y;
+          v.z += u.z;
+          v.w += u.w;
         }
+        y[a][b][0] = v.x;
+        y[a][b][1] = v.y;
+        y[a][b][2] = v.z;
+        y[a][b][3] = v.w;
       }
+#pragma unroll
+    for (int b = 0; b < NTB; ++b)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int r = row0 + 16 * rt + g + 8 * h, m = 8 * b + 2 * q + e;
+          if (r >= R || m >= M) continue;
+          const size_t o = static_cast<size_t>(m) * R + r;
+          const float y0 = y[0][b][2 * h + e];
+          if constexpr (MODE == MD_STORE) {
+            out[o] = __float2bfloat16_rn(y0);
+          } else if constexpr (MODE == MD_GATED) {
+            const float y1 = y[NMAT - 1][b][2 * h + e];
+            out[o] = __float2bfloat16_rn(s * act_f<ACT>(y0) * y1);
+            if (o1) o1[o] = __float2bfloat16_rn(y0);
+            if (o2) o2[o] = __float2bfloat16_rn(y1);
+          } else {
+            out[o] = __float2bfloat16_rn(s * act_f<ACT>(y0));
+            if (o1) o1[o] = __float2bfloat16_rn(y0);
+          }
+        }
+  }
 }
 
 // Warps per CTA: the most (up to the kernel's bound and the k groups) with
@@ -279,7 +302,8 @@ int md_warps(int blocks, int ngroups) {
 template <int ACT, int MODE, int NT>
 cudaError_t launch_md(const void* T, const void* W0, const void* W1, void* out, void* o1, void* o2,
                       int M, int R, int K, float s, cudaStream_t stream, bool pdl, int* status) {
-  const int blocks = (R + MD_ROWS - 1) / MD_ROWS;
+  constexpr int rows = MD_ROWS * md_row_tiles<MODE, NT>();
+  const int blocks = (R + rows - 1) / rows;
   const int ngroups = (K + MD_KG - 1) / MD_KG;
   const int warps = md_warps<ACT, MODE, NT>(blocks, ngroups);
   cudaLaunchConfig_t cfg = {};
