@@ -48,10 +48,19 @@
  *     mlp_workspace_size(p, mode) bytes, 256-byte aligned.  Its first 1 KB
  *     holds the device status word, the tile-scheduler counters and the
  *     one-launch gated forward's per-block counts; every call clears it on
- *     the stream before its kernels run.  Calls that share one workspace
- *     must be ordered (same stream, or synchronised).
+ *     the stream before its kernels run (a decode weight stream, which uses
+ *     no counters, clears only the status word, in its first kernel).
+ *     Calls that share one workspace must be ordered (same stream, or
+ *     synchronised).
  *   - Device-side errors (a bounded wait that expired) are recorded in the
  *     workspace status word; read it with mlp_device_status.
+ *   - Determinism: two calls with the same inputs, problem, mode and tile
+ *     policy write bitwise-identical outputs, except where the call splits
+ *     a sum over K across work units (mlp_plan's out_split or wgrad_split
+ *     above 1).  Those fp32 partial sums are added (in the workspace, or in
+ *     the caller's fp32 weight gradients) in the order the units finish, so
+ *     such outputs can differ in their last bits from one call to the next.
+ *     The FP8 amax records are maxima and do not depend on that order.
  */
 #ifndef MLP_GB300_H
 #define MLP_GB300_H
