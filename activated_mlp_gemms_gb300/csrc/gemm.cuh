@@ -384,18 +384,17 @@ __device__ __forceinline__ void dact_rows_to_lanes(const EpiWarp& e, uint4 (&g)[
 // while chunk c is computed; the caller has already loaded chunk `cb` into
 // (pg, pu) before waiting for the accumulator.  Each chunk's preacts pass
 // through the staging boxes to one row per lane before its outputs are
-// staged there (measured back to back, two builds, outputs bitwise equal: 2.7-3.3 %
-// off the derivative GEMM on the 4096- and 2048-wide SwiGLU shapes, 2.8 %
-// off the ReLU^2 backward, Llama-3-8B's unchanged).  In-place outputs are
-// safe: every element is read (global load) before the TMA store of its
-// chunk is issued, and chunks do not overlap.
+// staged there (measured back to back, two builds, outputs bitwise equal:
+// 2.7-3.3 % off the derivative GEMM on the 4096- and 2048-wide SwiGLU
+// shapes, 2.8 % off the ReLU^2 backward, Llama-3-8B's unchanged).  In-place
+// outputs are safe: every element is read (global load) before the TMA
+// store of its chunk is issued, and chunks do not overlap.
 template <int ACT, bool GATED>
 __device__ __forceinline__ void epi_dact(const Params& p, const EpiUnit& P, const EpiWarp& e,
                                          uint32_t tb, int col0, int cb, int ce, uint4 (&pg)[4],
                                          uint4 (&pu)[4]) {
   const float s = p.scale;
   const float sr = s * e.rs;
-  const int row = e.row0 + e.lane;
   constexpr int NOUT = GATED ? 3 : 2;
 #pragma unroll 1
   for (int c = cb; c < ce; c += 32) {
@@ -429,7 +428,7 @@ __device__ __forceinline__ void epi_dact(const Params& p, const EpiUnit& P, cons
           // time in fp32x2 instructions; each lane rounds as the scalar code
           // would, so the results are bitwise the same (measured 1.5-2 % off
           // dgated's time)
-          {
+          {  // (scope of the packed temporaries)
             const uint64_t half2 = f2_pack(0.5f, 0.5f), one2 = f2_pack(1.f, 1.f);
             const uint64_t g2 = f2_pack(gg.x, gg.y);
             const float2 uu = unpack_bf16x2(uw[j]);
