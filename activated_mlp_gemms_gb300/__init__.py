@@ -7,6 +7,9 @@ streams.  The functions carry the names of the C ABI (include/mlp.h):
     mlp_workspace_size, mlp_fwd, mlp_fwd_infer, mlp_bwd, mlp_bwd_recompute,
     mlp_status_string, mlp_device_status, mlp_version
 
+and mlp_func (module `autograd`) is the same forward and backward as one
+differentiable PyTorch function.
+
 Tensors are CUDA, contiguous, bf16 (fp32 for accumulated weight gradients),
 with x [M,H], Wg/Wu [I,H], Wd [H,I].  A missing library raises at the first
 call: there is no CPU fallback.
@@ -427,3 +430,8 @@ def mlp_debug_set_flags(flags: int) -> None:
     DEBUG_DECODE_FMA / DEBUG_DECODE_MMA force the decode-sized forward onto
     the CUDA-core or the warp-MMA weight stream."""
     _check(lib().mlp_debug_set_flags(int(flags)), "mlp_debug_set_flags")
+
+
+from .autograd import mlp_func  # noqa: E402  (the differentiable form of mlp_fwd / mlp_bwd)
+
+__all__.append("mlp_func")
