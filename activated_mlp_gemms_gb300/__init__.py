@@ -432,6 +432,6 @@ def mlp_debug_set_flags(flags: int) -> None:
     _check(lib().mlp_debug_set_flags(int(flags)), "mlp_debug_set_flags")
 
 
-from .autograd import mlp_func  # noqa: E402  (the differentiable form of mlp_fwd / mlp_bwd)
+from .autograd import mlp_block_func, mlp_func  # noqa: E402  (differentiable forms)
 
-__all__.append("mlp_func")
+__all__ += ["mlp_func", "mlp_block_func"]

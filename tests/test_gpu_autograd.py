@@ -170,3 +170,48 @@ def test_mlp_func_empty_batch():
     out.backward(torch.empty_like(out))
     assert x.grad.shape == x.shape
     assert torch.count_nonzero(W1.grad) == 0 and torch.count_nonzero(Wd.grad) == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("act,gm,dm,fuse", [("swiglu", 1.125, 2.0, False), ("relu_sq", 1.0, 1.0, True)])
+def test_mlp_block_func_equals_the_entry_points(act, gm, dm, fuse):
+    d = _inputs(2, 1024, 2048, 2816, act, seed=17)
+    B, S, H = d["x"].shape
+    x2 = d["x"].reshape(-1, H)
+    M, I = x2.shape[0], d["Wd"].shape[1]
+    gated = act in m.GATED_ACTS
+    lam, post, eps = 1.1 ** 0.5, 0.8, 2.0 ** -7
+    prob = m.problem(M, H, I, act, gm, dm)
+    blk = m.block(lam, post, eps)
+    assert m.mlp_plan(prob, m.MODE_FWD)["out_split"] == 1
+    bwd = m.mlp_plan(prob, m.MODE_BWD, fuse)
+    assert bwd["out_split"] == 1 and bwd["wgrad_split"] <= 1
+    g = torch.Generator(device="cpu").manual_seed(6)
+    prev = {k: (1e-3 * torch.randn(d[k].shape, generator=g)).cuda()
+            for k in ("Wg", "Wu", "Wd") if d[k] is not None}
+    y = torch.empty(M, H, dtype=BF, device="cuda")
+    G = torch.empty(M, I, dtype=BF, device="cuda")
+    U = torch.empty_like(G) if gated else None
+    rstd, _ = m.mlp_block_fwd(prob, blk, x2, d["Wg"], d["Wu"], d["Wd"], y, G, U)
+    dx = torch.empty_like(x2)
+    ref_w = [None if d[k] is None else prev[k].clone() if fuse else torch.empty_like(d[k])
+             for k in ("Wg", "Wu", "Wd")]
+    m.mlp_block_bwd(prob, blk, d["dout"].reshape(-1, H), x2, d["Wg"], d["Wu"], d["Wd"], G, U,
+                    rstd, dx, *ref_w, fuse_grad_accum=fuse)
+    torch.cuda.synchronize()
+
+    x, ws = _leaves(d, (True, True, True, True))
+    if fuse:
+        for w, k in zip(ws, ("Wg", "Wu", "Wd")):
+            if w is not None:
+                w.main_grad = prev[k].clone()
+    out = m.mlp_block_func(x, *ws, act, gm, dm, lam, post, eps, fuse_grad_accum=fuse)
+    assert torch.equal(out.detach().view(-1, H), y)
+    out.backward(d["dout"])
+    assert torch.equal(x.grad.view(-1, H), dx)
+    for w, r in zip(ws, ref_w):
+        if w is None:
+            continue
+        assert torch.equal(w.main_grad if fuse else w.grad, r)
+        if fuse:
+            assert w.grad is None
