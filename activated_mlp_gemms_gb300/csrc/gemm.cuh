@@ -938,46 +938,6 @@ __device__ __forceinline__ void epi_plain(const Params& p, const EpiUnit& P, con
   }
 }
 
-// EPI_STORE_BF16 with the block's residual (in0): D = alpha * residual +
-// acc.  The residual goes as the derivative epilogues' preacts do: loaded
-// row-coalesced a chunk ahead (the caller fetched chunk `cb` into pr before
-// waiting for the accumulator) and moved to one row per lane through the
-// staging box, which the chunk's output then reuses.
-__device__ __forceinline__ void epi_store_resid(const Params& p, const EpiUnit& P,
-                                                const EpiWarp& e, uint32_t tb, int col0, int cb,
-                                                int ce, uint4 (&pr)[4]) {
-#pragma unroll 1
-  for (int c = cb; c < ce; c += 32) {
-    const int col = col0 + c;
-    if (col >= P.N) break;
-    uint4 nr[4], unused[4];
-    if (c + 32 < ce) dact_load_rows<false>(P, e.row0, e.lane, col + 32, nr, unused);
-    uint32_t d[32];
-    __syncwarp();
-    tmem_ld32(tb + c, d);
-    tmem_wait_ld();
-    staging_acquire(e);
-    dact_rows_to_lanes<false>(e, pr, unused);
-    uint32_t q[16];
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const uint32_t rw[4] = {pr[v].x, pr[v].y, pr[v].z, pr[v].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = unpack_bf16x2(rw[j]);
-        q[4 * v + j] = pack_bf16x2(P.alpha * f.x + __uint_as_float(d[8 * v + 2 * j]),
-                                   P.alpha * f.y + __uint_as_float(d[8 * v + 2 * j + 1]));
-      }
-    }
-    stage_bf16(e.stg, e.lane, q);
-    flush_chunk<1, 2048, false>(p, P, e, col);
-    if (c + 32 < ce) {
-#pragma unroll
-      for (int v = 0; v < 4; ++v) pr[v] = nr[v];
-    }
-  }
-}
-
 // EPI_FWD_FUSED: the producer thread of a down unit waits (bounded) until
 // every gate/up tile of its 256-row block is stored, then orders its TMA
 // loads of the postact after that.  False on expiry or abort.
@@ -1567,9 +1527,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
         } else if (e.rows_ok) {
           dact_load_rows<EPI == EPI_DGATED>(P, e.row0, lane, col0 + cb, pg, pu);
         }
-      } else if constexpr (EPI == EPI_STORE_BF16) {
-        // the block's residual: its first chunk, too, before the accumulator
-        if (P.in0 != nullptr && e.rows_ok) dact_load_rows<false>(P, e.row0, lane, col0 + cb, pg, pu);
       }
       if (!mbar_wait<PAIR>(bar_s(TFULL + acc), aphase, lim, abort_flag)) {
         record_timeout(p, abort_flag);
@@ -1604,8 +1561,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_mlp_gemm(const __grid_consta
         } else if constexpr (EPI == EPI_DGRAD_F8_RECOMP) {
           epi_recomp_f8_dh(P, e, tb, col0, cb, dd);
         } else {
-          if (EPI == EPI_STORE_BF16 && P.in0 != nullptr) epi_store_resid(p, P, e, tb, col0, cb, ce, pg);
-          else epi_plain<EPI>(p, P, e, tb, col0, cb, ce);
+          epi_plain<EPI>(p, P, e, tb, col0, cb, ce);
         }
       }
       tc_fence_before();
